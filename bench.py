@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark per-cycle draft step on GB300; prints one JSON line.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. Markov block draft, full-vocab 27B-shaped lane (num_reqs x k=15 x vocab 248320,
+     rank 256, bf16 markov weights, fp32 base logits, identity d2t) -- one graph launch
+  2. 2048 confidence probes (2 per cycle x 1024 cycles), 7424-wide Q8_0, threshold 0.5
+  3. the four M=7 fp16 weight-stationary projections of a Qwen3-8B-shaped draft
+     (K,N) = (4096,4096), (4096,1024), (4096,12288), (12288,4096)
+
+value = microseconds per step (lower is better), device time from CUDA events around
+each step's work; L2 is flushed (256 MiB write) before every step, outside the events.
+`e2e` times the same step through the public API with the step's inputs copied from
+pinned host memory and its outputs copied back, inside the events.  `roofline` is for
+the Markov kernel (the dominant one): algorithmic bytes per launch / mean launch time.
+
+--impl reference times the CPU oracle on the host (the reference arm of this method).
+With torchrun (--gpus N > 1) every rank runs an independent replica (the path has no
+cross-GPU exchange); the timed region is bracketed by barriers and the max over ranks
+is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+if REPO not in sys.path:
+    sys.path.insert(0, REPO)
+
+from dspark_draft_sampling_gb300 import synth  # noqa: E402
+
+METRIC = "Markov draft-step µs and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "us"
+N_PROBES = 2048
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- workload ---------------
+def make_workload(num_reqs: int, seed: int = 0):
+    mk = synth.markov_config("full_vocab_27b", num_reqs=num_reqs, seed=seed)
+    pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=seed)
+    ws = [synth.ws_inputs(7, N, K, seed=seed + K + N) for (K, N) in synth.WS_SHAPES]
+    return mk, pr, ws
+
+
+def markov_bytes(B, k, V, R, d2t=False):
+    """Algorithmic bytes of one draft: markov_w2 re-read at every position, the base rows,
+    the gathered markov_w1 rows and the ids."""
+    return k * (V * R * 2 + B * V * 4 + B * R * 2) + B * k * 8 + (V * 4 if d2t else 0)
+
+
+def probe_bytes(n, K):
+    return n * (K * 4 + 8) + (K // 32) * 34
+
+
+def ws_bytes(M, N, K):
+    return N * K * 2 + M * K * 2 + M * N * 2
+
+
+def config_dict(B):
+    k, V, R = 15, 248320, 256
+    return {
+        "workload": (f"dspark draft step: Markov draft full-vocab 27B lane (num_reqs={B}, k={k}, "
+                     f"vocab={V}, rank={R}, bf16 markov_w1/w2, fp32 base, identity d2t) + "
+                     f"{N_PROBES} Q8_0 confidence probes (K=7424, threshold 0.5) + 4 M=7 fp16 "
+                     "weight-stationary matvecs (K,N)=(4096,4096),(4096,1024),(4096,12288),"
+                     "(12288,4096)"),
+        "num_reqs": B, "k": k, "vocab": V, "rank": R, "probes": N_PROBES, "probe_K": 7424,
+        "ws_M": 7, "ws_shapes_KN": [list(s) for s in synth.WS_SHAPES],
+        "l2": "flushed before every step (256 MiB write, outside the timed events)",
+        "timing": "CUDA events on the launch stream around each step's work; mean over steps",
+        "parallelism": "replicas",
+    }
+
+
+# ---------------------------------------------------------------- helpers ----------------
+def read_peak():
+    p = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def markov_source_hash():
+    h = hashlib.sha256()
+    for f in ("markov.cu", "common.cuh"):
+        with open(os.path.join(REPO, "dspark_draft_sampling_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(B):
+    """DRAM bytes per Markov launch from the committed ncu summary, if it was taken on the
+    current kernel source and this num_reqs; else None."""
+    p = os.path.join(REPO, "profiles", "markov_draft_full_vocab_27b.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not src or src.group(1) != markov_source_hash():
+        return None
+    m = re.search(rf"traffic_bytes_per_launch\[num_reqs={B}\]:\s*([0-9.eE+]+)", text)
+    return float(m.group(1)) if m else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm ----------------
+def run_gpu(args, rank, world):
+    import torch
+
+    from dspark_draft_sampling_gb300 import api
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    api.load_library()
+    B = args.num_reqs
+    mk, pr, ws = make_workload(B, seed=0)
+    k, V, R = mk["k"], mk["vocab"], mk["rank"]
+
+    # resident inputs
+    base = torch.from_numpy(mk["base"]).to(dev)
+    w1 = torch.from_numpy(mk["w1"].view(np.int16)).to(dev)
+    w2 = torch.from_numpy(mk["w2"].view(np.int16)).to(dev)
+    prev = torch.from_numpy(mk["prev0"].copy()).to(dev)
+    out_ids = torch.empty((B, k), dtype=torch.int64, device=dev)
+    wsp = api.new_markov_workspace(B, k, V, R, dev)
+    plan = api.MarkovPlan(base, w1, w2, None, prev, out_ids, wsp)
+    wq = torch.from_numpy(pr["wq"]).to(dev)
+    hid = torch.from_numpy(pr["hidden"]).to(dev)
+    z = torch.empty(N_PROBES, dtype=torch.float32, device=dev)
+    gate = torch.empty(N_PROBES, dtype=torch.int32, device=dev)
+    Ws = [torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
+    Xs = [torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
+    Ys = [torch.empty((7, w["N"]), dtype=torch.float16, device=dev) for w in ws]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_work():
+        plan.launch(stream)
+        api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
+                       stream=stream)
+        for W, X, Y in zip(Ws, Xs, Ys):
+            api.ws_matvec(W, X, out=Y, stream=stream)
+
+    kernels_per_step = 1 + 1 + len(Ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step_work()
+    torch.cuda.synchronize()
+    if api.markov_status(wsp) != 0:
+        raise RuntimeError("markov draft reported a device-side error during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    clocks = ClockSampler(dev.index)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        e = ev[s]
+        e[0].record(stream)
+        plan.launch(stream)
+        e[1].record(stream)
+        api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
+                       stream=stream)
+        e[2].record(stream)
+        for W, X, Y in zip(Ws, Xs, Ys):
+            api.ws_matvec(W, X, out=Y, stream=stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    step_ms = [ev[s][0].elapsed_time(ev[s][3]) for s in range(args.steps)]
+    markov_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    probe_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    ws_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(args.steps)]
+    if api.markov_status(wsp) != 0:
+        raise RuntimeError("markov draft reported a device-side error")
+    ms_step = statistics.mean(step_ms)
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        base_h = torch.from_numpy(mk["base"]).pin_memory()
+        prev_h = torch.from_numpy(mk["prev0"].copy()).pin_memory()
+        hid_h = torch.from_numpy(pr["hidden"]).pin_memory()
+        X_h = [torch.from_numpy(w["X"].view(np.int16)).pin_memory() for w in ws]
+        ids_h = torch.empty((B, k), dtype=torch.int64).pin_memory()
+        gate_h = torch.empty(N_PROBES, dtype=torch.int32).pin_memory()
+        Y_h = [torch.empty((7, w["N"]), dtype=torch.float16).pin_memory() for w in ws]
+        h2d = (base_h.numel() * 4 + prev_h.numel() * 8 + hid_h.numel() * 4
+               + sum(x.numel() * 2 for x in X_h))
+        d2h = ids_h.numel() * 8 + gate_h.numel() * 4 + sum(y.numel() * 2 for y in Y_h)
+        Xs16 = [x.view(torch.int16) for x in Xs]
+
+        def e2e_step():
+            base.copy_(base_h, non_blocking=True)
+            prev.copy_(prev_h, non_blocking=True)
+            hid.copy_(hid_h, non_blocking=True)
+            for xd, xh in zip(Xs16, X_h):
+                xd.copy_(xh, non_blocking=True)
+            step_work()
+            ids_h.copy_(out_ids, non_blocking=True)
+            gate_h.copy_(gate, non_blocking=True)
+            for yh, yd in zip(Y_h, Ys):
+                yh.copy_(yd, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            flush.fill_(2)
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = []
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+        e2e = {"value": statistics.mean(e2e_ms) * 1000.0, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    plan.close()
+
+    res = dict(ms_step=ms_step, wall=wall, markov_ms=statistics.mean(markov_ms),
+               probe_ms=statistics.mean(probe_ms), ws_ms=statistics.mean(ws_ms),
+               clocks=clk, e2e=e2e, kernels=kernels_per_step * args.steps,
+               markov_ms_min=min(markov_ms))
+    return res
+
+
+def cpu_oracle_step(mk, pr, ws):
+    """One step of the oracle on the host: the same three parts, single-threaded fp64."""
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.markov_draft(mk["base"], mk["w1"], mk["w2"], mk["d2t"], mk["prev0"])
+    t1 = time.perf_counter()
+    oracle.conf_probe(pr["wq"], pr["hidden"], pr["bias"], pr["threshold"])
+    t2 = time.perf_counter()
+    for w in ws:
+        oracle.ws_matvec(w["W"], w["X"])
+    t3 = time.perf_counter()
+    return t3 - t0, (t1 - t0, t2 - t1, t3 - t2)
+
+
+def cpu_baseline(B):
+    import oracle
+
+    oracle.build()
+    mk, pr, ws = make_workload(B, seed=0)
+    total, parts = cpu_oracle_step(mk, pr, ws)
+    return {"value": total * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": ("one full step of the same workload (Markov draft + 2048 probes + 4 WS "
+                       "matvecs), single-threaded fp64 C oracle"),
+            "parts_s": {"markov": parts[0], "probe": parts[1], "ws": parts[2]},
+            "host_cpus": os.cpu_count()}
+
+
+# ---------------------------------------------------------------- main -------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--num-reqs", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus))
+    B = args.num_reqs
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+
+        oracle.build()
+        mk, pr, ws = make_workload(B, seed=0)
+        for _ in range(args.warmup):
+            cpu_oracle_step(mk, pr, ws)
+        times = [cpu_oracle_step(mk, pr, ws)[0] for _ in range(args.steps)]
+        us = statistics.mean(times) * 1e6
+        line = {
+            "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1000.0, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(B),
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step is one full step of the workload, "
+                                       "single-threaded fp64 C oracle"},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return 0
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    res = run_gpu(args, rank, world)
+
+    ms_step = res["ms_step"]
+    markov_ms = res["markov_ms"]
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_step, markov_ms, res["wall"]], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, markov_ms, wall = (float(x) for x in t.tolist())
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    k, V, R = 15, 248320, 256
+    mb = markov_bytes(B, k, V, R)
+    pb = probe_bytes(N_PROBES, synth.PROBE_K)
+    wb = sum(ws_bytes(7, N, K) for (K, N) in synth.WS_SHAPES)
+    peak, peak_kind = read_peak()
+    achieved = mb / (markov_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(B)
+    line = {
+        "metric": METRIC,
+        "value": ms_step * 1000.0 / world,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64; shapes and distributions of the pages' lanes)",
+        "config": config_dict(B),
+        "roofline": {"kernel": "markov_draft_kernel (k=15 positions, one launch)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": mb,
+                     "traffic": traffic},
+        "parts": {
+            "markov_draft_us": markov_ms * 1000.0,
+            "markov_us_per_position": markov_ms * 1000.0 / k,
+            "markov_GBps": achieved,
+            "conf_probe_batch_us": res["probe_ms"] * 1000.0,
+            "conf_probe_us_per_probe": res["probe_ms"] * 1000.0 / N_PROBES,
+            "conf_probe_GBps": pb / (res["probe_ms"] * 1e-3) / 1e9,
+            "ws_matvec_4_shapes_us": res["ws_ms"] * 1000.0,
+            "ws_matvec_GBps": wb / (res["ws_ms"] * 1e-3) / 1e9,
+        },
+        "gpu_launches": res["kernels"],
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "wall_s_timed_region": res["wall"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(B)
+    elif not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(B)
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

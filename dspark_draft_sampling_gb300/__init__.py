@@ -1,0 +1,16 @@
+"""libdspark: GB300-native DSpark per-cycle draft step (Markov block draft,
+Q8_0 confidence probe, weight-stationary small-M matvec).
+
+Every step of the path runs in the CUDA kernels of ``libdspark.so``; this package
+only marshals torch tensors into the C ABI declared in ``include/dspark.h``.
+"""
+from .api import (  # noqa: F401
+    DsparkError,
+    MarkovPlan,
+    conf_probe,
+    lib_path,
+    load_library,
+    markov_draft,
+    markov_workspace_bytes,
+    ws_matvec,
+)

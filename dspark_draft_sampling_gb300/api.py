@@ -1,0 +1,248 @@
+"""Thin ctypes binding of libdspark (``include/dspark.h``) over torch CUDA tensors.
+
+Argument marshalling only: shapes, dtypes and device pointers are checked and passed
+to the C ABI; every arithmetic step runs in the library's CUDA kernels.  There is no
+CPU fallback: if ``libdspark.so`` is missing or a call fails, a ``DsparkError`` is
+raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "INDEX"}
+DSPARK_OK, DSPARK_ERR_INVALID, DSPARK_ERR_UNSUPPORTED = 0, 1, 2
+DSPARK_ERR_CUDA, DSPARK_ERR_TIMEOUT, DSPARK_ERR_INDEX = 3, 4, 5
+
+# Every symbol the header declares, with (restype, argtypes).
+_P, _I, _U, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "dspark_last_error": (ctypes.c_char_p, []),
+    "dspark_version": (ctypes.c_char_p, []),
+    "dspark_markov_workspace_bytes": (_Z, [_I, _I, _I, _I]),
+    "dspark_markov_draft": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "dspark_markov_status": (_I, [_P, _P]),
+    "dspark_markov_draft_debug": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _U, _U, _P]),
+    "dspark_markov_plan_create": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z,
+                                       ctypes.POINTER(_P)]),
+    "dspark_markov_plan_launch": (_I, [_P, _P]),
+    "dspark_markov_plan_destroy": (None, [_P]),
+    "dspark_conf_probe": (_I, [_P, _P, _F, _F, _I, _I, _P, _P, _P]),
+    "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"libdspark {_STATUS_NAMES.get(status, status)}: {message}")
+
+
+def lib_path() -> str:
+    return _build.lib_file()
+
+
+def load_library(path: str | None = None):
+    """Load libdspark.so (built by ``dspark_draft_sampling_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or lib_path()
+        if not os.path.exists(p):
+            raise DsparkError(DSPARK_ERR_CUDA, f"{p} not found; build it with "
+                              "`python -m dspark_draft_sampling_gb300.build`")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _err(lib) -> str:
+    msg = lib.dspark_last_error()
+    return msg.decode(errors="replace") if msg else ""
+
+
+def _check(lib, status: int):
+    if status != DSPARK_OK:
+        raise DsparkError(status, _err(lib))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t, name: str, *, dtypes=None, itemsize=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise ValueError(f"{name} must have {itemsize}-byte elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_BITS16 = (torch.bfloat16, torch.int16, torch.float16)
+
+
+def markov_workspace_bytes(num_reqs: int, k: int, vocab: int, rank: int) -> int:
+    return int(load_library().dspark_markov_workspace_bytes(num_reqs, k, vocab, rank))
+
+
+def new_markov_workspace(num_reqs: int, k: int, vocab: int, rank: int, device=None):
+    n = markov_workspace_bytes(num_reqs, k, vocab, rank)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def markov_draft(base, w1, w2, d2t, prev, *, out_ids=None, workspace=None, dbg_logits=None,
+                 dbg_bias=None, stream=None):
+    """k-step Markov block draft.  base [B,k,V] fp32, w1/w2 [V,R] bf16, d2t [V] int32 or
+    None, prev [B] int64 (updated in place).  Returns out_ids [B,k] int64 (target ids)."""
+    lib = load_library()
+    if base.dim() != 3:
+        raise ValueError("base must be [num_reqs, k, vocab]")
+    B, k, V = base.shape
+    R = w2.shape[1] if w2.dim() == 2 else -1
+    if out_ids is None:
+        out_ids = torch.empty((B, k), dtype=torch.int64, device=base.device)
+    if workspace is None:
+        workspace = new_markov_workspace(B, k, V, R, base.device)
+    st = lib.dspark_markov_draft(
+        _ptr(base, "base", dtypes=(torch.float32,)),
+        _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16),
+        _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
+        _ptr(d2t, "d2t", dtypes=(torch.int32,), allow_none=True),
+        _ptr(prev, "prev", dtypes=(torch.int64,)),
+        B, k, V, R,
+        _ptr(out_ids, "out_ids", dtypes=(torch.int64,)),
+        _ptr(dbg_logits, "dbg_logits", dtypes=(torch.float32,), allow_none=True),
+        _ptr(dbg_bias, "dbg_bias", dtypes=(torch.float32,), allow_none=True),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(lib, st)
+    return out_ids
+
+
+def markov_status(workspace, stream=None) -> int:
+    """Synchronize and return the device status of the last draft on ``workspace``
+    (0 = OK, DSPARK_ERR_INDEX, DSPARK_ERR_TIMEOUT)."""
+    lib = load_library()
+    return int(lib.dspark_markov_status(_ptr(workspace, "workspace"), _stream(stream)))
+
+
+def markov_draft_debug(base, w1, w2, d2t, prev, out_ids, workspace, *, missing_arrivals: int,
+                       timeout_us: int, stream=None):
+    """Fault-injection hook: see dspark_markov_draft_debug in dspark.h."""
+    lib = load_library()
+    B, k, V = base.shape
+    R = w2.shape[1]
+    st = lib.dspark_markov_draft_debug(
+        _ptr(base, "base"), _ptr(w1, "markov_w1"), _ptr(w2, "markov_w2"),
+        _ptr(d2t, "d2t", allow_none=True), _ptr(prev, "prev"), B, k, V, R,
+        _ptr(out_ids, "out_ids"), _ptr(workspace, "workspace"), workspace.numel(),
+        int(missing_arrivals), int(timeout_us), _stream(stream))
+    _check(lib, st)
+
+
+class MarkovPlan:
+    """A Markov draft recorded once into a CUDA graph; ``launch()`` replays it."""
+
+    def __init__(self, base, w1, w2, d2t, prev, out_ids=None, workspace=None):
+        self._lib = lib = load_library()
+        B, k, V = base.shape
+        R = w2.shape[1]
+        if out_ids is None:
+            out_ids = torch.empty((B, k), dtype=torch.int64, device=base.device)
+        if workspace is None:
+            workspace = new_markov_workspace(B, k, V, R, base.device)
+        # keep the tensors alive for the plan's lifetime
+        self.tensors = (base, w1, w2, d2t, prev, out_ids, workspace)
+        self.out_ids, self.workspace = out_ids, workspace
+        handle = ctypes.c_void_p()
+        st = lib.dspark_markov_plan_create(
+            _ptr(base, "base", dtypes=(torch.float32,)),
+            _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16),
+            _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
+            _ptr(d2t, "d2t", dtypes=(torch.int32,), allow_none=True),
+            _ptr(prev, "prev", dtypes=(torch.int64,)), B, k, V, R,
+            _ptr(out_ids, "out_ids", dtypes=(torch.int64,)),
+            _ptr(workspace, "workspace"), workspace.numel(), ctypes.byref(handle))
+        _check(lib, st)
+        self._handle = handle
+
+    def launch(self, stream=None):
+        _check(self._lib, self._lib.dspark_markov_plan_launch(self._handle, _stream(stream)))
+        return self.out_ids
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            self._lib.dspark_markov_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gate_out=None,
+               stream=None):
+    """Q8_0 confidence probes.  wq uint8 [K/32*34], hidden fp32 [n, K] (or [K]).
+    Returns (logit_out [n] fp32, gate_out [n] int32)."""
+    lib = load_library()
+    if hidden.dim() == 1:
+        hidden = hidden.view(1, -1)
+    n, K = hidden.shape
+    if wq.numel() != (K // 32) * 34:
+        raise ValueError("wq must hold K/32 Q8_0 blocks of 34 bytes")
+    if gate_out is None:
+        gate_out = torch.empty(n, dtype=torch.int32, device=hidden.device)
+    if logit_out is None:
+        logit_out = torch.empty(n, dtype=torch.float32, device=hidden.device)
+    st = lib.dspark_conf_probe(_ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)),
+                               _ptr(hidden, "hidden", dtypes=(torch.float32,)),
+                               float(bias), float(threshold), K, n,
+                               _ptr(logit_out, "logit_out", dtypes=(torch.float32,)),
+                               _ptr(gate_out, "gate_out", dtypes=(torch.int32,)),
+                               _stream(stream))
+    _check(lib, st)
+    return logit_out, gate_out
+
+
+def ws_matvec(W, X, *, out=None, out_fp32: bool = False, stream=None):
+    """Y = X W^T.  W fp16 [N, K], X fp16 [M, K]; returns Y [M, N] (fp16, or fp32)."""
+    lib = load_library()
+    N, K = W.shape
+    M, K2 = X.shape
+    if K != K2:
+        raise ValueError("W and X disagree on K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32 if out_fp32 else torch.float16,
+                          device=W.device)
+    y_fp32 = out.dtype == torch.float32
+    st = lib.dspark_ws_matvec(_ptr(W, "W", itemsize=2, dtypes=_BITS16),
+                              _ptr(X, "X", itemsize=2, dtypes=_BITS16),
+                              _ptr(out, "out", dtypes=(torch.float16, torch.float32)),
+                              1 if y_fp32 else 0, M, N, K, _stream(stream))
+    _check(lib, st)
+    return out

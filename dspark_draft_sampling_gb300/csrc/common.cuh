@@ -1,0 +1,204 @@
+// Internal helpers shared by the libdspark kernels (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// ---- host-side error reporting (common.cu) -------------------------------------------
+dspark_status fail(dspark_status s, const char *fmt, ...);
+dspark_status cuda_fail(cudaError_t e, const char *what);
+void clear_error();
+// SM count of the current device (cached per device).
+int current_sm_count(int *sm_count);
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Device status word bits (stored in the workspace header).
+constexpr unsigned kStatusIndex = 1u;
+constexpr unsigned kStatusTimeout = 2u;
+
+// Default limit for every device-side wait: far above any legitimate wait (a whole
+// draft takes well under a millisecond) and short enough to never look like a hang.
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+// ---- device helpers -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; false after
+// `timeout_ns` without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+// 1-D bulk copy global -> shared (TMA engine); completion is counted in bytes on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                         uint64_t l2_policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(l2_policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Named barrier over `nthreads` threads (a subset of the CTA).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Read-only 16-byte global load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// bf16 pair (lower address in the low half) -> two exact fp32 values.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Order-preserving map of an fp32 value to uint32 (-0 is first folded onto +0, so
+// equal values map to equal codes).  Larger float -> larger code.
+__device__ __forceinline__ uint32_t float_order_code(float x) {
+    uint32_t u = __float_as_uint(x + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (value desc, index asc) as one 64-bit key: max over keys = greedy argmax with the
+// lowest-index tie-break.  Every finite or infinite logit gives a key > 0.
+__device__ __forceinline__ unsigned long long argmax_key(float logit, uint32_t index) {
+    return (static_cast<unsigned long long>(float_order_code(logit)) << 32) |
+           static_cast<unsigned long long>(0xffffffffu - index);
+}
+
+__device__ __forceinline__ uint32_t argmax_key_index(unsigned long long key) {
+    return 0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull);
+}
+
+// Reduce-scatter of N per-lane values over the lane groups that differ in the bits
+// O, O/2, ..., 1 of the lane index (a butterfly).  Each value is summed over the same
+// fixed tree (partner lanes combined in the order O, O/2, ..., 1), so its result does
+// not depend on N.  While more than one value remains, the lane whose bit is set keeps
+// the upper half.  Afterwards v[0 .. max(1, N >> log2(2*O)) - 1] hold complete sums
+// of a contiguous block of value indices (see rs_first_index).
+template <int N, int O>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int lane) {
+        if constexpr (O == 0) {
+            return;
+        } else if constexpr (N > 1) {
+            const bool up = (lane & O) != 0;
+#pragma unroll
+            for (int t = 0; t < N / 2; ++t) {
+                const float send = up ? v[t] : v[t + N / 2];
+                const float keep = up ? v[t + N / 2] : v[t];
+                v[t] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            ReduceScatter<N / 2, O / 2>::run(v, lane);
+        } else {
+            v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], O);
+            ReduceScatter<1, O / 2>::run(v, lane);
+        }
+    }
+};
+
+// Index of the first value a lane holds after ReduceScatter<N, O>.
+template <int N, int O>
+__device__ __forceinline__ int rs_first_index(int lane) {
+    int vi = 0, n = N;
+#pragma unroll
+    for (int o = O; o >= 1; o >>= 1) {
+        if (n > 1) {
+            if (lane & o) vi += n / 2;
+            n /= 2;
+        }
+    }
+    return vi;
+}
+
+template <int N, int O>
+constexpr int rs_values_left() {
+    int n = N;
+    for (int o = O; o >= 1; o >>= 1)
+        if (n > 1) n /= 2;
+    return n;
+}
+
+}  // namespace dspark

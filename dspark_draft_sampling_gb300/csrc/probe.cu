@@ -1,0 +1,94 @@
+// Proposer confidence probe: Q8_0 dequant-dot of the hidden state + logit-space gate.
+//
+// Method (ds4 PR #772 "dspark: cut per-cycle CUDA overheads", sections "Summary" and
+// "Root cause"): a 7424-wide matvec of the hidden vector against Q8_0 weights, run on
+// the GPU so that only a 4-byte gate decision crosses to the host.
+//
+// One CTA per probe.  Threads stride over 16-byte chunks of the hidden vector (one
+// vector load each), dequantize the matching four int8 weights with their block's fp16
+// scale exactly in fp32, and accumulate; a fixed warp butterfly plus an in-order sum of
+// the eight warp totals gives z, so the result does not depend on scheduling.  The gate
+// compares z with logit(threshold) (computed on the host), which is the same decision as
+// sigmoid(z) >= threshold without evaluating an exponential on the device.
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "common.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kProbeThreads = 256;
+constexpr int kProbeWarps = kProbeThreads / 32;
+
+__device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
+    const uint4 u = ldg_nc_v4(p);
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+
+__global__ void __launch_bounds__(kProbeThreads) conf_probe_kernel(const uint8_t *__restrict__ wq,
+                                                                   const float *__restrict__ hidden, float bias,
+                                                                   float t_logit, int K, float *logit_out,
+                                                                   int32_t *gate_out) {
+    __shared__ float warp_sum[kProbeWarps];
+    const float *x = hidden + size_t(blockIdx.x) * K;
+    const int nchunks = K >> 2;  // 4 floats per chunk; a Q8_0 block spans 8 chunks
+    float acc = 0.f;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < nchunks; c += kProbeThreads) {
+        const float4 xv = ldg_stream_f4(x + 4 * c);
+        const uint8_t *blk = wq + size_t(c >> 3) * 34;
+        const int off = 2 + 4 * (c & 7);
+        const unsigned short dbits = static_cast<unsigned short>(__ldg(blk) | (__ldg(blk + 1) << 8));
+        const float d = __half2float(__ushort_as_half(dbits));
+        const float q0 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 0)));
+        const float q1 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 1)));
+        const float q2 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 2)));
+        const float q3 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 3)));
+        float s = q0 * xv.x;
+        s = fmaf(q1, xv.y, s);
+        s = fmaf(q2, xv.z, s);
+        s = fmaf(q3, xv.w, s);
+        acc = fmaf(d, s, acc);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float z = warp_sum[0];
+#pragma unroll
+        for (int w = 1; w < kProbeWarps; ++w) z += warp_sum[w];
+        z += bias;
+        if (logit_out) logit_out[blockIdx.x] = z;
+        gate_out[blockIdx.x] = (z >= t_logit) ? 1 : 0;
+    }
+}
+
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float bias, float threshold,
+                                           int K, int n_probes, float *logit_out, int32_t *gate_out,
+                                           dspark_stream_t stream) {
+    using namespace dspark;
+    clear_error();
+    if (K <= 0 || (K % 32) != 0) return fail(DSPARK_ERR_INVALID, "conf_probe: K=%d must be a positive multiple of 32", K);
+    if (n_probes < 0) return fail(DSPARK_ERR_INVALID, "conf_probe: n_probes=%d < 0", n_probes);
+    if (!(threshold > 0.f && threshold < 1.f))
+        return fail(DSPARK_ERR_INVALID, "conf_probe: threshold must lie in (0, 1)");
+    if (n_probes == 0) return DSPARK_OK;  // nothing to enqueue
+    if (!w_q8_0 || !hidden || !gate_out) return fail(DSPARK_ERR_INVALID, "conf_probe: null pointer argument");
+    if (!aligned(hidden, 16)) return fail(DSPARK_ERR_INVALID, "conf_probe: hidden must be 16-byte aligned");
+    if (!aligned(gate_out, 4) || (logit_out && !aligned(logit_out, 4)))
+        return fail(DSPARK_ERR_INVALID, "conf_probe: misaligned output pointer");
+    // logit(t) on the host in double: sigmoid(z) >= t  <=>  z >= log(t / (1 - t)).
+    const double t = static_cast<double>(threshold);
+    const float t_logit = static_cast<float>(std::log(t / (1.0 - t)));
+    conf_probe_kernel<<<n_probes, kProbeThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_q8_0), hidden, bias, t_logit, K, logit_out, gate_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "conf_probe launch");
+    return DSPARK_OK;
+}

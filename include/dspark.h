@@ -1,0 +1,180 @@
+/*
+ * libdspark -- the DSpark per-cycle draft step on one GB300 (sm_103a).
+ *
+ * Three operations, each a hand-written CUDA kernel:
+ *   dspark_markov_draft  the sequential Markov block-draft sampler
+ *   dspark_conf_probe    the proposer's Q8_0 confidence probe and its gate
+ *   dspark_ws_matvec     the weight-stationary small-M fp16 projection matvec
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations), owned
+ *     by the caller, row-major and contiguous.  The library never allocates, copies
+ *     to the host or synchronizes in these calls: work is enqueued on `stream`
+ *     (a cudaStream_t; NULL means the legacy default stream) and the call returns.
+ *   - The return value reports argument checking and launch errors only.  Faults
+ *     that can only be seen on the device (an out-of-range prev or d2t entry, a
+ *     device-side wait that gave up) are recorded in the workspace and reported by
+ *     dspark_markov_status().
+ *   - dspark_last_error() returns a message for the last non-OK status returned on
+ *     the calling thread.  No call aborts, exits or traps.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *dspark_stream_t;
+
+typedef enum dspark_status {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID = 1,     /* null pointer, negative or inconsistent size, misalignment */
+    DSPARK_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement */
+    DSPARK_ERR_CUDA = 3,        /* a CUDA runtime call failed (message in dspark_last_error) */
+    DSPARK_ERR_TIMEOUT = 4,     /* a device-side wait hit its time limit; outputs undefined */
+    DSPARK_ERR_INDEX = 5        /* a prev or d2t entry was out of range; those ids are -1 */
+} dspark_status;
+
+/* Message for the last non-OK status on this thread ("" if none).  Thread-local storage
+ * owned by the library; valid until the next call on the same thread. */
+const char *dspark_last_error(void);
+
+/* Library version string, e.g. "libdspark 0.1 sm_103a". */
+const char *dspark_version(void);
+
+/* =====================================================================================
+ * Markov block draft
+ *
+ * Source: vllm.cpp issue #436 "SPEC-DSPARK W7: the sequential Markov sample loop is
+ * HOST-side", section "The fix" (per-step chain, lowest-index tie-break, identity d2t,
+ * prev kept on the device, only the final ids read back) and "W7 LANDED"
+ * (markov_w2 is [draft_vocab, markov_rank] bf16 and is re-read whole every step).
+ *
+ * For every request r and draft position i = 0 .. k-1, with p = prev[r] at i = 0:
+ *   h        = markov_w1[p, :]                                  (gather)
+ *   bias[v]  = sum_j markov_w2[v, j] * h[j]                     (bias GEMV, fp32 accumulate)
+ *   logit[v] = base_logits[r, i, v] + bias[v]                   (fp32)
+ *   id       = smallest v attaining max_v logit[v]               (greedy argmax)
+ *   out_ids[r, i] = d2t ? d2t[id] : id                          (target-space id)
+ *   p        = id                                               (draft-space id)
+ *
+ * Arguments
+ *   base_logits  float  [num_reqs, k, vocab]
+ *   markov_w1    bf16   [vocab, rank] (raw 16-bit patterns)
+ *   markov_w2    bf16   [vocab, rank]; 16-byte aligned
+ *   d2t          int32  [vocab] draft->target map, or NULL for the identity
+ *   prev         int64  [num_reqs]; in: previous draft id per request,
+ *                out: the last draft-space id of each request (written at the end)
+ *   out_ids      int64  [num_reqs, k] target-space draft ids
+ *   dbg_logits   float  [num_reqs, k, vocab] or NULL: every logit (tests only; costs
+ *                bandwidth)
+ *   dbg_bias     float  [num_reqs, k, vocab] or NULL: every bias value (tests only)
+ *   workspace    device scratch of at least dspark_markov_workspace_bytes() bytes,
+ *                256-byte aligned; it also holds the device status word.  Calls that
+ *                share one workspace must not overlap on the device.
+ * Supported: rank in {64, 128, 256, 512}; 1 <= num_reqs <= 8; vocab >= 1;
+ *   k >= 0 (k == 0 or num_reqs == 0 enqueues nothing).
+ * Device-side errors: a prev entry outside [0, vocab) or a negative d2t entry makes
+ *   the affected ids -1 and sets DSPARK_ERR_INDEX in the status word.
+ * The k positions run in one cooperative kernel launch (one CTA per SM) preceded by
+ *   a memset of the workspace header; both can be captured in a CUDA graph.
+ * ===================================================================================== */
+size_t dspark_markov_workspace_bytes(int num_reqs, int k, int vocab, int rank);
+
+dspark_status dspark_markov_draft(const float *base_logits, const uint16_t *markov_w1,
+                                  const uint16_t *markov_w2, const int32_t *d2t, int64_t *prev,
+                                  int num_reqs, int k, int vocab, int rank, int64_t *out_ids,
+                                  float *dbg_logits, float *dbg_bias, void *workspace,
+                                  size_t workspace_bytes, dspark_stream_t stream);
+
+/* Synchronizes `stream`, then reads the status word that the last dspark_markov_draft
+ * on `workspace` left: DSPARK_OK, DSPARK_ERR_INDEX or DSPARK_ERR_TIMEOUT. */
+dspark_status dspark_markov_status(const void *workspace, dspark_stream_t stream);
+
+/* Fault-injection hook for testing the device-side wait limit: the same launch as
+ * dspark_markov_draft, except that the grid-wide step barrier expects
+ * `missing_arrivals` more arrivals than there are CTAs (so with missing_arrivals > 0
+ * it can never complete) and every device-side wait gives up after `timeout_us`
+ * microseconds.  The kernel then records DSPARK_ERR_TIMEOUT, drains its in-flight
+ * copies and returns; nothing hangs.  Not for production use. */
+dspark_status dspark_markov_draft_debug(const float *base_logits, const uint16_t *markov_w1,
+                                        const uint16_t *markov_w2, const int32_t *d2t,
+                                        int64_t *prev, int num_reqs, int k, int vocab, int rank,
+                                        int64_t *out_ids, void *workspace,
+                                        size_t workspace_bytes, unsigned missing_arrivals,
+                                        unsigned timeout_us, dspark_stream_t stream);
+
+/* Plan form: records one dspark_markov_draft call (fixed pointers and sizes) into an
+ * instantiated CUDA graph, so that each draft is a single graph launch.  Creation
+ * captures on a private stream and may allocate host/driver objects; launching
+ * allocates nothing.  The tensors must stay alive while the plan is used. */
+typedef struct dspark_markov_plan dspark_markov_plan;
+
+dspark_status dspark_markov_plan_create(const float *base_logits, const uint16_t *markov_w1,
+                                        const uint16_t *markov_w2, const int32_t *d2t,
+                                        int64_t *prev, int num_reqs, int k, int vocab,
+                                        int rank, int64_t *out_ids, void *workspace,
+                                        size_t workspace_bytes, dspark_markov_plan **plan_out);
+dspark_status dspark_markov_plan_launch(dspark_markov_plan *plan, dspark_stream_t stream);
+void dspark_markov_plan_destroy(dspark_markov_plan *plan);
+
+/* =====================================================================================
+ * Confidence probe
+ *
+ * Source: ds4 PR #772 "dspark: cut per-cycle CUDA overheads (single-draft decode, GPU
+ * confidence probe)", sections "Summary" and "Root cause": a 7424-wide matvec of the
+ * hidden state against Q8_0 weights, evaluated on the GPU with a 4-byte readback; the
+ * result only gates the proposal length.
+ *
+ * For each probe p:
+ *   z[p]    = bias + sum_b d_b * sum_{j<32} q_{b,j} * hidden[p, 32b + j]
+ *   gate[p] = (sigmoid(z[p]) >= threshold), computed as z[p] >= log(t / (1 - t))
+ *
+ * Arguments
+ *   w_q8_0     K/32 Q8_0 blocks of 34 bytes each: fp16 scale d (little endian) followed
+ *              by 32 int8 values q; any byte alignment
+ *   hidden     float [n_probes, K]; 16-byte aligned
+ *   bias       scalar added to every probe's dot product
+ *   threshold  in (0, 1)
+ *   K          > 0, multiple of 32
+ *   n_probes   >= 0 (0 enqueues nothing); probes are independent (one CTA each)
+ *   logit_out  float [n_probes] or NULL
+ *   gate_out   int32 [n_probes]: 1 = keep drafting, 0 = stop.  May be device memory or
+ *              mapped pinned host memory (then the 4-byte readback is the kernel's
+ *              own store).  Must not be NULL.
+ * ===================================================================================== */
+dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float bias,
+                                float threshold, int K, int n_probes, float *logit_out,
+                                int32_t *gate_out, dspark_stream_t stream);
+
+/* =====================================================================================
+ * Weight-stationary small-M matvec
+ *
+ * Source: SharpInference issue #441 "DSpark GPU draft round runs ~3x the bandwidth
+ * floor -- small-M (B=7) projection GEMMs -> weight-stationary matvec", sections
+ * "Observation", "Hypothesis" and "Proposed work": fp16 projections with M = B = 7
+ * rows where each weight element should be read from HBM once for all rows.
+ *
+ *   Y[m, n] = sum_k X[m, k] * W[n, k]      (fp16 inputs, fp32 accumulation)
+ *
+ * Arguments
+ *   W          fp16 [N, K] (out x in), 16-byte aligned
+ *   X          fp16 [M, K], 16-byte aligned
+ *   Y          [M, N]: fp32 if y_is_fp32, else fp16 rounded to nearest even
+ *   Supported: 1 <= M <= 16, N >= 1, K >= 8 with K % 8 == 0 (M == 0 or N == 0
+ *   enqueues nothing).  The result of row m does not depend on M: every output is
+ *   summed in one fixed order.
+ * ===================================================================================== */
+dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32,
+                               int M, int N, int K, dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

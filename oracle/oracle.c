@@ -34,6 +34,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ---- number formats ---------------------------------------------------------- */
@@ -216,15 +217,29 @@ int oracle_ws_matvec(const uint16_t *W, const uint16_t *X, int M, int N, int K, 
 {
     if (M < 0 || N < 0 || K < 0 || !W || !X || !Y)
         return -1;
-    for (int m = 0; m < M; ++m)
-        for (int n = 0; n < N; ++n) {
+    /* decode the fp16 operands once (exact), then sum k ascending per output */
+    double *xd = malloc(sizeof(double) * ((size_t)M * K + 1));
+    double *wd = malloc(sizeof(double) * ((size_t)K + 1));
+    if (!xd || !wd) {
+        free(xd);
+        free(wd);
+        return -1;
+    }
+    for (size_t e = 0; e < (size_t)M * K; ++e)
+        xd[e] = oracle_f16_to_f64(X[e]);
+    for (int n = 0; n < N; ++n) {
+        for (int kk = 0; kk < K; ++kk)
+            wd[kk] = oracle_f16_to_f64(W[(size_t)n * K + kk]);
+        for (int m = 0; m < M; ++m) {
             double acc = 0.0;
             for (int kk = 0; kk < K; ++kk)
-                acc += oracle_f16_to_f64(X[(size_t)m * K + kk]) *
-                       oracle_f16_to_f64(W[(size_t)n * K + kk]);
+                acc += xd[(size_t)m * K + kk] * wd[kk];
             Y[(size_t)m * N + n] = acc;
             if (Y16)
                 Y16[(size_t)m * N + n] = oracle_f64_to_f16_rne(acc);
         }
+    }
+    free(xd);
+    free(wd);
     return 0;
 }

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from dspark_draft_sampling_gb300 import api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "dspark.h")
+
+INVALID, UNSUPPORTED = api.DSPARK_ERR_INVALID, api.DSPARK_ERR_UNSUPPORTED
+FAKE = ctypes.c_void_p(0x10000)        # never dereferenced: every case fails validation first
+FAKE_ODD = ctypes.c_void_p(0x10002)    # not 16-byte aligned
+NULL = None
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("dspark_markov_draft", "dspark_conf_probe", "dspark_ws_matvec"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(dspark_lib):
+    names = declared_functions()
+    assert set(names) == set(api.SIGNATURES), "binding and header disagree"
+    out = subprocess.run(["nm", "-D", "--defined-only", api.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (dspark_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert getattr(dspark_lib, n) is not None
+
+
+def test_version(dspark_lib):
+    assert dspark_lib.dspark_version().decode().startswith("libdspark")
+
+
+def test_workspace_bytes(dspark_lib):
+    a = dspark_lib.dspark_markov_workspace_bytes(1, 15, 248320, 256)
+    b = dspark_lib.dspark_markov_workspace_bytes(8, 15, 248320, 256)
+    assert a == b and a % 256 == 0 and a >= 256 + 15 * 8 * 8
+    assert dspark_lib.dspark_markov_workspace_bytes(1, 0, 10, 64) == 256
+
+
+def _markov(lib, *, base=FAKE, w1=FAKE, w2=FAKE, d2t=NULL, prev=FAKE, B=1, k=4, V=4096, R=64,
+            out=FAKE, ws=FAKE, wsb=1 << 20):
+    return lib.dspark_markov_draft(base, w1, w2, d2t, prev, B, k, V, R, out, NULL, NULL, ws, wsb,
+                                   NULL)
+
+
+def test_markov_validation(dspark_lib):
+    lib = dspark_lib
+    assert _markov(lib, R=100) == UNSUPPORTED
+    assert _markov(lib, R=512) == UNSUPPORTED
+    assert _markov(lib, B=9) == UNSUPPORTED
+    assert _markov(lib, B=-1) == INVALID
+    assert _markov(lib, V=0) == INVALID
+    assert _markov(lib, base=NULL) == INVALID
+    assert _markov(lib, w2=NULL) == INVALID
+    assert _markov(lib, prev=NULL) == INVALID
+    assert _markov(lib, out=NULL) == INVALID
+    assert _markov(lib, ws=NULL) == INVALID
+    assert _markov(lib, w2=FAKE_ODD) == INVALID
+    assert _markov(lib, w1=FAKE_ODD) == INVALID
+    assert _markov(lib, ws=FAKE_ODD) == INVALID
+    assert _markov(lib, wsb=16) == INVALID
+    assert "workspace" in lib.dspark_last_error().decode()
+    # nothing to do: accepted without launching anything
+    assert _markov(lib, k=0) == 0
+    assert _markov(lib, B=0) == 0
+    assert lib.dspark_last_error().decode() == ""
+
+
+def test_markov_debug_and_plan_validation(dspark_lib):
+    lib = dspark_lib
+    assert lib.dspark_markov_draft_debug(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 64, 64, FAKE, FAKE,
+                                         4096, 1, 0, NULL) == INVALID
+    assert lib.dspark_markov_plan_create(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 64, 64, FAKE, FAKE,
+                                         4096, None) == INVALID
+    assert lib.dspark_markov_plan_launch(NULL, NULL) == INVALID
+    lib.dspark_markov_plan_destroy(NULL)
+    assert lib.dspark_markov_status(NULL, NULL) == INVALID
+
+
+def test_probe_validation(dspark_lib):
+    lib = dspark_lib
+    f = lib.dspark_conf_probe
+    assert f(FAKE, FAKE, 0.0, 0.5, 33, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 0.5, 0, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 1.0, 64, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 0.0, 64, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 0.5, 64, -1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 0.5, 64, 1, NULL, NULL, NULL) == INVALID
+    assert f(FAKE, FAKE_ODD, 0.0, 0.5, 64, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 0.0, 0.5, 64, 0, NULL, FAKE, NULL) == 0
+
+
+def test_ws_validation(dspark_lib):
+    lib = dspark_lib
+    f = lib.dspark_ws_matvec
+    assert f(FAKE, FAKE, FAKE, 0, 17, 64, 64, NULL) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 12, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 0, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, -1, 64, 64, NULL) == INVALID
+    assert f(NULL, FAKE, FAKE, 0, 7, 64, 64, NULL) == INVALID
+    assert f(FAKE_ODD, FAKE, FAKE, 0, 7, 64, 64, NULL) == INVALID
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 0, 7, 64, 64, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 1, 0, 64, 64, NULL) == 0
+    assert f(FAKE, FAKE, FAKE, 1, 7, 0, 64, NULL) == 0
+
+
+def test_python_binding_rejects_cpu_tensors(dspark_lib):
+    import torch
+
+    with pytest.raises(ValueError):
+        api.ws_matvec(torch.zeros(4, 8, dtype=torch.float16), torch.zeros(1, 8, dtype=torch.float16))

@@ -1,0 +1,70 @@
+"""GPU confidence probe vs the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from dspark_draft_sampling_gb300 import api, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(dspark_lib):
+    return dspark_lib
+
+
+def test_batched_cycle_workload():
+    """2 probes per cycle x 1024 cycles, 7424-wide, threshold 0.5."""
+    inp = synth.probe_inputs(2048, 7424, seed=0)
+    z, gate = parity.gpu_probe(inp)
+    rep = parity.check_probe(inp, z, gate)
+    assert rep["n_near_threshold"] == 0
+    assert 0 < gate.sum() < 2048
+
+
+@pytest.mark.parametrize("n,K,t,seed", [(1, 7424, 0.5, 1), (7, 32, 0.5, 2), (33, 7424, 0.8, 3),
+                                        (100, 4096, 0.2, 4), (5, 7456, 0.5, 5)])
+def test_shapes_and_thresholds(n, K, t, seed):
+    inp = synth.probe_inputs(n, K, seed=seed, threshold=t, random_scales=True, scale=0.01)
+    z, gate = parity.gpu_probe(inp)
+    parity.check_probe(inp, z, gate)
+
+
+def test_one_hot_is_exact():
+    inp = synth.probe_inputs(1, 7424, seed=6, random_scales=True)
+    x = np.zeros((3, 7424), np.float32)
+    for p, (b, j) in enumerate([(0, 0), (100, 17), (231, 31)]):
+        x[p, 32 * b + j] = 1.0
+    inp["hidden"] = x
+    z, _ = parity.gpu_probe(inp)
+    zo, _ = parity.oracle.conf_probe(inp["wq"], x, inp["bias"], 0.5)
+    np.testing.assert_array_equal(z.astype(np.float64), zo.astype(np.float32).astype(np.float64))
+
+
+def test_repeat_bit_identical():
+    inp = synth.probe_inputs(64, 7424, seed=7)
+    a, ga = parity.gpu_probe(inp)
+    b, gb = parity.gpu_probe(inp)
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+    np.testing.assert_array_equal(ga, gb)
+
+
+def test_gate_readback_is_four_bytes():
+    inp = synth.probe_inputs(1, 7424, seed=8)
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    hid = torch.from_numpy(inp["hidden"]).cuda()
+    gate = torch.empty(1, dtype=torch.int32, device="cuda")
+    api.conf_probe(wq, hid, inp["bias"], 0.5, gate_out=gate)
+    host = gate.cpu()
+    assert host.numel() * host.element_size() == 4
+    _, go = parity.oracle.conf_probe(inp["wq"], inp["hidden"], inp["bias"], 0.5)
+    assert int(host[0]) == int(go[0])
+
+
+def test_rejects_misaligned_hidden():
+    inp = synth.probe_inputs(2, 64, seed=9)
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    flat = torch.from_numpy(inp["hidden"].reshape(-1)).cuda()
+    with pytest.raises(api.DsparkError):
+        api.conf_probe(wq, flat[1:65], inp["bias"], 0.5)

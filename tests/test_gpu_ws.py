@@ -1,0 +1,73 @@
+"""GPU weight-stationary matvec vs the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from dspark_draft_sampling_gb300 import api, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(dspark_lib):
+    return dspark_lib
+
+
+def _dev(inp):
+    W = torch.from_numpy(inp["W"].view(np.int16)).cuda().view(torch.float16)
+    X = torch.from_numpy(inp["X"].view(np.int16)).cuda().view(torch.float16)
+    return W, X
+
+
+def _run(inp):
+    W, X = _dev(inp)
+    y32 = api.ws_matvec(W, X, out_fp32=True)
+    y16 = api.ws_matvec(W, X)
+    torch.cuda.synchronize()
+    return y32.cpu().numpy(), y16.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("K,N", synth.WS_SHAPES)
+def test_qwen3_8b_projection_shapes(K, N):
+    inp = synth.ws_inputs(7, N, K, seed=K + N)
+    y32, y16 = _run(inp)
+    parity.check_ws(inp, y32=y32, y16=y16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 8), (2, 100, 64), (3, 1000, 2056), (5, 153, 4104),
+                                   (8, 4096, 512), (9, 300, 1024), (16, 777, 4096), (7, 1, 12288),
+                                   (4, 5000, 8)])
+def test_ragged_shapes(M, N, K):
+    inp = synth.ws_inputs(M, N, K, seed=M * 7 + N)
+    y32, y16 = _run(inp)
+    parity.check_ws(inp, y32=y32, y16=y16)
+
+
+def test_rows_independent_of_m_bitwise():
+    inp = synth.ws_inputs(16, 1000, 4096, seed=3)
+    W, X = _dev(inp)
+    full = api.ws_matvec(W, X, out_fp32=True)
+    for M in (1, 2, 3, 7, 9):
+        part = api.ws_matvec(W, X[:M].contiguous(), out_fp32=True)
+        torch.cuda.synchronize()
+        assert torch.equal(part.view(torch.int32), full[:M].view(torch.int32)), M
+    for m in (0, 5, 15):
+        one = api.ws_matvec(W, X[m:m + 1].contiguous(), out_fp32=True)
+        assert torch.equal(one[0].view(torch.int32), full[m].view(torch.int32))
+
+
+def test_close_to_cublas():
+    inp = synth.ws_inputs(7, 4096, 4096, seed=4)
+    W, X = _dev(inp)
+    y = api.ws_matvec(W, X, out_fp32=True)
+    ref = torch.matmul(X.float(), W.float().t())
+    assert torch.allclose(y, ref, rtol=1e-3, atol=2e-3)
+
+
+def test_repeat_bit_identical():
+    inp = synth.ws_inputs(7, 12288, 4096, seed=5)
+    W, X = _dev(inp)
+    a = api.ws_matvec(W, X, out_fp32=True)
+    b = api.ws_matvec(W, X, out_fp32=True)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
