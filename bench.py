@@ -86,6 +86,22 @@ def config_dict(B):
 
 
 # ---------------------------------------------------------------- helpers ----------------
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (the job is as slow as its slowest replica)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_value_us(max_ms_per_step, world):
+    """Whole-job microseconds per draft step: every rank completes one step per max time."""
+    return max_ms_per_step * 1000.0 / world
+
+
 def read_peak():
     p = os.path.join(REPO, "MEASURED_PEAKS.json")
     try:
@@ -390,11 +406,7 @@ def main():
     ms_step = res["ms_step"]
     markov_ms = res["markov_ms"]
     if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms_step, markov_ms, res["wall"]], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, markov_ms, wall = (float(x) for x in t.tolist())
+        ms_step, markov_ms, _ = max_over_ranks([ms_step, markov_ms, res["wall"]], "cuda")
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -409,7 +421,7 @@ def main():
     traffic = recorded_traffic(B)
     line = {
         "metric": METRIC,
-        "value": ms_step * 1000.0 / world,
+        "value": job_value_us(ms_step, world),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,

@@ -8,8 +8,9 @@ Tolerances
     later position.  The bound for a logit base + sum_j w2[v,j] h[j] summed in fp32 in
     any order is (R + 2) * 2^-24 * (sum_j |w2[v,j] h[j]| + |base| + |bias|); the margin
     allowed is twice the sum of the two bounds.
-  * probe gates: identical, except where |z_oracle - logit(t)| is within
-    2 (K + 2) 2^-24 (sum |d q x| + |bias|).
+  * probe gates: identical, except where |z_oracle - logit(t)| is within the value
+    tolerance above (the GPU logit is checked to lie within it of the oracle's, so only
+    inside that band can a correct fp32 evaluation land on the other side).
 """
 from __future__ import annotations
 
@@ -118,17 +119,6 @@ def check_markov(inp, g, *, values=True):
 
 
 # ---------------------------------------------------------------- confidence probe ------
-def probe_margin_bound(inp):
-    K = inp["K"]
-    nb = K // 32
-    blk = inp["wq"].reshape(nb, 34)
-    d = blk[:, :2].copy().view("<u2").reshape(nb).view(np.float16).astype(np.float64)
-    q = blk[:, 2:].copy().view(np.int8).astype(np.float64)
-    w = (d[:, None] * q).reshape(-1)
-    a = np.abs(inp["hidden"].astype(np.float64) * w[None, :]).sum(axis=1) + abs(inp["bias"])
-    return 2 * (K + 2) * U32 * a
-
-
 def gpu_probe(inp, device="cuda"):
     wq = torch.from_numpy(inp["wq"]).to(device)
     hid = torch.from_numpy(np.ascontiguousarray(inp["hidden"])).to(device)
@@ -142,10 +132,11 @@ def check_probe(inp, z, gate):
     assert ok, f"{nbad} probe logits outside tolerance (max err {err:.3e})"
     t = inp["threshold"]
     thr = np.log(t / (1 - t))
-    near = np.abs(zo - thr) <= probe_margin_bound(inp)
+    near = np.abs(zo - thr) <= TOL_ABS + TOL_REL * abs(thr)
     mism = (gate != go) & ~near
     assert not mism.any(), f"{int(mism.sum())} gate decisions differ"
-    return dict(max_z_err=err, n_near_threshold=int(near.sum()))
+    return dict(max_z_err=err, n_near_threshold=int(near.sum()),
+                n_gate_mismatch=int((gate != go).sum()))
 
 
 # ---------------------------------------------------------------- WS matvec -------------

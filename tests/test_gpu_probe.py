@@ -19,7 +19,9 @@ def test_batched_cycle_workload():
     inp = synth.probe_inputs(2048, 7424, seed=0)
     z, gate = parity.gpu_probe(inp)
     rep = parity.check_probe(inp, z, gate)
-    assert rep["n_near_threshold"] == 0
+    assert rep["n_gate_mismatch"] == 0
+    assert rep["n_near_threshold"] <= 2
+    assert rep["max_z_err"] < 1e-4
     assert 0 < gate.sum() < 2048
 
 
