@@ -28,6 +28,7 @@ SIGNATURES = {
     "dspark_markov_draft": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "dspark_markov_status": (_I, [_P, _P]),
     "dspark_markov_draft_debug": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _U, _U, _P]),
+    "dspark_markov_draft_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dspark_markov_plan_create": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z,
                                        ctypes.POINTER(_P)]),
     "dspark_markov_plan_launch": (_I, [_P, _P]),

@@ -486,6 +486,61 @@ extern "C" dspark_status dspark_markov_draft_debug(const float *base_logits, con
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---- allocation-free variant ----------------------------------------------------------
+// Scratch for dspark_markov_draft_noalloc: the same header + per-position argmax keys that
+// a caller-provided workspace holds, sized for at most kNoAllocMaxK positions.  It lives in
+// the library's own device memory, allocated when the module is loaded on a device and
+// held until the process exits.  In host code `g_markov_noalloc_scratch` is only a host-side
+// handle for the symbol: its device address comes from cudaGetSymbolAddress below.
+namespace dspark {
+namespace {
+constexpr int kNoAllocMaxK = 64;
+constexpr size_t kNoAllocScratchBytes = kHeaderBytes + size_t(kNoAllocMaxK) * kMaxReqs * sizeof(unsigned long long);
+static_assert(kNoAllocScratchBytes == 4352, "scratch size");
+}  // namespace
+}  // namespace dspark
+
+static __device__ __align__(256) unsigned char g_markov_noalloc_scratch[dspark::kNoAllocScratchBytes];
+
+namespace dspark {
+namespace {
+// Device address of the scratch array, looked up once per device with that device current.
+dspark_status noalloc_scratch(void **out) {
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(DSPARK_ERR_UNSUPPORTED, "markov_noalloc: device ordinal %d >= 64", dev);
+    void *p = __atomic_load_n(&addr[dev], __ATOMIC_ACQUIRE);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_markov_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(markov scratch)");
+        __atomic_store_n(&addr[dev], p, __ATOMIC_RELEASE);
+    }
+    *out = p;
+    return DSPARK_OK;
+}
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status dspark_markov_draft_noalloc(const float *base_logits, const uint16_t *markov_w1,
+                                                     const uint16_t *markov_w2, const int32_t *d2t, int64_t *prev,
+                                                     int num_reqs, int k, int vocab, int rank, int64_t *out_ids,
+                                                     dspark_stream_t stream) {
+    dspark::clear_error();
+    if (k > dspark::kNoAllocMaxK)
+        return dspark::fail(DSPARK_ERR_UNSUPPORTED,
+                            "markov_noalloc: k=%d exceeds the %d positions its static scratch holds; "
+                            "use dspark_markov_draft with a workspace",
+                            k, dspark::kNoAllocMaxK);
+    void *scratch = nullptr;
+    dspark_status st = dspark::noalloc_scratch(&scratch);
+    if (st != DSPARK_OK) return st;
+    return dspark::markov_enqueue(base_logits, markov_w1, markov_w2, d2t, prev, num_reqs, k, vocab, rank, out_ids,
+                                  nullptr, nullptr, scratch, dspark::kNoAllocScratchBytes, 0u,
+                                  dspark::kDefaultTimeoutNs, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" dspark_status dspark_markov_status(const void *workspace, dspark_stream_t stream) {
     dspark::clear_error();
     if (!workspace) return dspark::fail(DSPARK_ERR_INVALID, "markov_status: null workspace");

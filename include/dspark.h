@@ -77,7 +77,7 @@ const char *dspark_version(void);
  *   workspace    device scratch of at least dspark_markov_workspace_bytes() bytes,
  *                256-byte aligned; it also holds the device status word.  Calls that
  *                share one workspace must not overlap on the device.
- * Supported: rank in {64, 128, 256, 512}; 1 <= num_reqs <= 8; vocab >= 1;
+ * Supported: rank in {64, 128, 256}; 1 <= num_reqs <= 8; vocab >= 1;
  *   k >= 0 (k == 0 or num_reqs == 0 enqueues nothing).
  * Device-side errors: a prev entry outside [0, vocab) or a negative d2t entry makes
  *   the affected ids -1 and sets DSPARK_ERR_INDEX in the status word.
@@ -122,6 +122,28 @@ dspark_status dspark_markov_plan_create(const float *base_logits, const uint16_t
                                         size_t workspace_bytes, dspark_markov_plan **plan_out);
 dspark_status dspark_markov_plan_launch(dspark_markov_plan *plan, dspark_stream_t stream);
 void dspark_markov_plan_destroy(dspark_markov_plan *plan);
+
+/* Allocation-free Markov draft.  The paper has no counterpart: this entry point exists
+ * for callers that cannot call cudaMalloc or hand over device scratch -- for example a
+ * plugin inside a host engine whose device memory is owned by the engine's allocator, or
+ * a latency-critical loop where cudaMalloc's implicit device synchronization is not
+ * acceptable.  It computes exactly what dspark_markov_draft computes (same kernel, same
+ * arguments except the workspace and the debug outputs) and calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   Scratch: a 4352-byte array in the library's static device memory (enough for
+ *   k <= 64 positions; larger k is rejected with DSPARK_ERR_UNSUPPORTED).  Every GPU that
+ *   loads the library holds its own copy until the process exits.  Each call clears it
+ *   (a memset on `stream`) before the kernel.  All calls on one device share that copy:
+ *   calls that overlap on the GPU (for example on two streams with no ordering between
+ *   them) race and give undefined results, so serialize them.  The device status word
+ *   lives in the same array and is not readable by the caller.
+ *   Set-up: the first call on each device (with that device current) looks up the
+ *   array's device address with cudaGetSymbolAddress and caches it; make that first call
+ *   before any stream capture. */
+dspark_status dspark_markov_draft_noalloc(const float *base_logits, const uint16_t *markov_w1,
+                                          const uint16_t *markov_w2, const int32_t *d2t,
+                                          int64_t *prev, int num_reqs, int k, int vocab, int rank,
+                                          int64_t *out_ids, dspark_stream_t stream);
 
 /* =====================================================================================
  * Confidence probe
