@@ -9,7 +9,8 @@ One step = one pass of the whole hot path over one batch of synthetic input:
      (K,N) = (4096,4096), (4096,1024), (4096,12288), (12288,4096)
 
 value = microseconds per step (lower is better), device time from CUDA events around
-each step's work; L2 is flushed (256 MiB write) before every step, outside the events.
+each step's work; L2 is flushed before every step (256 MiB write, then a read of the
+buffer so the write-back of dirty lines is not charged to the step), outside the events.
 `e2e` times the same step through the public API with the step's inputs copied from
 pinned host memory and its outputs copied back, inside the events.  `roofline` is for
 the Markov kernel (the dominant one): algorithmic bytes per launch / mean launch time.
@@ -79,7 +80,8 @@ def config_dict(B):
                      "(12288,4096)"),
         "num_reqs": B, "k": k, "vocab": V, "rank": R, "probes": N_PROBES, "probe_K": 7424,
         "ws_M": 7, "ws_shapes_KN": [list(s) for s in synth.WS_SHAPES],
-        "l2": "flushed before every step (256 MiB write, outside the timed events)",
+        "l2": ("flushed before every step: 256 MiB write then a read of the same buffer, "
+               "so no dirty lines are left; outside the timed events"),
         "timing": "CUDA events on the launch stream around each step's work; mean over steps",
         "parallelism": "replicas",
     }
@@ -217,7 +219,15 @@ def run_gpu(args, rank, world):
     Xs = [torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
     Ys = [torch.empty((7, w["N"]), dtype=torch.float16, device=dev) for w in ws]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(s):
+        """Evict L2 (write a buffer twice its size), then read it back so the lines left
+        behind are clean: otherwise the write-back of ~126 MB of dirty lines would be
+        charged to the first kernel of the timed step."""
+        flush.fill_(s & 0xFF)
+        torch.amax(flush.view(torch.int32), dim=0, out=flush_sink)
 
     def step_work():
         plan.launch(stream)
@@ -230,7 +240,7 @@ def run_gpu(args, rank, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(1)
         step_work()
     torch.cuda.synchronize()
     if api.markov_status(wsp) != 0:
@@ -248,7 +258,7 @@ def run_gpu(args, rank, world):
     clocks.start()
     t0 = time.perf_counter()
     for s in range(args.steps):
-        flush.fill_(s & 0xFF)
+        flush_l2(s)
         e = ev[s]
         e[0].record(stream)
         plan.launch(stream)
@@ -299,12 +309,12 @@ def run_gpu(args, rank, world):
                 yh.copy_(yd, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
-            flush.fill_(2)
+            flush_l2(2)
             e2e_step()
         torch.cuda.synchronize()
         e2e_ms = []
         for s in range(args.steps):
-            flush.fill_(s & 0xFF)
+            flush_l2(s)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)

@@ -7,11 +7,11 @@
 //
 // GB300 design
 //  * One CTA per SM, each owning a fixed contiguous slice of vocab rows for every step.
-//  * A producer warp streams the slice's markov_w2 rows through a 4-stage ring of
-//    32 KB shared-memory tiles with 1-D TMA bulk copies (cp.async.bulk + mbarrier).
+//  * A producer warp streams the slice's markov_w2 rows through a 7-stage ring of
+//    28 KB shared-memory tiles with 1-D TMA bulk copies (cp.async.bulk + mbarrier).
 //    markov_w2 does not depend on prev, so the producer runs ahead across step
 //    boundaries and HBM stays busy while the consumers wait for the step's argmax.
-//  * Eight consumer warps hold h = markov_w1[prev] in registers (fp32, exact from bf16)
+//  * Seven consumer warps hold h = markov_w1[prev] in registers (fp32, exact from bf16)
 //    and evaluate rows with packed fp32x2 FMAs; row sums use a fixed butterfly
 //    (reduce-scatter across the lanes of a row), so every logit is produced in one
 //    order, independent of grid size and num_reqs.
@@ -23,6 +23,7 @@
 //  * A grid-wide barrier (monotonic arrival counter, bounded spin) separates steps;
 //    every CTA then reads the winning key, CTA 0 writes out_ids (through d2t) and, at
 //    the last step, prev.
+#include <cuda/std/type_traits>
 #include <cuda_fp16.h>
 
 #include <new>
@@ -32,11 +33,13 @@
 namespace dspark {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+// 1 producer + 7 consumer warps: 8 warps = 2 per SM sub-partition, so each thread may
+// hold up to 255 registers (a 9th warp would put 3 warps on one 16K-register partition).
+constexpr int kConsumerWarps = 7;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kStages = 4;
-constexpr int kTileBytes = 32768;
+constexpr int kStages = 7;
+constexpr int kTileBytes = 28672;  // 7 x 4 KB: passes divide evenly over 7 warps
 constexpr int kMaxReqs = 8;
 constexpr size_t kHeaderBytes = 256;  // [0] barrier arrivals, [1] status bits
 
@@ -78,7 +81,7 @@ constexpr size_t smem_bytes() {
            16;
 }
 
-template <int R, int NB>
+template <int R, int NB, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a) {
     using G = Geo<R, NB>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -96,6 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
     const int v1 = static_cast<int>(static_cast<long long>(cta + 1) * a.V / nctas);
     const int rows_c = v1 - v0;
     const int ntiles = (rows_c + G::TR - 1) / G::TR;
+    // Odd positions walk the slice backwards, so each position starts on the rows the
+    // previous one touched last -- the ones most likely still in L2.
+    auto tile_at = [ntiles](int i, int t) { return (i & 1) ? ntiles - 1 - t : t; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
     }
     __syncthreads();
 
-    // ---------------- producer warp: stream markov_w2 tiles for every step -------------
+    // ---------------- producer warp: stream markov_w2 tiles for every position ---------
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             uint64_t pol;
@@ -121,10 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
                         atomicOr(a.status, kStatusTimeout);
                         return;
                     }
-                    const int rows = min(G::TR, rows_c - t * G::TR);
+                    const int tt = tile_at(i, t);
+                    const int rows = min(G::TR, rows_c - tt * G::TR);
                     const uint32_t bytes = static_cast<uint32_t>(rows) * R * 2u;
                     mbar_arrive_expect_tx(&full[stage], bytes);
-                    bulk_g2s(ring + size_t(stage) * kTileBytes, a.w2 + size_t(v0 + t * G::TR) * R, bytes,
+                    bulk_g2s(ring + size_t(stage) * kTileBytes, a.w2 + size_t(v0 + tt * G::TR) * R, bytes,
                              &full[stage], pol);
                     if (++stage == kStages) {
                         stage = 0;
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
         }
     }
     if (bad_mask && cta == 0 && threadIdx.x == 0) atomicOr(a.status, kStatusIndex);
+    const bool my_ok = my_req < a.B && !((bad_mask >> my_req) & 1u);
 
     float2 h2[NB][G::CH][4];
     auto load_h = [&]() {
@@ -178,16 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
     };
     load_h();
 
-    // Base-logit values this lane needs for tile (i, t), one per pass.
+    // Base-logit values this lane needs for the t-th tile of position i, one per pass.
     auto load_base = [&](int i, int t, float (&dst)[G::PPW]) {
-        const int tile_rows = min(G::TR, rows_c - t * G::TR);
-        const bool req_ok = my_req < a.B;
+        const int tt = tile_at(i, t);
+        const int tile_rows = min(G::TR, rows_c - tt * G::TR);
+        const float *brow = a.base + (size_t(my_req) * a.k + i) * a.V + (v0 + tt * G::TR);
 #pragma unroll
         for (int pw = 0; pw < G::PPW; ++pw) {
             const int row = (warp + pw * kConsumerWarps) * G::P + slot * G::U + my_u;
-            dst[pw] = 0.f;
-            if (req_ok && row < tile_rows)
-                dst[pw] = __ldg(a.base + (size_t(my_req) * a.k + i) * a.V + (v0 + t * G::TR + row));
+            dst[pw] = (my_ok && row < tile_rows) ? __ldg(brow + row) : 0.f;
         }
     };
 
@@ -195,6 +202,59 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
 #pragma unroll
     for (int pw = 0; pw < G::PPW; ++pw) bnext[pw] = 0.f;
     if (ntiles > 0 && a.k > 0) load_base(0, 0, bnext);
+
+    // All passes of one tile.  FULL: every row of the tile exists (no row guards).
+    auto consume = [&](auto full_tag, const unsigned char *tile, int tile_rows, int vt0, int i,
+                       const float (&bcur)[G::PPW], unsigned long long &best) {
+        constexpr bool FULL = decltype(full_tag)::value;
+#pragma unroll
+        for (int pw = 0; pw < G::PPW; ++pw) {
+            const int pass = warp + pw * kConsumerWarps;
+            if (FULL || pass * G::P < tile_rows) {
+                const int row0 = pass * G::P + slot * G::U;
+                float2 acc[G::U][NB];
+#pragma unroll
+                for (int u = 0; u < G::U; ++u)
+#pragma unroll
+                    for (int r = 0; r < NB; ++r) acc[u][r] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < G::U; ++u) {
+#pragma unroll
+                    for (int c = 0; c < G::CH; ++c) {
+                        const uint4 wv = *reinterpret_cast<const uint4 *>(
+                            tile + size_t(row0 + u) * (R * 2) + (c * (G::LPR * 8) + q * 8) * 2);
+                        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 wf = bf16x2_to_float2(words[e]);
+#pragma unroll
+                            for (int r = 0; r < NB; ++r) acc[u][r] = __ffma2_rn(wf, h2[r][c][e], acc[u][r]);
+                        }
+                    }
+                }
+                float vals[G::VALS];
+#pragma unroll
+                for (int u = 0; u < G::U; ++u)
+#pragma unroll
+                    for (int r = 0; r < NB; ++r) vals[u * NB + r] = acc[u][r].x + acc[u][r].y;
+                ReduceScatter<G::VALS, G::LPR / 2>::run(vals, lane);
+                const float bias = vals[0];
+                const int row = row0 + my_u;
+                const bool valid = my_ok && (FULL || row < tile_rows);
+                const float logit = bcur[pw] + bias;
+                const int v = vt0 + row;
+                const unsigned long long key = argmax_key(logit, static_cast<uint32_t>(v));
+                best = (valid && key > best) ? key : best;
+                if constexpr (DBG) {
+                    if (valid) {
+                        const size_t o = (size_t(my_req) * a.k + i) * a.V + v;
+                        if (a.dbg_logits) a.dbg_logits[o] = logit;
+                        if (a.dbg_bias) a.dbg_bias[o] = bias;
+                    }
+                }
+            }
+        }
+    };
 
     int stage = 0;
     uint32_t phase = 0;
@@ -227,54 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
                 broken = true;
             }
             if (!aborted && !broken) {
-                const int tile_rows = min(G::TR, rows_c - t * G::TR);
+                const int tt = tile_at(i, t);
+                const int tile_rows = min(G::TR, rows_c - tt * G::TR);
                 const unsigned char *tile = ring + size_t(stage) * kTileBytes;
-#pragma unroll
-                for (int pw = 0; pw < G::PPW; ++pw) {
-                    const int pass = warp + pw * kConsumerWarps;
-                    if (pass * G::P < tile_rows) {
-                        const int row0 = pass * G::P + slot * G::U;
-                        float2 acc[G::U][NB];
-#pragma unroll
-                        for (int u = 0; u < G::U; ++u)
-#pragma unroll
-                            for (int r = 0; r < NB; ++r) acc[u][r] = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int u = 0; u < G::U; ++u) {
-#pragma unroll
-                            for (int c = 0; c < G::CH; ++c) {
-                                const uint4 wv = *reinterpret_cast<const uint4 *>(
-                                    tile + size_t(row0 + u) * (R * 2) + (c * (G::LPR * 8) + q * 8) * 2);
-                                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 wf = bf16x2_to_float2(words[e]);
-#pragma unroll
-                                    for (int r = 0; r < NB; ++r) acc[u][r] = __ffma2_rn(wf, h2[r][c][e], acc[u][r]);
-                                }
-                            }
-                        }
-                        float vals[G::VALS];
-#pragma unroll
-                        for (int u = 0; u < G::U; ++u)
-#pragma unroll
-                            for (int r = 0; r < NB; ++r) vals[u * NB + r] = acc[u][r].x + acc[u][r].y;
-                        ReduceScatter<G::VALS, G::LPR / 2>::run(vals, lane);
-                        const float bias = vals[0];
-                        const int row = row0 + my_u;
-                        if (row < tile_rows && my_req < a.B && !((bad_mask >> my_req) & 1u)) {
-                            const float logit = bcur[pw] + bias;
-                            const int v = v0 + t * G::TR + row;
-                            const unsigned long long key = argmax_key(logit, static_cast<uint32_t>(v));
-                            best = key > best ? key : best;
-                            if (a.dbg_logits || a.dbg_bias) {
-                                const size_t o = (size_t(my_req) * a.k + i) * a.V + v;
-                                if (a.dbg_logits) a.dbg_logits[o] = logit;
-                                if (a.dbg_bias) a.dbg_bias[o] = bias;
-                            }
-                        }
-                    }
-                }
+                if (tile_rows == G::TR)
+                    consume(cuda::std::true_type{}, tile, tile_rows, v0 + tt * G::TR, i, bcur, best);
+                else
+                    consume(cuda::std::false_type{}, tile, tile_rows, v0 + tt * G::TR, i, bcur, best);
             }
             __syncwarp();
             if (lane == 0 && !broken) mbar_arrive(&empty[stage]);
@@ -285,28 +304,30 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
         }
         if (aborted) continue;  // keep draining the ring; no more barriers
 
-        // ---- end of step: CTA reduction, global max, grid barrier, winner -------------
-        if (my_req < a.B && best != 0ull) atomicMax(&s_best[my_req], best);
-        named_bar_sync(1, kConsumerThreads);
-        if (threadIdx.x < a.B) {
-            const unsigned long long k_cta = s_best[threadIdx.x];
-            if (k_cta != 0ull) atomicMax(&a.best[size_t(i) * kMaxReqs + threadIdx.x], k_cta);
-            s_best[threadIdx.x] = 0ull;
-        }
+        // ---- end of position: CTA max, global max, grid barrier, winner ----------------
+        if (my_ok && best != 0ull) atomicMax(&s_best[my_req], best);
         named_bar_sync(1, kConsumerThreads);
         if (threadIdx.x == 0) {
+            // one thread publishes the CTA's keys, then arrives: its release orders them
+            for (int r = 0; r < a.B; ++r) {
+                const unsigned long long k_cta = s_best[r];
+                if (k_cta != 0ull) atomicMax(&a.best[size_t(i) * kMaxReqs + r], k_cta);
+                s_best[r] = 0ull;
+            }
             __threadfence();
             red_release_add_u32(a.bar_count, 1u);
             const unsigned target = static_cast<unsigned>(nctas) * static_cast<unsigned>(i + 1) + a.bar_extra;
-            if (ld_acquire_u32(a.bar_count) < target) {
-                const unsigned long long t0 = global_timer_ns();
-                while (ld_acquire_u32(a.bar_count) < target) {
+            unsigned spins = 0;
+            unsigned long long t0 = 0;
+            while (ld_acquire_u32(a.bar_count) < target) {
+                if (++spins > 256) {
+                    if (t0 == 0) t0 = global_timer_ns();
                     if (global_timer_ns() - t0 > a.timeout_ns) {
                         atomicOr(a.status, kStatusTimeout);
-                        *s_abort = 1;
+                        *reinterpret_cast<volatile int *>(s_abort) = 1;
                         break;
                     }
-                    __nanosleep(64);
+                    __nanosleep(32);
                 }
             }
             __threadfence();
@@ -324,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
                 cur[r] = key ? static_cast<int>(argmax_key_index(key)) : 0;
             }
         }
+        if (i + 1 < a.k) load_h();
         if (cta == 0 && threadIdx.x < a.B) {
             const int r = threadIdx.x;
             long long out = -1;
@@ -346,13 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) markov_draft_kernel(MarkovArgs a)
             }
             a.out_ids[size_t(r) * a.k + i] = out;
         }
-        if (i + 1 < a.k) load_h();
     }
 }
 
-template <int R, int NB>
+template <int R, int NB, bool DBG>
 dspark_status launch_markov(const MarkovArgs &args, int nctas, cudaStream_t stream) {
-    auto kern = markov_draft_kernel<R, NB>;
+    auto kern = markov_draft_kernel<R, NB, DBG>;
     static bool configured = false;  // per-process: the attribute is set on every device used
     static int configured_dev = -1;
     int dev = 0;
@@ -383,12 +404,18 @@ dspark_status launch_markov(const MarkovArgs &args, int nctas, cudaStream_t stre
     return DSPARK_OK;
 }
 
+template <int R, bool DBG>
+dspark_status launch_reqs(const MarkovArgs &args, int nctas, cudaStream_t stream) {
+    if (args.B <= 1) return launch_markov<R, 1, DBG>(args, nctas, stream);
+    if (args.B <= 2) return launch_markov<R, 2, DBG>(args, nctas, stream);
+    if (args.B <= 4) return launch_markov<R, 4, DBG>(args, nctas, stream);
+    return launch_markov<R, 8, DBG>(args, nctas, stream);
+}
+
 template <int R>
 dspark_status launch_rank(const MarkovArgs &args, int nctas, cudaStream_t stream) {
-    if (args.B <= 1) return launch_markov<R, 1>(args, nctas, stream);
-    if (args.B <= 2) return launch_markov<R, 2>(args, nctas, stream);
-    if (args.B <= 4) return launch_markov<R, 4>(args, nctas, stream);
-    return launch_markov<R, 8>(args, nctas, stream);
+    if (args.dbg_logits || args.dbg_bias) return launch_reqs<R, true>(args, nctas, stream);
+    return launch_reqs<R, false>(args, nctas, stream);
 }
 
 size_t workspace_bytes(int k) {

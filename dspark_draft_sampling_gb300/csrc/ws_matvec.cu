@@ -8,15 +8,17 @@
 // GB300 design
 //  * Persistent grid (at most one CTA per SM); CTA c owns the contiguous output rows
 //    [c*N/G, (c+1)*N/G), processed in groups of TN rows.
-//  * A producer warp streams each group's W rows through a 4-stage shared-memory ring
-//    with 1-D TMA bulk copies: one stage = TN rows x 2048 k-elements (32 KB at TN = 8).
-//  * Eight consumer warps split each stage's k-range (warp w: 256 elements, 8 per lane);
-//    every weight element is converted to fp32 once and multiplied into all M rows with
-//    packed fp32x2 FMAs (two rows of X per instruction).  X (a few tens of KB) is read
-//    through L1/L2 and converted once per stage.
+//  * Each group's W rows stream through a 6-stage shared-memory ring with 1-D TMA bulk
+//    copies (one stage = TN rows x 2048 k-elements, 32 KB at TN = 8), issued by lane 0 of
+//    warp 0 between its own tiles.
+//  * Eight warps split each stage's k-range (warp w: 256 elements, 8 per lane);
+//    every weight pair is converted to fp32 once and multiplied into all M rows with
+//    packed fp32x2 FMAs over (even k, odd k) pairs, so operands are used as loaded.  X (a
+//    few tens of KB) is read through L1/L2 and converted once per stage and row group.
 //  * Lane partials are combined by a fixed butterfly, warp partials by an in-order sum
 //    in shared memory: each output has one summation order, independent of M, N and the
 //    grid size.
+#include <cuda/std/type_traits>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -24,10 +26,13 @@
 namespace dspark {
 namespace {
 
+// 8 warps = 2 per SM sub-partition, so a thread may hold up to 255 registers.  All 8 warps
+// compute; lane 0 of warp 0 also issues the TMA copies (no dedicated producer warp, which
+// would put a third warp on one sub-partition and cap registers at 168).
 constexpr int kWarpsC = 8;
 constexpr int kThreadsC = kWarpsC * 32;
-constexpr int kThreads = kThreadsC + 32;
-constexpr int kStages = 4;
+constexpr int kThreads = kThreadsC;
+constexpr int kStages = 6;
 constexpr int kKC = kWarpsC * 256;  // k-elements per stage
 
 struct WsArgs {
@@ -36,13 +41,12 @@ struct WsArgs {
     void *Y;
     int y_fp32;
     int M, N, K;
-    unsigned *status;  // unused for now (no cross-CTA waits); kept null
     unsigned long long timeout_ns;
 };
 
 template <int TN>
-constexpr size_t ws_smem_bytes(int mp) {
-    return size_t(kStages) * TN * kKC * 2 + size_t(kWarpsC) * TN * mp * sizeof(float) +
+constexpr size_t ws_smem_bytes(int mt) {
+    return size_t(kStages) * TN * kKC * 2 + size_t(kWarpsC) * 64 * sizeof(float) * ((TN * mt + 63) / 64) +
            2 * kStages * sizeof(uint64_t) + 16;
 }
 
@@ -51,14 +55,33 @@ __device__ __forceinline__ float2 h2f(uint32_t w) {
     return __half22float2(h);
 }
 
-template <int MP, int TN>
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr int pow2_at_least(int n) {
+    int p = 1;
+    while (p < n) p *= 2;
+    return p;
+}
+
+template <int MT, int TN>
 __global__ void __launch_bounds__(kThreads, 1) ws_matvec_kernel(WsArgs a) {
-    constexpr int SB = TN * kKC * 2;  // stage bytes
-    constexpr int NV = TN * MP;       // partial sums per lane
+    constexpr int SB = TN * kKC * 2;        // stage bytes
+    constexpr int NV = TN * MT;             // partial sums per lane
+    constexpr int NVP = pow2_at_least(NV);  // padded for the butterfly
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *ring = smem;
-    float *red = reinterpret_cast<float *>(smem + size_t(kStages) * SB);  // [kWarpsC][NV]
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + kWarpsC * NV);
+    float *red = reinterpret_cast<float *>(smem + size_t(kStages) * SB);  // [kWarpsC][NVP]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + kWarpsC * NVP);
     uint64_t *empty = full + kStages;
 
     const int warp = threadIdx.x >> 5;
@@ -70,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_kernel(WsArgs a) {
     const int rows_c = n1 - n0;
     const int ngroups = (rows_c + TN - 1) / TN;
     const int nkc = (a.K + kKC - 1) / kKC;
+    const int ntiles = ngroups * nkc;  // tile j = (group j / nkc, k-chunk j % nkc)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -80,51 +104,89 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_kernel(WsArgs a) {
     }
     __syncthreads();
 
-    if (warp == kWarpsC) {  // producer
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int g = 0; g < ngroups; ++g) {
-                const int vrows = min(TN, rows_c - g * TN);
-                for (int kc = 0; kc < nkc; ++kc) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, a.timeout_ns)) return;
-                    const int klen = min(kKC, a.K - kc * kKC);
-                    const uint32_t row_bytes = static_cast<uint32_t>(klen) * 2u;
-                    mbar_arrive_expect_tx(&full[stage], row_bytes * vrows);
-                    for (int t = 0; t < vrows; ++t)
-                        bulk_g2s(ring + size_t(stage) * SB + size_t(t) * kKC * 2,
-                                 a.W + size_t(n0 + g * TN + t) * a.K + size_t(kc) * kKC, row_bytes, &full[stage],
-                                 pol);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+    // ---- producer duty of thread 0: tile j goes to stage j % kStages once tile
+    // j - kStages has been released by all warps (phase (j / kStages) - 1 of empty).
+    const bool producer = threadIdx.x == 0;
+    uint64_t pol = 0;
+    if (producer) pol = l2_policy_evict_first();
+    int issued = 0;
+    bool broken = false;  // a wait timed out: stop waiting (results undefined, nothing hangs)
+    auto issue = [&](int j) {
+        const int g = j / nkc, kc = j % nkc, st = j % kStages;
+        const int vrows = min(TN, rows_c - g * TN);
+        const int klen = min(kKC, a.K - kc * kKC);
+        const uint32_t row_bytes = static_cast<uint32_t>(klen) * 2u;
+        mbar_arrive_expect_tx(&full[st], row_bytes * vrows);
+        for (int t = 0; t < vrows; ++t)
+            bulk_g2s(ring + size_t(st) * SB + size_t(t) * kKC * 2,
+                     a.W + size_t(n0 + g * TN + t) * a.K + size_t(kc) * kKC, row_bytes, &full[st], pol);
+    };
+    auto refill = [&](int j) {  // thread 0: make sure tile j is issued, then top up the ring
+        while (!broken && issued <= j) {
+            if (!mbar_wait(&empty[issued % kStages], ((issued / kStages) & 1) ^ 1, a.timeout_ns)) {
+                broken = true;
+                break;
+            }
+            issue(issued++);
+        }
+        while (!broken && issued < ntiles && issued < j + kStages &&
+               mbar_test_wait(&empty[issued % kStages], ((issued / kStages) & 1) ^ 1))
+            issue(issued++);
+    };
+
+    const int M = a.M;
+    const int kl = warp * 256 + lane * 8;  // this lane's k offset inside a stage
+
+    // One stage: this lane's 8 k-elements of TN weight rows against MT rows of X.
+    // acc[t][m] holds (sum over even k, sum over odd k): one fp32x2 FMA consumes a
+    // weight pair and an activation pair exactly as they sit in memory.
+    auto stage_fma = [&](auto full_tag, const unsigned char *st, int vrows, const uint32_t (&xh)[MT][4],
+                         float2 (&acc)[TN][MT]) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        uint32_t wh[TN][4];
+#pragma unroll
+        for (int t = 0; t < TN; ++t) {
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (FULL || t < vrows) u = *reinterpret_cast<const uint4 *>(st + size_t(t) * kKC * 2 + size_t(kl) * 2);
+            wh[t][0] = u.x;
+            wh[t][1] = u.y;
+            wh[t][2] = u.z;
+            wh[t][3] = u.w;
+        }
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+            float2 xp[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) xp[m] = h2f(xh[m][e2]);
+#pragma unroll
+            for (int t = 0; t < TN; ++t) {
+                if (FULL || t < vrows) {
+                    const float2 wp = h2f(wh[t][e2]);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) acc[t][m] = __ffma2_rn(wp, xp[m], acc[t][m]);
                 }
             }
         }
-        return;
-    }
+    };
 
-    int stage = 0;
-    uint32_t phase = 0;
-    bool broken = false;  // a tile wait timed out: wait on no further tiles (results undefined)
-    const int M = a.M;
+    int j = 0;  // tile index
+    bool wbroken = false;  // this warp stopped waiting on tiles
     for (int g = 0; g < ngroups; ++g) {
         const int vrows = min(TN, rows_c - g * TN);
-        float2 acc[TN][MP / 2];
+        float2 acc[TN][MT];
 #pragma unroll
         for (int t = 0; t < TN; ++t)
 #pragma unroll
-            for (int mp = 0; mp < MP / 2; ++mp) acc[t][mp] = make_float2(0.f, 0.f);
+            for (int m = 0; m < MT; ++m) acc[t][m] = make_float2(0.f, 0.f);
 
-        for (int kc = 0; kc < nkc; ++kc) {
-            const int kl = warp * 256 + lane * 8;  // this lane's k offset inside the stage
+        for (int kc = 0; kc < nkc; ++kc, ++j) {
+            const int st = j % kStages;
+            const uint32_t ph = (j / kStages) & 1;
             const int k0 = kc * kKC + kl;
             const bool active = k0 < a.K;
-            uint32_t xh[MP][4];
+            uint32_t xh[MT][4];
 #pragma unroll
-            for (int m = 0; m < MP; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 uint4 u = make_uint4(0u, 0u, 0u, 0u);
                 if (active && m < M) u = *reinterpret_cast<const uint4 *>(a.X + size_t(m) * a.K + k0);
                 xh[m][0] = u.x;
@@ -132,94 +194,65 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_kernel(WsArgs a) {
                 xh[m][2] = u.z;
                 xh[m][3] = u.w;
             }
-            if (!broken && !mbar_wait(&full[stage], phase, a.timeout_ns)) broken = true;
-            if (active && !broken) {
-                const unsigned char *st = ring + size_t(stage) * SB;
-                uint32_t wh[TN][4];
-#pragma unroll
-                for (int t = 0; t < TN; ++t) {
-                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                    if (t < vrows) u = *reinterpret_cast<const uint4 *>(st + size_t(t) * kKC * 2 + size_t(kl) * 2);
-                    wh[t][0] = u.x;
-                    wh[t][1] = u.y;
-                    wh[t][2] = u.z;
-                    wh[t][3] = u.w;
-                }
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    float2 xe[MP / 2], xo[MP / 2];
-#pragma unroll
-                    for (int mp = 0; mp < MP / 2; ++mp) {
-                        const float2 f0 = h2f(xh[2 * mp][e2]);
-                        const float2 f1 = h2f(xh[2 * mp + 1][e2]);
-                        xe[mp] = make_float2(f0.x, f1.x);
-                        xo[mp] = make_float2(f0.y, f1.y);
-                    }
-#pragma unroll
-                    for (int t = 0; t < TN; ++t) {
-                        if (t < vrows) {
-                            const float2 wf = h2f(wh[t][e2]);
-                            const float2 wa = make_float2(wf.x, wf.x);
-                            const float2 wb = make_float2(wf.y, wf.y);
-#pragma unroll
-                            for (int mp = 0; mp < MP / 2; ++mp) {
-                                acc[t][mp] = __ffma2_rn(wa, xe[mp], acc[t][mp]);
-                                acc[t][mp] = __ffma2_rn(wb, xo[mp], acc[t][mp]);
-                            }
-                        }
-                    }
-                }
+            if (producer) refill(j);
+            __syncwarp();
+            if (!wbroken && !mbar_wait(&full[st], ph, a.timeout_ns)) wbroken = true;
+            if (active && !wbroken) {
+                const unsigned char *sp = ring + size_t(st) * SB;
+                if (vrows == TN)
+                    stage_fma(cuda::std::true_type{}, sp, vrows, xh, acc);
+                else
+                    stage_fma(cuda::std::false_type{}, sp, vrows, xh, acc);
             }
             __syncwarp();
-            if (lane == 0 && !broken) mbar_arrive(&empty[stage]);
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            if (lane == 0 && !wbroken) mbar_arrive(&empty[st]);
         }
 
-        float vals[NV];
+        float vals[NVP];
 #pragma unroll
         for (int t = 0; t < TN; ++t)
 #pragma unroll
-            for (int mp = 0; mp < MP / 2; ++mp) {
-                vals[t * MP + 2 * mp] = acc[t][mp].x;
-                vals[t * MP + 2 * mp + 1] = acc[t][mp].y;
-            }
-        ReduceScatter<NV, 16>::run(vals, lane);
-        constexpr int LEFT = rs_values_left<NV, 16>();
-        const int first = rs_first_index<NV, 16>(lane);
+            for (int m = 0; m < MT; ++m) vals[t * MT + m] = acc[t][m].x + acc[t][m].y;
 #pragma unroll
-        for (int j = 0; j < LEFT; ++j) red[warp * NV + first + j] = vals[j];
-        named_bar_sync(1, kThreadsC);
+        for (int q = NV; q < NVP; ++q) vals[q] = 0.f;
+        ReduceScatter<NVP, 16>::run(vals, lane);
+        constexpr int LEFT = rs_values_left<NVP, 16>();
+        const int first = rs_first_index<NVP, 16>(lane);
+#pragma unroll
+        for (int q = 0; q < LEFT; ++q) red[warp * NVP + first + q] = vals[q];
+        __syncthreads();
         for (int idx = threadIdx.x; idx < NV; idx += kThreadsC) {
-            const int t = idx / MP;
-            const int m = idx % MP;
+            const int t = idx / MT;
+            const int m = idx % MT;
             if (t < vrows && m < M) {
-                float s = red[idx];
+                float sum = red[idx];
 #pragma unroll
-                for (int w = 1; w < kWarpsC; ++w) s += red[w * NV + idx];
+                for (int w = 1; w < kWarpsC; ++w) sum += red[w * NVP + idx];
                 const size_t o = size_t(m) * a.N + (n0 + g * TN + t);
                 if (a.y_fp32)
-                    static_cast<float *>(a.Y)[o] = s;
+                    static_cast<float *>(a.Y)[o] = sum;
                 else
-                    static_cast<__half *>(a.Y)[o] = __float2half_rn(s);
+                    static_cast<__half *>(a.Y)[o] = __float2half_rn(sum);
             }
         }
-        named_bar_sync(1, kThreadsC);
+        __syncthreads();
     }
 }
 
-template <int MP, int TN>
+template <int MT, int TN>
 dspark_status launch_ws(const WsArgs &args, int nctas, cudaStream_t stream) {
-    auto kern = ws_matvec_kernel<MP, TN>;
-    const size_t smem = ws_smem_bytes<TN>(MP);
+    auto kern = ws_matvec_kernel<MT, TN>;
+    const size_t smem = ws_smem_bytes<TN>(MT);
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
+        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
         configured_dev = dev;
     }
     kern<<<nctas, kThreads, smem, stream>>>(args);
@@ -253,12 +286,18 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     args.M = M;
     args.N = N;
     args.K = K;
-    args.status = nullptr;
     args.timeout_ns = kDefaultTimeoutNs;
     const int nctas = N < sms ? N : sms;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (M <= 2) return launch_ws<2, 8>(args, nctas, s);
-    if (M <= 4) return launch_ws<4, 8>(args, nctas, s);
-    if (M <= 8) return launch_ws<8, 8>(args, nctas, s);
-    return launch_ws<16, 4>(args, nctas, s);
+    switch (M) {
+        case 1: return launch_ws<1, 8>(args, nctas, s);
+        case 2: return launch_ws<2, 8>(args, nctas, s);
+        case 3: return launch_ws<3, 8>(args, nctas, s);
+        case 4: return launch_ws<4, 8>(args, nctas, s);
+        case 5: return launch_ws<5, 8>(args, nctas, s);
+        case 6: return launch_ws<6, 8>(args, nctas, s);
+        case 7: return launch_ws<7, 8>(args, nctas, s);
+        case 8: return launch_ws<8, 8>(args, nctas, s);
+        default: return launch_ws<16, 2>(args, nctas, s);
+    }
 }
