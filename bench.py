@@ -218,6 +218,7 @@ def run_gpu(args, rank, world):
     Ws = [torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
     Xs = [torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
     Ys = [torch.empty((7, w["N"]), dtype=torch.float16, device=dev) for w in ws]
+    WSs = [api.new_ws_workspace(7, w["N"], w["K"], dev) for w in ws]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_sink = torch.empty((), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -233,8 +234,8 @@ def run_gpu(args, rank, world):
         plan.launch(stream)
         api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
                        stream=stream)
-        for W, X, Y in zip(Ws, Xs, Ys):
-            api.ws_matvec(W, X, out=Y, stream=stream)
+        for W, X, Y, WS in zip(Ws, Xs, Ys, WSs):
+            api.ws_matvec(W, X, out=Y, workspace=WS, stream=stream)
 
     kernels_per_step = 1 + 1 + len(Ws)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -266,8 +267,8 @@ def run_gpu(args, rank, world):
         api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
                        stream=stream)
         e[2].record(stream)
-        for W, X, Y in zip(Ws, Xs, Ys):
-            api.ws_matvec(W, X, out=Y, stream=stream)
+        for W, X, Y, WS in zip(Ws, Xs, Ys, WSs):
+            api.ws_matvec(W, X, out=Y, workspace=WS, stream=stream)
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier()

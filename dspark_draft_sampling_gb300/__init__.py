@@ -13,4 +13,5 @@ from .api import (  # noqa: F401
     markov_draft,
     markov_workspace_bytes,
     ws_matvec,
+    ws_matvec_workspace_bytes,
 )

@@ -34,7 +34,8 @@ SIGNATURES = {
     "dspark_markov_plan_launch": (_I, [_P, _P]),
     "dspark_markov_plan_destroy": (None, [_P]),
     "dspark_conf_probe": (_I, [_P, _P, _F, _F, _I, _I, _P, _P, _P]),
-    "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
+    "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
 }
 
 _lock = threading.Lock()
@@ -230,20 +231,35 @@ def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gat
     return logit_out, gate_out
 
 
-def ws_matvec(W, X, *, out=None, out_fp32: bool = False, stream=None):
+def ws_matvec_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().dspark_ws_matvec_workspace_bytes(M, N, K))
+
+
+def new_ws_workspace(M: int, N: int, K: int, device=None):
+    n = ws_matvec_workspace_bytes(M, N, K)
+    if n == 0:
+        raise DsparkError(DSPARK_ERR_CUDA, "could not size the ws_matvec workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def ws_matvec(W, X, *, out=None, out_fp32: bool = False, workspace=None, stream=None):
     """Y = X W^T.  W fp16 [N, K], X fp16 [M, K]; returns Y [M, N] (fp16, or fp32)."""
     lib = load_library()
     N, K = W.shape
     M, K2 = X.shape
     if K != K2:
         raise ValueError("W and X disagree on K")
+    w_p = _ptr(W, "W", itemsize=2, dtypes=_BITS16)
+    x_p = _ptr(X, "X", itemsize=2, dtypes=_BITS16)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32 if out_fp32 else torch.float16,
                           device=W.device)
+    if workspace is None:
+        workspace = new_ws_workspace(M, N, K, W.device)
     y_fp32 = out.dtype == torch.float32
-    st = lib.dspark_ws_matvec(_ptr(W, "W", itemsize=2, dtypes=_BITS16),
-                              _ptr(X, "X", itemsize=2, dtypes=_BITS16),
+    st = lib.dspark_ws_matvec(w_p, x_p,
                               _ptr(out, "out", dtypes=(torch.float16, torch.float32)),
-                              1 if y_fp32 else 0, M, N, K, _stream(stream))
+                              1 if y_fp32 else 0, M, N, K,
+                              _ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
     _check(lib, st)
     return out

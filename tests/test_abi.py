@@ -109,15 +109,18 @@ def test_probe_validation(dspark_lib):
 def test_ws_validation(dspark_lib):
     lib = dspark_lib
     f = lib.dspark_ws_matvec
-    assert f(FAKE, FAKE, FAKE, 0, 17, 64, 64, NULL) == UNSUPPORTED
-    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 12, NULL) == INVALID
-    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 0, NULL) == INVALID
-    assert f(FAKE, FAKE, FAKE, 0, -1, 64, 64, NULL) == INVALID
-    assert f(NULL, FAKE, FAKE, 0, 7, 64, 64, NULL) == INVALID
-    assert f(FAKE_ODD, FAKE, FAKE, 0, 7, 64, 64, NULL) == INVALID
-    assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 0, 7, 64, 64, NULL) == INVALID
-    assert f(FAKE, FAKE, FAKE, 1, 0, 64, 64, NULL) == 0
-    assert f(FAKE, FAKE, FAKE, 1, 7, 0, 64, NULL) == 0
+    B = 1 << 20
+    assert f(FAKE, FAKE, FAKE, 0, 17, 64, 64, FAKE, B, NULL) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 12, FAKE, B, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 0, FAKE, B, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, -1, 64, 64, FAKE, B, NULL) == INVALID
+    assert f(NULL, FAKE, FAKE, 0, 7, 64, 64, FAKE, B, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 64, NULL, B, NULL) == INVALID
+    assert f(FAKE_ODD, FAKE, FAKE, 0, 7, 64, 64, FAKE, B, NULL) == INVALID
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 0, 7, 64, 64, FAKE, B, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 0, 7, 64, 64, FAKE_ODD, B, NULL) == INVALID
+    assert f(FAKE, FAKE, FAKE, 1, 0, 64, 64, FAKE, B, NULL) == 0
+    assert f(FAKE, FAKE, FAKE, 1, 7, 0, 64, FAKE, B, NULL) == 0
 
 
 def test_python_binding_rejects_cpu_tensors(dspark_lib):
