@@ -16,7 +16,7 @@ SRC_DIR = os.path.join(PKG_DIR, "csrc")
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libdspark.so"
-SOURCES = ["common.cu", "markov.cu", "probe.cu", "ws_matvec.cu"]
+SOURCES = ["common.cu", "markov.cu", "markov_tc.cu", "probe.cu", "ws_matvec.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,7 +45,8 @@ def _stale(out: str, deps) -> bool:
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    headers = [os.path.join(SRC_DIR, "common.cuh"), os.path.join(INCLUDE_DIR, "dspark.h")]
+    headers = [os.path.join(SRC_DIR, h) for h in ("common.cuh", "markov.cuh", "tc.cuh")]
+    headers.append(os.path.join(INCLUDE_DIR, "dspark.h"))
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE_DIR, "--expt-relaxed-constexpr"]
     if verbose_ptxas:

@@ -76,17 +76,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     return true;
 }
 
-// 1-D bulk copy global -> shared (TMA engine); completion is counted in bytes on `bar`.
-// dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
-                                         uint64_t l2_policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            smem_addr(dst_smem)),
-        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(l2_policy)
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -129,11 +118,6 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     return r;
 }
 
-// bf16 pair (lower address in the low half) -> two exact fp32 values.
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
 // Order-preserving map of an fp32 value to uint32 (-0 is first folded onto +0, so
 // equal values map to equal codes).  Larger float -> larger code.
 __device__ __forceinline__ uint32_t float_order_code(float x) {
@@ -150,55 +134,6 @@ __device__ __forceinline__ unsigned long long argmax_key(float logit, uint32_t i
 
 __device__ __forceinline__ uint32_t argmax_key_index(unsigned long long key) {
     return 0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull);
-}
-
-// Reduce-scatter of N per-lane values over the lane groups that differ in the bits
-// O, O/2, ..., 1 of the lane index (a butterfly).  Each value is summed over the same
-// fixed tree (partner lanes combined in the order O, O/2, ..., 1), so its result does
-// not depend on N.  While more than one value remains, the lane whose bit is set keeps
-// the upper half.  Afterwards v[0 .. max(1, N >> log2(2*O)) - 1] hold complete sums
-// of a contiguous block of value indices (see rs_first_index).
-template <int N, int O>
-struct ReduceScatter {
-    static __device__ __forceinline__ void run(float *v, int lane) {
-        if constexpr (O == 0) {
-            return;
-        } else if constexpr (N > 1) {
-            const bool up = (lane & O) != 0;
-#pragma unroll
-            for (int t = 0; t < N / 2; ++t) {
-                const float send = up ? v[t] : v[t + N / 2];
-                const float keep = up ? v[t + N / 2] : v[t];
-                v[t] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-            }
-            ReduceScatter<N / 2, O / 2>::run(v, lane);
-        } else {
-            v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], O);
-            ReduceScatter<1, O / 2>::run(v, lane);
-        }
-    }
-};
-
-// Index of the first value a lane holds after ReduceScatter<N, O>.
-template <int N, int O>
-__device__ __forceinline__ int rs_first_index(int lane) {
-    int vi = 0, n = N;
-#pragma unroll
-    for (int o = O; o >= 1; o >>= 1) {
-        if (n > 1) {
-            if (lane & o) vi += n / 2;
-            n /= 2;
-        }
-    }
-    return vi;
-}
-
-template <int N, int O>
-constexpr int rs_values_left() {
-    int n = N;
-    for (int o = O; o >= 1; o >>= 1)
-        if (n > 1) n /= 2;
-    return n;
 }
 
 }  // namespace dspark

@@ -1,0 +1,31 @@
+// Shared definitions of the Markov block-draft kernels (CUDA-core and tcgen05 forms).
+#pragma once
+
+#include "common.cuh"
+
+namespace dspark {
+
+constexpr int kMaxReqs = 8;
+constexpr size_t kHeaderBytes = 256;  // workspace header: [0] barrier arrivals, [1] status bits
+
+struct MarkovArgs {
+    const float *base;
+    const uint16_t *w1;
+    const uint16_t *w2;
+    const int32_t *d2t;
+    int64_t *prev;
+    int64_t *out_ids;
+    float *dbg_logits;
+    float *dbg_bias;
+    unsigned *bar_count;
+    unsigned *status;
+    unsigned long long *best;  // [k][kMaxReqs] winning keys
+    int B, k, V;
+    unsigned bar_extra;
+    unsigned long long timeout_ns;
+};
+
+// tcgen05 form (markov_tc.cu): one CTA per SM, cooperative launch.
+dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,374 @@
+// Markov block draft with the bias GEMV on tcgen05 tensor cores.
+//
+// Method (vllm.cpp issue #436 "SPEC-DSPARK W7", section "The fix"): per draft position,
+// gather markov_w1[prev], bias GEMV over the whole bf16 markov_w2 [vocab, rank], add the
+// position's base-logit row, greedy argmax with lowest-index tie-break, d2t map, prev kept
+// on the device.
+//
+// The bias of one vocab row for all requests is the row of markov_w2 times the matrix
+// H = [markov_w1[prev_0]; ...; markov_w1[prev_{B-1}]]: a [vocab x rank] x [rank x B] product.
+// Here it runs on the 5th-generation tensor cores; the SMs only stream markov_w2 and do the
+// argmax epilogue, so the cost no longer grows with the number of requests.
+//
+// GB300 design (one persistent CTA per SM, cooperative launch for the step barrier)
+//  * CTA c owns a contiguous range of 128-row tiles of markov_w2 for every position; odd
+//    positions walk it backwards so each position starts on rows still in L2.
+//  * Warp 4 (one thread): 2-D TMA tensor copies of [128 rows x 64 k] bf16 boxes (16 KB,
+//    128-byte swizzle) into a 12-stage ring.  markov_w2 does not depend on prev, so it
+//    runs ahead across position boundaries.
+//  * Warp 5: allocates 32 TMEM columns (two 128 x 16 fp32 accumulators); one thread
+//    issues, per box, four tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows,
+//    N = 16 request slots, K = 16) against H, which the epilogue warps write into shared
+//    memory in the same swizzled layout (rows >= num_reqs stay zero).
+//  * Warps 0-3 (thread = TMEM lane = vocab row of the tile): tcgen05.ld the accumulator,
+//    add the base logits, keep the best (value, lowest index) key per request; at the end
+//    of a position reduce keys (warp shuffles, shared atomicMax, one global atomicMax per
+//    request), pass the grid barrier, read the winners, write out_ids / prev and build the
+//    next position's H from markov_w1.
+// Products of bf16 values are exact in fp32; the tensor core accumulates in fp32.  Every
+// row's sum is computed the same way regardless of the grid and of num_reqs.
+#include "markov.cuh"
+#include "tc.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
+constexpr int kEpiThreads = 128;
+constexpr int kTileRows = 128;
+constexpr int kKB = 64;                            // k per box (128 B of bf16)
+constexpr int kBoxBytes = kTileRows * kKB * 2;     // 16 KB
+constexpr int kStages = 12;
+constexpr int kNPad = 16;                          // MMA N: request slots
+constexpr int kHBlockBytes = kNPad * kKB * 2;      // 2 KB per k-block of H
+constexpr int kHMaxBytes = 4 * kHBlockBytes;       // rank <= 256
+constexpr uint32_t kTmemCols = 32;
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kBoxBytes + 2 * kHMaxBytes + 512;
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+template <int NB, bool DBG>
+__global__ void __launch_bounds__(kThreads, 1)
+    markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, MarkovArgs a, int R) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    unsigned char *ring = smem;
+    unsigned char *hbuf = smem + size_t(kStages) * kBoxBytes;  // 2 buffers
+    uint64_t *full = reinterpret_cast<uint64_t *>(hbuf + 2 * kHMaxBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;    // [2]
+    uint64_t *h_full = acc_empty + 2;      // [2]
+    unsigned long long *s_best = reinterpret_cast<unsigned long long *>(h_full + 2);  // [kMaxReqs]
+    int *s_cur = reinterpret_cast<int *>(s_best + kMaxReqs);                          // [kMaxReqs]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_cur + kMaxReqs);
+    int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nctas = gridDim.x;
+    const int cta = blockIdx.x;
+    const int nkb = R / kKB;
+    const int T = (a.V + kTileRows - 1) / kTileRows;
+    const int t0 = static_cast<int>(static_cast<long long>(cta) * T / nctas);
+    const int t1 = static_cast<int>(static_cast<long long>(cta + 1) * T / nctas);
+    const int ntiles = t1 - t0;
+    auto tile_at = [t0, ntiles](int i, int t) { return t0 + ((i & 1) ? ntiles - 1 - t : t); };
+
+    // requests with an out-of-range prev give -1 ids and no candidates
+    unsigned bad_mask = 0;
+    for (int r = 0; r < a.B; ++r) {
+        const long long p = a.prev[r];
+        if (p < 0 || p >= a.V) bad_mask |= 1u << r;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiThreads / 32);
+            mbar_init(&h_full[b], kEpiThreads);
+        }
+        for (int r = 0; r < kMaxReqs; ++r) {
+            s_best[r] = 0ull;
+            const long long p = r < a.B ? a.prev[r] : 0;
+            s_cur[r] = (p >= 0 && p < a.V) ? static_cast<int>(p) : 0;
+        }
+        *s_abort = 0;
+        if (bad_mask && cta == 0) atomicOr(a.status, kStatusIndex);
+        fence_mbar_init();
+    }
+    {  // zero both H buffers (rows >= num_reqs stay zero for the whole kernel)
+        uint4 *h4 = reinterpret_cast<uint4 *>(hbuf);
+        for (int q = threadIdx.x; q < 2 * kHMaxBytes / 16; q += kThreads) h4[q] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint64_t pol;
+            asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+            int j = 0;
+            for (int i = 0; i < a.k; ++i)
+                for (int t = 0; t < ntiles; ++t) {
+                    const int tile = tile_at(i, t);
+                    for (int kb = 0; kb < nkb; ++kb, ++j) {
+                        const int st = j % kStages;
+                        if (!mbar_wait(&empty[st], ((j / kStages) & 1) ^ 1, a.timeout_ns)) {
+                            atomicOr(a.status, kStatusTimeout);
+                            goto producer_done;
+                        }
+                        mbar_arrive_expect_tx(&full[st], kBoxBytes);
+                        tma_load_2d(ring + size_t(st) * kBoxBytes, &tmW2, kb * kKB, tile * kTileRows, &full[st], pol);
+                    }
+                }
+        producer_done:;
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(true, kTileRows, kNPad);
+            int j = 0, tc = 0;
+            bool broken = false;
+            for (int i = 0; i < a.k && !broken; ++i) {
+                if (!mbar_wait(&h_full[i & 1], (i >> 1) & 1, a.timeout_ns)) {
+                    broken = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t hb = smem_addr(hbuf + (i & 1) * kHMaxBytes);
+                for (int t = 0; t < ntiles && !broken; ++t, ++tc) {
+                    const int ab = tc & 1;
+                    if (!mbar_wait(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.timeout_ns)) {
+                        broken = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < nkb; ++kb, ++j) {
+                        const int st = j % kStages;
+                        if (!mbar_wait(&full[st], (j / kStages) & 1, a.timeout_ns)) {
+                            broken = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_addr(ring + size_t(st) * kBoxBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kKB / 16; ++kk)
+                            tc_mma_f16(tmem + ab * kNPad, smem_desc_sw128(sa + kk * 32),
+                                       smem_desc_sw128(hb + kb * kHBlockBytes + kk * 32), idesc, (kb | kk) != 0);
+                        tc_commit(&empty[st]);
+                    }
+                    tc_commit(&acc_full[ab]);
+                }
+            }
+            if (broken) atomicOr(a.status, kStatusTimeout);
+        }
+    } else {
+        // ---------------- epilogue warps: thread = TMEM lane = row of the tile ----------------
+        const int et = threadIdx.x;
+        auto build_h = [&](int buf) {
+            unsigned char *H = hbuf + buf * kHMaxBytes;
+            const int cpr = R / 8;  // 16-byte chunks per row
+            for (int q = et; q < a.B * cpr; q += kEpiThreads) {
+                const int r = q / cpr;
+                const int c = q - r * cpr;
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                if (!((bad_mask >> r) & 1u))
+                    val = *reinterpret_cast<const uint4 *>(a.w1 + size_t(s_cur[r]) * R + c * 8);
+                const int kb = c >> 3, cc = c & 7;
+                *reinterpret_cast<uint4 *>(H + kb * kHBlockBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = val;
+            }
+            fence_proxy_async_smem();
+        };
+        build_h(0);
+        mbar_arrive(&h_full[0]);
+
+        bool aborted = false;  // CTA-uniform: no more computing or grid barriers, keep draining
+        bool broken = false;   // this thread's wait on an accumulator timed out
+        int tc = 0;
+        for (int i = 0; i < a.k; ++i) {
+            unsigned long long best[NB];
+#pragma unroll
+            for (int r = 0; r < NB; ++r) best[r] = 0ull;
+            for (int t = 0; t < ntiles; ++t, ++tc) {
+                const int ab = tc & 1;
+                const int row = tile_at(i, t) * kTileRows + et;
+                const bool valid = row < a.V && !aborted;
+                float bv[NB];
+#pragma unroll
+                for (int r = 0; r < NB; ++r) {
+                    bv[r] = 0.f;
+                    if (valid && r < a.B) bv[r] = __ldg(a.base + (size_t(r) * a.k + i) * a.V + row);
+                }
+                if (!broken && !mbar_wait(&acc_full[ab], (tc >> 1) & 1, a.timeout_ns)) {
+                    broken = true;
+                    atomicOr(a.status, kStatusTimeout);
+                    *reinterpret_cast<volatile int *>(s_abort) = 1;
+                }
+                tc_fence_after();
+                uint32_t v[16];
+                tmem_ld_16(tmem + ab * kNPad + (static_cast<uint32_t>(warp * 32) << 16), v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                if (valid && !broken) {
+#pragma unroll
+                    for (int r = 0; r < NB; ++r) {
+                        if (r < a.B && !((bad_mask >> r) & 1u)) {
+                            const float bias = __uint_as_float(v[r]);
+                            const float logit = bv[r] + bias;
+                            const unsigned long long key = argmax_key(logit, static_cast<uint32_t>(row));
+                            best[r] = key > best[r] ? key : best[r];
+                            if constexpr (DBG) {
+                                const size_t o = (size_t(r) * a.k + i) * a.V + row;
+                                if (a.dbg_logits) a.dbg_logits[o] = logit;
+                                if (a.dbg_bias) a.dbg_bias[o] = bias;
+                            }
+                        }
+                    }
+                }
+            }
+            if (!aborted) {
+                // ---- end of position: CTA max, global max, grid barrier, winner ----
+#pragma unroll
+                for (int r = 0; r < NB; ++r) {
+                    const unsigned long long k_w = shfl_max_u64(best[r]);
+                    if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
+                }
+                named_bar_sync(1, kEpiThreads);
+                if (et == 0) {
+                    for (int r = 0; r < a.B; ++r) {
+                        const unsigned long long k_cta = s_best[r];
+                        if (k_cta != 0ull) atomicMax(&a.best[size_t(i) * kMaxReqs + r], k_cta);
+                        s_best[r] = 0ull;
+                    }
+                    __threadfence();
+                    red_release_add_u32(a.bar_count, 1u);
+                    const unsigned target =
+                        static_cast<unsigned>(nctas) * static_cast<unsigned>(i + 1) + a.bar_extra;
+                    unsigned spins = 0;
+                    unsigned long long ts = 0;
+                    while (ld_acquire_u32(a.bar_count) < target) {
+                        if (++spins > 256) {
+                            if (ts == 0) ts = global_timer_ns();
+                            if (global_timer_ns() - ts > a.timeout_ns) {
+                                atomicOr(a.status, kStatusTimeout);
+                                *reinterpret_cast<volatile int *>(s_abort) = 1;
+                                break;
+                            }
+                            __nanosleep(32);
+                        }
+                    }
+                    __threadfence();
+                }
+                named_bar_sync(1, kEpiThreads);
+                if (*reinterpret_cast<volatile int *>(s_abort)) aborted = true;
+                if (!aborted && et < a.B && !((bad_mask >> et) & 1u)) {
+                    const unsigned long long key = ld_relaxed_u64(&a.best[size_t(i) * kMaxReqs + et]);
+                    s_cur[et] = key ? static_cast<int>(argmax_key_index(key)) : 0;
+                }
+                named_bar_sync(1, kEpiThreads);
+                if (!aborted && cta == 0 && et < a.B) {
+                    long long out = -1;
+                    if (!((bad_mask >> et) & 1u)) {
+                        const int id = s_cur[et];
+                        out = id;
+                        if (a.d2t) {
+                            const int tgt = a.d2t[id];
+                            if (tgt < 0) {
+                                out = -1;
+                                atomicOr(a.status, kStatusIndex);
+                            } else {
+                                out = tgt;
+                            }
+                        }
+                        if (i == a.k - 1) a.prev[et] = id;
+                    }
+                    a.out_ids[size_t(et) * a.k + i] = out;
+                }
+            }
+            if (i + 1 < a.k) {
+                if (!aborted) build_h((i + 1) & 1);
+                mbar_arrive(&h_full[(i + 1) & 1]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int NB, bool DBG>
+dspark_status launch_nb(const CUtensorMap &tm, const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
+    auto kern = markov_tc_kernel<NB, DBG>;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(markov_tc)");
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(markov_tc)");
+        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "markov_tc kernel cannot be resident on an SM");
+        configured_dev = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm, args, R);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(markov_tc)");
+    return DSPARK_OK;
+}
+
+template <bool DBG>
+dspark_status launch_dbg(const CUtensorMap &tm, const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
+    if (args.B <= 1) return launch_nb<1, DBG>(tm, args, R, nctas, stream);
+    if (args.B <= 2) return launch_nb<2, DBG>(tm, args, R, nctas, stream);
+    if (args.B <= 4) return launch_nb<4, DBG>(tm, args, R, nctas, stream);
+    return launch_nb<8, DBG>(tm, args, R, nctas, stream);
+}
+
+}  // namespace
+
+dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
+    if (R % kKB != 0 || R > 256) return fail(DSPARK_ERR_UNSUPPORTED, "markov_tc: rank %d", R);
+    CUtensorMap tm;
+    dspark_status st = make_tmap_2d(&tm, args.w2, true, static_cast<uint64_t>(args.V), static_cast<uint64_t>(R),
+                                    kTileRows, kKB);
+    if (st != DSPARK_OK) return st;
+    if (args.dbg_logits || args.dbg_bias) return launch_dbg<true>(tm, args, R, nctas, stream);
+    return launch_dbg<false>(tm, args, R, nctas, stream);
+}
+
+}  // namespace dspark
