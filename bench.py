@@ -116,7 +116,7 @@ def read_peak():
 
 def markov_source_hash():
     h = hashlib.sha256()
-    for f in ("markov.cu", "common.cuh"):
+    for f in ("markov_tc.cu", "markov.cu", "markov.cuh", "tc.cuh", "common.cuh"):
         with open(os.path.join(REPO, "dspark_draft_sampling_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -137,7 +137,7 @@ def recorded_traffic(B):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -155,7 +155,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -366,7 +366,7 @@ def cpu_baseline(B):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--num-reqs", type=int, default=1)
@@ -444,7 +444,7 @@ def main():
         "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64; shapes and distributions of the pages' lanes)",
         "config": config_dict(B),
-        "roofline": {"kernel": "markov_draft_kernel (k=15 positions, one launch)",
+        "roofline": {"kernel": "markov_tc_kernel (k=15 positions, one launch)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": mb,

@@ -257,13 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
                 }
                 named_bar_sync(1, kEpiThreads);
+                if (et < a.B && s_best[et] != 0ull && i + 1 < a.k) {
+                    // this CTA's candidate may be the winner: pull its markov_w1 row into L2 so
+                    // the gather after the barrier is an L2 hit
+                    const uint32_t cand = argmax_key_index(s_best[et]);
+                    const uint16_t *row = a.w1 + size_t(cand) * R;
+                    for (int off = 0; off < R * 2; off += 128)
+                        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<const char *>(row) + off));
+                }
                 if (et == 0) {
                     for (int r = 0; r < a.B; ++r) {
                         const unsigned long long k_cta = s_best[r];
                         if (k_cta != 0ull) atomicMax(&a.best[size_t(i) * kMaxReqs + r], k_cta);
                         s_best[r] = 0ull;
                     }
-                    __threadfence();
+                    // the release orders this thread's atomicMax updates before the arrival
                     red_release_add_u32(a.bar_count, 1u);
                     const unsigned target =
                         static_cast<unsigned>(nctas) * static_cast<unsigned>(i + 1) + a.bar_extra;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __nanosleep(32);
                         }
                     }
-                    __threadfence();
+                    // the acquire load above orders the winners' reads after every arrival
                 }
                 named_bar_sync(1, kEpiThreads);
                 if (*reinterpret_cast<volatile int *>(s_abort)) aborted = true;

@@ -153,15 +153,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*s_last) {
                 __threadfence();
                 if (ok && row < a.N) {
-                    const float *base = a.partial + (size_t(rb) * a.S * kRowsPerUnit + lrow) * kNPad;
-                    for (int m = 0; m < M; ++m) {
-                        float y = 0.f;
-                        for (int s = 0; s < a.S; ++s) y += __ldcg(base + size_t(s) * kRowsPerUnit * kNPad + m);
-                        const size_t o = size_t(m) * a.N + row;
-                        if (a.y_fp32)
-                            static_cast<float *>(a.Y)[o] = y;
-                        else
-                            static_cast<__half *>(a.Y)[o] = __float2half_rn(y);
+                    // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads are issued
+                    // four units at a time so their latencies overlap, the sum order is fixed
+                    const float4 *base =
+                        reinterpret_cast<const float4 *>(a.partial + (size_t(rb) * a.S * kRowsPerUnit + lrow) * kNPad);
+                    constexpr size_t kUnitF4 = size_t(kRowsPerUnit) * kNPad / 4;
+                    float y[kNPad];
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
+                    int s = 0;
+                    for (; s + 4 <= a.S; s += 4) {
+                        float4 t[4][4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) t[u][q] = __ldcg(base + size_t(s + u) * kUnitF4 + q);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                y[4 * q] += t[u][q].x;
+                                y[4 * q + 1] += t[u][q].y;
+                                y[4 * q + 2] += t[u][q].z;
+                                y[4 * q + 3] += t[u][q].w;
+                            }
+                    }
+                    for (; s < a.S; ++s) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 t = __ldcg(base + size_t(s) * kUnitF4 + q);
+                            y[4 * q] += t.x;
+                            y[4 * q + 1] += t.y;
+                            y[4 * q + 2] += t.z;
+                            y[4 * q + 3] += t.w;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) {
+                        if (m < M) {
+                            const size_t o = size_t(m) * a.N + row;
+                            if (a.y_fp32)
+                                static_cast<float *>(a.Y)[o] = y[m];
+                            else
+                                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+                        }
                     }
                 }
                 if (threadIdx.x == 0) a.tickets[rb] = 0u;  // ready for the next call
