@@ -129,18 +129,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint64_t pol;
             asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-            int j = 0;
+            int st = 0;
+            uint32_t ph = 0;
             for (int i = 0; i < a.k; ++i)
                 for (int t = 0; t < ntiles; ++t) {
-                    const int tile = tile_at(i, t);
-                    for (int kb = 0; kb < nkb; ++kb, ++j) {
-                        const int st = j % kStages;
-                        if (!mbar_wait(&empty[st], ((j / kStages) & 1) ^ 1, a.timeout_ns)) {
+                    const int y = tile_at(i, t) * kTileRows;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) {
                             atomicOr(a.status, kStatusTimeout);
                             goto producer_done;
                         }
                         mbar_arrive_expect_tx(&full[st], kBoxBytes);
-                        tma_load_2d(ring + size_t(st) * kBoxBytes, &tmW2, kb * kKB, tile * kTileRows, &full[st], pol);
+                        tma_load_2d(ring + size_t(st) * kBoxBytes, &tmW2, kb * kKB, y, &full[st], pol);
+                        if (++st == kStages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
         producer_done:;
@@ -149,7 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(true, kTileRows, kNPad);
-            int j = 0, tc = 0;
+            // Descriptors are built once and advanced by adding byte offsets >> 4 to their
+            // address field (all of shared memory is below 256 KB, so it never carries).
+            const uint64_t dA0 = smem_desc_sw128(smem_addr(ring));
+            const uint64_t dH0 = smem_desc_sw128(smem_addr(hbuf));
+            int st = 0, ab = 0;
+            uint32_t ph = 0, aph = 0;
             bool broken = false;
             for (int i = 0; i < a.k && !broken; ++i) {
                 if (!mbar_wait(&h_full[i & 1], (i >> 1) & 1, a.timeout_ns)) {
@@ -157,29 +166,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t hb = smem_addr(hbuf + (i & 1) * kHMaxBytes);
-                for (int t = 0; t < ntiles && !broken; ++t, ++tc) {
-                    const int ab = tc & 1;
-                    if (!mbar_wait(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, a.timeout_ns)) {
+                const uint64_t dH = dH0 + static_cast<uint64_t>((i & 1) * (kHMaxBytes >> 4));
+                for (int t = 0; t < ntiles && !broken; ++t) {
+                    if (!mbar_wait(&acc_empty[ab], aph ^ 1u, a.timeout_ns)) {
                         broken = true;
                         break;
                     }
                     tc_fence_after();
-                    for (int kb = 0; kb < nkb; ++kb, ++j) {
-                        const int st = j % kStages;
-                        if (!mbar_wait(&full[st], (j / kStages) & 1, a.timeout_ns)) {
+                    const uint32_t d = tmem + ab * kNPad;
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait(&full[st], ph, a.timeout_ns)) {
                             broken = true;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = smem_addr(ring + size_t(st) * kBoxBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kKB / 16; ++kk)
-                            tc_mma_f16(tmem + ab * kNPad, smem_desc_sw128(sa + kk * 32),
-                                       smem_desc_sw128(hb + kb * kHBlockBytes + kk * 32), idesc, (kb | kk) != 0);
+                        const uint64_t dA = dA0 + static_cast<uint64_t>(st * (kBoxBytes >> 4));
+                        const uint64_t dB = dH + static_cast<uint64_t>(kb * (kHBlockBytes >> 4));
+                        tc_mma_f16(d, dA, dB, idesc, kb != 0);  // K = 16 per MMA, 32 B apart
+                        tc_mma_f16(d, dA + 2, dB + 2, idesc, 1u);
+                        tc_mma_f16(d, dA + 4, dB + 4, idesc, 1u);
+                        tc_mma_f16(d, dA + 6, dB + 6, idesc, 1u);
                         tc_commit(&empty[st]);
+                        if (++st == kStages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                     tc_commit(&acc_full[ab]);
+                    if (++ab == 2) {
+                        ab = 0;
+                        aph ^= 1u;
+                    }
                 }
             }
             if (broken) atomicOr(a.status, kStatusTimeout);

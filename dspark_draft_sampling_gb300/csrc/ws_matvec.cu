@@ -30,7 +30,13 @@ namespace dspark {
 namespace {
 
 constexpr int kThreads = 192;      // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
-constexpr int kStages = 5;
+#ifndef DSPARK_WS_STAGES
+#define DSPARK_WS_STAGES 5
+#endif
+#ifndef DSPARK_WS_UNITS_PER_SM
+#define DSPARK_WS_UNITS_PER_SM 2
+#endif
+constexpr int kStages = DSPARK_WS_STAGES;
 constexpr int kRowsPerUnit = 128;  // MMA M
 constexpr int kNPad = 16;          // MMA N: X rows padded to 16
 constexpr int kKB = 64;            // k per block (128 bytes of fp16 = the swizzle span)
@@ -91,29 +97,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
+            int st = 0;
+            uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                const int st = j % kStages;
-                if (!mbar_wait(&empty[st], ((j / kStages) & 1) ^ 1, a.timeout_ns)) break;
+                if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) break;
                 unsigned char *sa = smem + size_t(st) * kStageBytes;
                 mbar_arrive_expect_tx(&full[st], kStageBytes);
                 tma_load_2d(sa, &tmW, (kb0 + j) * kKB, n0, &full[st], pol_w);
                 tma_load_2d(sa + kABytes, &tmX, (kb0 + j) * kKB, 0, &full[st], pol_x);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
         }
     } else if (warp == 5) {
         // ---- MMA issuer ----
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(false, kRowsPerUnit, kNPad);
+            // descriptors built once, advanced by byte offsets >> 4 (shared memory < 256 KB)
+            const uint64_t dA0 = smem_desc_sw128(smem_addr(smem));
+            int st = 0;
+            uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                const int st = j % kStages;
-                if (!mbar_wait(&full[st], (j / kStages) & 1, a.timeout_ns)) break;
+                if (!mbar_wait(&full[st], ph, a.timeout_ns)) break;
                 tc_fence_after();
-                const uint32_t sa = smem_addr(smem + size_t(st) * kStageBytes);
-#pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
-                    tc_mma_f16(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sa + kABytes + kk * 32), idesc,
-                               (j | kk) != 0);
+                const uint64_t dA = dA0 + static_cast<uint64_t>(st * (kStageBytes >> 4));
+                const uint64_t dB = dA + static_cast<uint64_t>(kABytes >> 4);
+                tc_mma_f16(tmem, dA, dB, idesc, j != 0);  // K = 16 per MMA, 32 B apart
+                tc_mma_f16(tmem, dA + 2, dB + 2, idesc, 1u);
+                tc_mma_f16(tmem, dA + 4, dB + 4, idesc, 1u);
+                tc_mma_f16(tmem, dA + 6, dB + 6, idesc, 1u);
                 tc_commit(&empty[st]);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
             tc_commit(done);
         }
@@ -218,7 +237,7 @@ Plan plan_for(int N, int K, int sms) {
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
     p.nkb = (K + kKB - 1) / kKB;
     // about two units per SM, each with at least 4 k-blocks to amortize the pipeline fill
-    int S = (2 * sms) / p.nrb;
+    int S = (DSPARK_WS_UNITS_PER_SM * sms) / p.nrb;
     const int smax = p.nkb / 4 > 0 ? p.nkb / 4 : 1;
     if (S > smax) S = smax;
     if (S < 1) S = 1;
