@@ -236,10 +236,11 @@ def ws_matvec_workspace_bytes(M: int, N: int, K: int) -> int:
 
 
 def new_ws_workspace(M: int, N: int, K: int, device=None):
+    """Zero-filled scratch for ws_matvec (the kernel leaves it zero-filled after each call)."""
     n = ws_matvec_workspace_bytes(M, N, K)
     if n == 0:
         raise DsparkError(DSPARK_ERR_CUDA, "could not size the ws_matvec workspace")
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def ws_matvec(W, X, *, out=None, out_fp32: bool = False, workspace=None, stream=None):

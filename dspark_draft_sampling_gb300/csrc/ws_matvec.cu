@@ -8,11 +8,11 @@
 // tensor cores, which leaves the SMs free to keep the stream going.
 //
 // GB300 design
-//  * Work unit = (128 weight rows, a contiguous range of 64-wide k-blocks).  Units split
-//    K so that about two units run per SM (two CTAs per SM fit in shared memory and TMEM).
+//  * Work unit = (128 weight rows, a contiguous range of 64-wide k-blocks).  K is split so
+//    that there is about one unit per SM.
 //  * Warp 4 (one thread) streams, per k-block, the W tile [128 rows x 64 k] (16 KB) and
 //    the X tile [16 rows x 64 k] (2 KB; rows >= M read as zero) with 2-D TMA tensor copies
-//    in the 128-byte-swizzled layout, through a 5-stage mbarrier ring.
+//    in the 128-byte-swizzled layout, through a 10-stage mbarrier ring (180 KB).
 //  * Warp 5 allocates 32 TMEM columns and one thread issues, per k-block, four
 //    tcgen05.mma kind::f16 (M=128, N=16, K=16; fp16 in, fp32 accumulate) into TMEM.
 //    tcgen05.commit frees each stage once its MMAs are done, and signals the epilogue
@@ -30,13 +30,10 @@ namespace dspark {
 namespace {
 
 constexpr int kThreads = 192;      // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
-#ifndef DSPARK_WS_STAGES
-#define DSPARK_WS_STAGES 5
-#endif
-#ifndef DSPARK_WS_UNITS_PER_SM
-#define DSPARK_WS_UNITS_PER_SM 2
-#endif
-constexpr int kStages = DSPARK_WS_STAGES;
+// 10 x 18 KB stages, one CTA per SM and about one unit per SM: measured best on GB300 among
+// {5, 8, 10, 12} stages x {1, 2, 4} units per SM for the four Qwen3-8B projection shapes.
+constexpr int kStages = 10;
+constexpr int kUnitsPerSm = 1;
 constexpr int kRowsPerUnit = 128;  // MMA M
 constexpr int kNPad = 16;          // MMA N: X rows padded to 16
 constexpr int kKB = 64;            // k per block (128 bytes of fp16 = the swizzle span)
@@ -218,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (threadIdx.x == 0) a.tickets[rb] = 0u;  // ready for the next call
+                if (threadIdx.x == 0) a.tickets[rb] = 0u;  // zero again for the next call
             }
         }
     }
@@ -236,8 +233,8 @@ Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
     p.nkb = (K + kKB - 1) / kKB;
-    // about two units per SM, each with at least 4 k-blocks to amortize the pipeline fill
-    int S = (DSPARK_WS_UNITS_PER_SM * sms) / p.nrb;
+    // about kUnitsPerSm units per SM, each with at least 4 k-blocks to amortize the pipeline fill
+    int S = (kUnitsPerSm * sms) / p.nrb;
     const int smax = p.nkb / 4 > 0 ? p.nkb / 4 : 1;
     if (S > smax) S = smax;
     if (S < 1) S = 1;
@@ -245,11 +242,13 @@ Plan plan_for(int N, int K, int sms) {
     return p;
 }
 
+// Workspace: a fixed ticket area first (so tickets stay at the same place and stay zero
+// whatever shapes share the workspace), then the partial tiles.
+constexpr size_t kTicketBytes = 65536;  // up to 16384 row blocks (N <= 2,097,152)
+
 size_t workspace_bytes_for(const Plan &p) {
-    if (p.S == 1) return 256;
-    const size_t partial = size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
-    const size_t tickets = (size_t(p.nrb) * sizeof(unsigned) + 255) / 256 * 256;
-    return partial + tickets;
+    if (p.S == 1) return kTicketBytes;
+    return kTicketBytes + size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
 }
 
 }  // namespace
@@ -258,7 +257,7 @@ size_t workspace_bytes_for(const Plan &p) {
 extern "C" size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K) {
     (void)M;
     int sms = 0;
-    if (N <= 0 || K <= 0) return 256;
+    if (N <= 0 || K <= 0) return dspark::kTicketBytes;
     if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
     return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
 }
@@ -279,6 +278,8 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
     const Plan p = plan_for(N, K, sms);
+    if (size_t(p.nrb) * sizeof(unsigned) > kTicketBytes)
+        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: N=%d exceeds %zu rows", N, kTicketBytes / 4 * kRowsPerUnit);
     const size_t need = workspace_bytes_for(p);
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec: workspace of %zu bytes < required %zu", workspace_bytes, need);
@@ -303,10 +304,8 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     args.tickets = nullptr;
     if (p.S > 1) {
         unsigned char *ws = static_cast<unsigned char *>(workspace);
-        args.partial = reinterpret_cast<float *>(ws);
-        args.tickets = reinterpret_cast<unsigned *>(ws + size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float));
-        cudaError_t e = cudaMemsetAsync(args.tickets, 0, size_t(p.nrb) * sizeof(unsigned), s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ws_matvec tickets)");
+        args.tickets = reinterpret_cast<unsigned *>(ws);
+        args.partial = reinterpret_cast<float *>(ws + kTicketBytes);
     }
 
     static int configured_dev = -1;

@@ -184,16 +184,18 @@ dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float b
  *
  *   Y[m, n] = sum_k X[m, k] * W[n, k]      (fp16 inputs, fp32 accumulation)
  *
- * Runs on the tcgen05 tensor cores (128 weight rows x 16 padded activation rows per MMA);
- * K may be split over several CTAs, whose fp32 partial sums are added in a fixed order.
+ * Runs on the tcgen05 tensor cores (128 weight rows x 16 padded activation rows per MMA).
+ * K may be split over several CTAs (about one per SM in total); their fp32 partial sums
+ * are added by the last of them in a fixed order.
  *
  * Arguments
  *   W          fp16 [N, K] (out x in), 16-byte aligned
  *   X          fp16 [M, K], 16-byte aligned
  *   Y          [M, N]: fp32 if y_is_fp32, else fp16 rounded to nearest even
  *   workspace  device scratch of at least dspark_ws_matvec_workspace_bytes(M, N, K)
- *              bytes (depends on N, K and the current device), 256-byte aligned;
- *              calls sharing a workspace must not overlap on the device
+ *              bytes (depends on N, K and the current device), 256-byte aligned, and
+ *              ZERO-FILLED before its first use; every call leaves it zero-filled again.
+ *              Calls sharing a workspace must not overlap on the device.
  *   Supported: 1 <= M <= 16, N >= 1, K >= 8 with K % 8 == 0 (M == 0 or N == 0
  *   enqueues nothing).  The result of row m does not depend on M: every output is
  *   summed in one fixed order.

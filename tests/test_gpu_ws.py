@@ -71,3 +71,19 @@ def test_repeat_bit_identical():
     a = api.ws_matvec(W, X, out_fp32=True)
     b = api.ws_matvec(W, X, out_fp32=True)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_workspace_shared_across_shapes():
+    """One zero-filled workspace serves calls of different shapes in any order: the split-K
+    tickets live in a fixed area that every call leaves zero."""
+    shapes = [(7, 1024, 4096), (7, 4096, 4096), (3, 12288, 4096), (7, 4096, 12288)]
+    size = max(api.ws_matvec_workspace_bytes(*s) for s in shapes)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for (M, N, K) in shapes:
+            inp = synth.ws_inputs(M, N, K, seed=N + K)
+            W, X = _dev(inp)
+            y = api.ws_matvec(W, X, out_fp32=True, workspace=ws)
+            ref = api.ws_matvec(W, X, out_fp32=True)  # its own fresh workspace
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), (M, N, K)
