@@ -5,9 +5,12 @@ Every step of the path runs in the CUDA kernels of ``libdspark.so``; this packag
 only marshals torch tensors into the C ABI declared in ``include/dspark.h``.
 """
 from .api import (  # noqa: F401
+    DraftPlan,
     DsparkError,
+    GatedDraftPlan,
     MarkovPlan,
     conf_probe,
+    conf_probe_split,
     lib_path,
     load_library,
     markov_draft,

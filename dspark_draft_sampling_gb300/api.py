@@ -33,7 +33,17 @@ SIGNATURES = {
                                        ctypes.POINTER(_P)]),
     "dspark_markov_plan_launch": (_I, [_P, _P]),
     "dspark_markov_plan_destroy": (None, [_P]),
+    "dspark_draft_plan_create": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P,
+                                      _Z, ctypes.POINTER(_P)]),
+    "dspark_draft_plan_launch": (_I, [_P, _P]),
+    "dspark_draft_plan_destroy": (None, [_P]),
+    "dspark_gated_draft_plan_create": (_I, [_P, _P, _I, _F, _F, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                            _I, _I, _P, _P, _Z, ctypes.POINTER(_P)]),
+    "dspark_gated_draft_plan_launch": (_I, [_P, _P]),
+    "dspark_gated_draft_plan_destroy": (None, [_P]),
     "dspark_conf_probe": (_I, [_P, _P, _F, _F, _I, _I, _P, _P, _P]),
+    "dspark_conf_probe_split": (_I, [_P, _P, _I, ctypes.c_longlong, _P, _I, ctypes.c_longlong, _F, _F,
+                                     _I, _P, _P, _P]),
     "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
 }
@@ -207,6 +217,100 @@ class MarkovPlan:
             pass
 
 
+class DraftPlan:
+    """lm_head matvec (base logits written on the device) + Markov draft in one CUDA graph.
+
+    lm_head fp16 [vocab, H]; hidden fp16 [num_reqs * k, H]; markov_w1/w2 bf16 [vocab, R];
+    d2t int32 [vocab] or None; prev int64 [num_reqs] (updated on the device)."""
+
+    def __init__(self, lm_head, hidden, w1, w2, d2t, prev, k: int):
+        self._lib = lib = load_library()
+        V, H = lm_head.shape
+        B = prev.numel()
+        R = w2.shape[1]
+        if hidden.shape != (B * k, H):
+            raise ValueError("hidden must be [num_reqs * k, hidden_dim]")
+        dev = lm_head.device
+        self.base = torch.empty((B, k, V), dtype=torch.float32, device=dev)
+        self.out_ids = torch.empty((B, k), dtype=torch.int64, device=dev)
+        self.markov_ws = new_markov_workspace(B, k, V, R, dev)
+        self.ws_ws = new_ws_workspace(B * k, V, H, dev)
+        self.tensors = (lm_head, hidden, w1, w2, d2t, prev)
+        handle = ctypes.c_void_p()
+        st = lib.dspark_draft_plan_create(
+            _ptr(lm_head, "lm_head", itemsize=2, dtypes=_BITS16), _ptr(hidden, "hidden", itemsize=2,
+                                                                        dtypes=_BITS16), H,
+            _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16),
+            _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
+            _ptr(d2t, "d2t", dtypes=(torch.int32,), allow_none=True),
+            _ptr(prev, "prev", dtypes=(torch.int64,)), B, k, V, R,
+            _ptr(self.base, "base"), _ptr(self.out_ids, "out_ids"),
+            _ptr(self.markov_ws, "markov_ws"), self.markov_ws.numel(),
+            _ptr(self.ws_ws, "ws_ws"), self.ws_ws.numel(), ctypes.byref(handle))
+        _check(lib, st)
+        self._handle = handle
+
+    def launch(self, stream=None):
+        _check(self._lib, self._lib.dspark_draft_plan_launch(self._handle, _stream(stream)))
+        return self.out_ids
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            self._lib.dspark_draft_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class GatedDraftPlan:
+    """Probe -> (if sigmoid(z) >= threshold) Markov draft, decided on the device, one graph."""
+
+    def __init__(self, wq, probe_input, bias: float, threshold: float, base, w1, w2, d2t, prev):
+        self._lib = lib = load_library()
+        B, k, V = base.shape
+        R = w2.shape[1]
+        K = probe_input.numel()
+        dev = base.device
+        self.logit = torch.empty(1, dtype=torch.float32, device=dev)
+        self.gate = torch.empty(1, dtype=torch.int32, device=dev)
+        self.out_ids = torch.empty((B, k), dtype=torch.int64, device=dev)
+        self.workspace = new_markov_workspace(B, k, V, R, dev)
+        self.tensors = (wq, probe_input, base, w1, w2, d2t, prev)
+        handle = ctypes.c_void_p()
+        st = lib.dspark_gated_draft_plan_create(
+            _ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)),
+            _ptr(probe_input, "probe_input", dtypes=(torch.float32,)), K, float(bias), float(threshold),
+            _ptr(self.logit, "logit"), _ptr(self.gate, "gate"),
+            _ptr(base, "base", dtypes=(torch.float32,)),
+            _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16),
+            _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
+            _ptr(d2t, "d2t", dtypes=(torch.int32,), allow_none=True),
+            _ptr(prev, "prev", dtypes=(torch.int64,)), B, k, V, R,
+            _ptr(self.out_ids, "out_ids"), _ptr(self.workspace, "workspace"), self.workspace.numel(),
+            ctypes.byref(handle))
+        _check(lib, st)
+        self._handle = handle
+
+    def launch(self, stream=None):
+        _check(self._lib, self._lib.dspark_gated_draft_plan_launch(self._handle, _stream(stream)))
+        return self.out_ids
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            self._lib.dspark_gated_draft_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gate_out=None,
                stream=None):
     """Q8_0 confidence probes.  wq uint8 [K/32*34], hidden fp32 [n, K] (or [K]).
@@ -227,6 +331,35 @@ def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gat
                                _ptr(logit_out, "logit_out", dtypes=(torch.float32,)),
                                _ptr(gate_out, "gate_out", dtypes=(torch.int32,)),
                                _stream(stream))
+    _check(lib, st)
+    return logit_out, gate_out
+
+
+def conf_probe_split(wq, hidden, state, bias: float, threshold: float, *, logit_out=None,
+                     gate_out=None, stream=None):
+    """Probes over [hidden; state] given as two row-major tensors [n, K_hidden], [n, K_state]
+    (any row strides that keep rows 16-byte aligned).  Returns (logit [n], gate [n])."""
+    lib = load_library()
+    n, Kh = hidden.shape
+    n2, Ks = state.shape
+    if n != n2:
+        raise ValueError("hidden and state disagree on the number of probes")
+    if wq.numel() != ((Kh + Ks) // 32) * 34:
+        raise ValueError("wq must hold (K_hidden + K_state) / 32 Q8_0 blocks of 34 bytes")
+    for t, name in ((hidden, "hidden"), (state, "state")):
+        if not t.is_cuda or t.dtype != torch.float32 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be a CUDA float32 tensor with unit column stride")
+    if gate_out is None:
+        gate_out = torch.empty(n, dtype=torch.int32, device=hidden.device)
+    if logit_out is None:
+        logit_out = torch.empty(n, dtype=torch.float32, device=hidden.device)
+    st = lib.dspark_conf_probe_split(_ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)),
+                                     ctypes.c_void_p(hidden.data_ptr()), Kh, hidden.stride(0),
+                                     ctypes.c_void_p(state.data_ptr()), Ks, state.stride(0),
+                                     float(bias), float(threshold), n,
+                                     _ptr(logit_out, "logit_out", dtypes=(torch.float32,)),
+                                     _ptr(gate_out, "gate_out", dtypes=(torch.int32,)),
+                                     _stream(stream))
     _check(lib, st)
     return logit_out, gate_out
 

@@ -15,6 +15,12 @@ void clear_error();
 // SM count of the current device (cached per device).
 int current_sm_count(int *sm_count);
 
+// Checked probe enqueue behind dspark_conf_probe / dspark_conf_probe_split (probe.cu).  With
+// set_cond != 0 the kernel also sets the graph conditional `cond` to probe 0's gate.
+dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long long lda, const float *xb, int Kb,
+                            long long ldb, float bias, float threshold, int n_probes, float *logit_out,
+                            int32_t *gate_out, cudaStream_t stream, cudaGraphConditionalHandle cond, int set_cond);
+
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Device status word bits (stored in the workspace header).

@@ -11,7 +11,6 @@
 #include "markov.cuh"
 
 namespace dspark {
-namespace {
 
 size_t workspace_bytes(int k) {
     const size_t keys = size_t(k > 0 ? k : 0) * kMaxReqs * sizeof(unsigned long long);
@@ -65,7 +64,6 @@ dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16
     return launch_markov_tc(args, R, sms, stream);
 }
 
-}  // namespace
 }  // namespace dspark
 
 struct dspark_markov_plan {

@@ -27,17 +27,22 @@ __device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
     return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
 }
 
-__global__ void __launch_bounds__(kProbeThreads) conf_probe_kernel(const uint8_t *__restrict__ wq,
-                                                                   const float *__restrict__ hidden, float bias,
-                                                                   float t_logit, int K, float *logit_out,
-                                                                   int32_t *gate_out) {
+// The probe's input vector may come in two pieces (the hidden state and the Markov
+// state): chunk c < nchunks_a reads piece a, the rest read piece b.  With one piece
+// (nchunks_b == 0) this is the plain contiguous probe; the chunk order, and so every
+// rounding, is the same either way.
+__global__ void __launch_bounds__(kProbeThreads)
+    conf_probe_kernel(const uint8_t *__restrict__ wq, const float *__restrict__ xa, long long lda, int nchunks_a,
+                      const float *__restrict__ xb, long long ldb, int nchunks_b, float bias, float t_logit,
+                      float *logit_out, int32_t *gate_out, cudaGraphConditionalHandle cond, int set_cond) {
     __shared__ float warp_sum[kProbeWarps];
-    const float *x = hidden + size_t(blockIdx.x) * K;
-    const int nchunks = K >> 2;  // 4 floats per chunk; a Q8_0 block spans 8 chunks
+    const float *pa = xa + size_t(blockIdx.x) * lda;
+    const float *pb = xb ? xb + size_t(blockIdx.x) * ldb : nullptr;
+    const int nchunks = nchunks_a + nchunks_b;  // 4 floats per chunk; a Q8_0 block spans 8 chunks
     float acc = 0.f;
 #pragma unroll 4
     for (int c = threadIdx.x; c < nchunks; c += kProbeThreads) {
-        const float4 xv = ldg_stream_f4(x + 4 * c);
+        const float4 xv = ldg_stream_f4(c < nchunks_a ? pa + 4 * c : pb + 4 * (c - nchunks_a));
         const uint8_t *blk = wq + size_t(c >> 3) * 34;
         const int off = 2 + 4 * (c & 7);
         const unsigned short dbits = static_cast<unsigned short>(__ldg(blk) | (__ldg(blk + 1) << 8));
@@ -61,34 +66,64 @@ __global__ void __launch_bounds__(kProbeThreads) conf_probe_kernel(const uint8_t
 #pragma unroll
         for (int w = 1; w < kProbeWarps; ++w) z += warp_sum[w];
         z += bias;
+        const int gate = (z >= t_logit) ? 1 : 0;
         if (logit_out) logit_out[blockIdx.x] = z;
-        gate_out[blockIdx.x] = (z >= t_logit) ? 1 : 0;
+        gate_out[blockIdx.x] = gate;
+        // inside a gated draft graph: probe 0's decision selects whether the draft runs
+        if (set_cond && blockIdx.x == 0) cudaGraphSetConditional(cond, static_cast<unsigned>(gate));
     }
 }
 
 }  // namespace
-}  // namespace dspark
 
-extern "C" dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float bias, float threshold,
-                                           int K, int n_probes, float *logit_out, int32_t *gate_out,
-                                           dspark_stream_t stream) {
-    using namespace dspark;
+dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long long lda, const float *xb, int Kb,
+                            long long ldb, float bias, float threshold, int n_probes, float *logit_out,
+                            int32_t *gate_out, cudaStream_t stream, cudaGraphConditionalHandle cond,
+                            int set_cond) {
     clear_error();
-    if (K <= 0 || (K % 32) != 0) return fail(DSPARK_ERR_INVALID, "conf_probe: K=%d must be a positive multiple of 32", K);
+    const int K = Ka + Kb;
+    if (Ka <= 0 || Kb < 0 || (K % 32) != 0 || (Ka % 4) != 0 || (Kb % 4) != 0)
+        return fail(DSPARK_ERR_INVALID, "conf_probe: widths %d + %d must be multiples of 4 summing to a multiple of 32",
+                    Ka, Kb);
     if (n_probes < 0) return fail(DSPARK_ERR_INVALID, "conf_probe: n_probes=%d < 0", n_probes);
     if (!(threshold > 0.f && threshold < 1.f))
         return fail(DSPARK_ERR_INVALID, "conf_probe: threshold must lie in (0, 1)");
     if (n_probes == 0) return DSPARK_OK;  // nothing to enqueue
-    if (!w_q8_0 || !hidden || !gate_out) return fail(DSPARK_ERR_INVALID, "conf_probe: null pointer argument");
-    if (!aligned(hidden, 16)) return fail(DSPARK_ERR_INVALID, "conf_probe: hidden must be 16-byte aligned");
+    if (!w_q8_0 || !xa || (Kb > 0 && !xb) || !gate_out)
+        return fail(DSPARK_ERR_INVALID, "conf_probe: null pointer argument");
+    if (!aligned(xa, 16) || (Kb > 0 && !aligned(xb, 16)) || (lda % 4) != 0 || (Kb > 0 && (ldb % 4) != 0) ||
+        lda < Ka || (Kb > 0 && ldb < Kb))
+        return fail(DSPARK_ERR_INVALID, "conf_probe: inputs must be 16-byte aligned with row strides >= widths");
     if (!aligned(gate_out, 4) || (logit_out && !aligned(logit_out, 4)))
         return fail(DSPARK_ERR_INVALID, "conf_probe: misaligned output pointer");
     // logit(t) on the host in double: sigmoid(z) >= t  <=>  z >= log(t / (1 - t)).
     const double t = static_cast<double>(threshold);
     const float t_logit = static_cast<float>(std::log(t / (1.0 - t)));
-    conf_probe_kernel<<<n_probes, kProbeThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t *>(w_q8_0), hidden, bias, t_logit, K, logit_out, gate_out);
+    conf_probe_kernel<<<n_probes, kProbeThreads, 0, stream>>>(static_cast<const uint8_t *>(w_q8_0), xa, lda, Ka / 4,
+                                                              Kb > 0 ? xb : nullptr, ldb, Kb / 4, bias, t_logit,
+                                                              logit_out, gate_out, cond, set_cond);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "conf_probe launch");
     return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+extern "C" dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float bias, float threshold,
+                                           int K, int n_probes, float *logit_out, int32_t *gate_out,
+                                           dspark_stream_t stream) {
+    if (K <= 0 || (K % 32) != 0) {
+        dspark::clear_error();
+        return dspark::fail(DSPARK_ERR_INVALID, "conf_probe: K=%d must be a positive multiple of 32", K);
+    }
+    return dspark::probe_enqueue(w_q8_0, hidden, K, K, nullptr, 0, 0, bias, threshold, n_probes, logit_out, gate_out,
+                                 reinterpret_cast<cudaStream_t>(stream), 0ull, 0);
+}
+
+extern "C" dspark_status dspark_conf_probe_split(const void *w_q8_0, const float *hidden, int K_hidden,
+                                                 long long ld_hidden, const float *state, int K_state,
+                                                 long long ld_state, float bias, float threshold, int n_probes,
+                                                 float *logit_out, int32_t *gate_out, dspark_stream_t stream) {
+    return dspark::probe_enqueue(w_q8_0, hidden, K_hidden, ld_hidden, state, K_state, ld_state, bias, threshold,
+                                 n_probes, logit_out, gate_out, reinterpret_cast<cudaStream_t>(stream), 0ull, 0);
 }

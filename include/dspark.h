@@ -174,6 +174,19 @@ dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float b
                                 float threshold, int K, int n_probes, float *logit_out,
                                 int32_t *gate_out, dspark_stream_t stream);
 
+/* The same probe over an input that arrives in two pieces, e.g. the hidden state and the
+ * Markov state kept in separate buffers (ds4 PR #772, "Summary": the probe reads the hidden
+ * copy and the markov_state).  Probe p's input vector is
+ *   [hidden[p * ld_hidden + 0 .. K_hidden); state[p * ld_state + 0 .. K_state)]
+ * and the Q8_0 row covers K_hidden + K_state elements.  K_hidden > 0 and K_state >= 0 are
+ * multiples of 4 with a sum that is a multiple of 32; hidden and state are 16-byte aligned,
+ * ld_* are multiples of 4 and at least the widths.  The result is bit-identical to
+ * dspark_conf_probe on the concatenated vector. */
+dspark_status dspark_conf_probe_split(const void *w_q8_0, const float *hidden, int K_hidden,
+                                      long long ld_hidden, const float *state, int K_state,
+                                      long long ld_state, float bias, float threshold, int n_probes,
+                                      float *logit_out, int32_t *gate_out, dspark_stream_t stream);
+
 /* =====================================================================================
  * Weight-stationary small-M matvec
  *
@@ -205,6 +218,65 @@ size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K);
 dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32,
                                int M, int N, int K, void *workspace, size_t workspace_bytes,
                                dspark_stream_t stream);
+
+/* =====================================================================================
+ * Draft step with device-side base logits
+ *
+ * Source: vllm.cpp issue #436, "W7 LANDED": the half W7 deferred is a block-forward
+ * variant that returns the base logits on the device instead of downloading
+ * [num_reqs, k, draft_vocab] floats.  Here the draft head's lm_head projection runs as a
+ * weight-stationary matvec (SharpInference issue #441) that writes the fp32 base logits into
+ * device memory, followed by the Markov draft; both are recorded into one CUDA graph.
+ *
+ *   base[r, i, v] = sum_h hidden_states[r * k + i, h] * lm_head[v, h]   (fp32)
+ *   then dspark_markov_draft(base, ...)
+ *
+ * Arguments
+ *   lm_head        fp16 [vocab, hidden_dim], 16-byte aligned
+ *   hidden_states  fp16 [num_reqs * k, hidden_dim], 16-byte aligned
+ *   base_logits    float [num_reqs, k, vocab] device buffer the plan writes and reads
+ *   markov_workspace  >= dspark_markov_workspace_bytes(num_reqs, k, vocab, rank)
+ *   ws_workspace   >= dspark_ws_matvec_workspace_bytes(num_reqs * k, vocab, hidden_dim),
+ *                  zero-filled before first use (see dspark_ws_matvec)
+ *   other arguments as for dspark_markov_draft.
+ * Supported: num_reqs * k <= 16 (the matvec's row limit), plus the limits of the two calls.
+ * ===================================================================================== */
+typedef struct dspark_draft_plan dspark_draft_plan;
+
+dspark_status dspark_draft_plan_create(const uint16_t *lm_head, const uint16_t *hidden_states,
+                                       int hidden_dim, const uint16_t *markov_w1,
+                                       const uint16_t *markov_w2, const int32_t *d2t, int64_t *prev,
+                                       int num_reqs, int k, int vocab, int rank, float *base_logits,
+                                       int64_t *out_ids, void *markov_workspace,
+                                       size_t markov_workspace_bytes, void *ws_workspace,
+                                       size_t ws_workspace_bytes, dspark_draft_plan **plan_out);
+dspark_status dspark_draft_plan_launch(dspark_draft_plan *plan, dspark_stream_t stream);
+void dspark_draft_plan_destroy(dspark_draft_plan *plan);
+
+/* =====================================================================================
+ * Confidence-gated draft (decision stays on the device)
+ *
+ * Source: ds4 PR #772, "Summary" and "Root cause": the confidence probe gates whether the
+ * proposer keeps drafting; the PR evaluates it on the GPU but reads the 4-byte decision back.
+ * Here one CUDA graph holds the probe (one probe over probe_input[0 .. K)) and a conditional
+ * IF node whose body is the Markov draft: the probe kernel sets the condition, so the draft
+ * runs only if sigmoid(z) >= threshold, with no host round trip.  gate_out[0] / logit_out[0]
+ * still receive the decision and the logit.  When the gate is 0 the draft's outputs (out_ids,
+ * prev, the workspace status word) are left untouched.
+ * Arguments: the probe's (see dspark_conf_probe, n_probes = 1) followed by the Markov
+ * draft's (see dspark_markov_draft, no debug outputs).
+ * ===================================================================================== */
+typedef struct dspark_gated_plan dspark_gated_plan;
+
+dspark_status dspark_gated_draft_plan_create(const void *w_q8_0, const float *probe_input, int K,
+                                             float bias, float threshold, float *logit_out,
+                                             int32_t *gate_out, const float *base_logits,
+                                             const uint16_t *markov_w1, const uint16_t *markov_w2,
+                                             const int32_t *d2t, int64_t *prev, int num_reqs, int k,
+                                             int vocab, int rank, int64_t *out_ids, void *workspace,
+                                             size_t workspace_bytes, dspark_gated_plan **plan_out);
+dspark_status dspark_gated_draft_plan_launch(dspark_gated_plan *plan, dspark_stream_t stream);
+void dspark_gated_draft_plan_destroy(dspark_gated_plan *plan);
 
 #ifdef __cplusplus
 }

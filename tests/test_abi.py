@@ -93,6 +93,40 @@ def test_markov_debug_and_plan_validation(dspark_lib):
     assert lib.dspark_markov_status(NULL, NULL) == INVALID
 
 
+def test_draft_plan_validation(dspark_lib):
+    lib = dspark_lib
+    f = lib.dspark_draft_plan_create
+    h = api.ctypes.c_void_p()
+    args = lambda B, k: (FAKE, FAKE, 256, FAKE, FAKE, NULL, FAKE, B, k, 1000, 64, FAKE, FAKE, FAKE,
+                         1 << 20, FAKE, 1 << 20)
+    assert f(*args(1, 4), None) == INVALID
+    assert f(*args(2, 9), api.ctypes.byref(h)) == UNSUPPORTED
+    assert f(*args(0, 4), api.ctypes.byref(h)) == INVALID
+    assert lib.dspark_draft_plan_launch(NULL, NULL) == INVALID
+    lib.dspark_draft_plan_destroy(NULL)
+
+
+def test_gated_plan_validation(dspark_lib):
+    lib = dspark_lib
+    f = lib.dspark_gated_draft_plan_create
+    h = api.ctypes.c_void_p()
+    args = lambda K, B, k: (FAKE, FAKE, K, 0.0, 0.5, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, B, k,
+                            1000, 64, FAKE, FAKE, 1 << 20)
+    assert f(*args(7424, 1, 4), None) == INVALID
+    assert f(*args(7425, 1, 4), api.ctypes.byref(h)) == INVALID
+    assert f(*args(7424, 0, 4), api.ctypes.byref(h)) == INVALID
+    assert lib.dspark_gated_draft_plan_launch(NULL, NULL) == INVALID
+    lib.dspark_gated_draft_plan_destroy(NULL)
+
+
+def test_probe_split_validation(dspark_lib):
+    f = dspark_lib.dspark_conf_probe_split
+    assert f(FAKE, FAKE, 7168, 7168, FAKE, 250, 256, 0.0, 0.5, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 7168, 7000, FAKE, 256, 256, 0.0, 0.5, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 7168, 7168, NULL, 256, 256, 0.0, 0.5, 1, NULL, FAKE, NULL) == INVALID
+    assert f(FAKE, FAKE, 7168, 7168, FAKE, 256, 256, 0.0, 0.5, 0, NULL, FAKE, NULL) == 0
+
+
 def test_probe_validation(dspark_lib):
     lib = dspark_lib
     f = lib.dspark_conf_probe

@@ -70,3 +70,21 @@ def test_rejects_misaligned_hidden():
     flat = torch.from_numpy(inp["hidden"].reshape(-1)).cuda()
     with pytest.raises(api.DsparkError):
         api.conf_probe(wq, flat[1:65], inp["bias"], 0.5)
+
+
+def test_split_input_matches_concatenated():
+    """[hidden(7168); markov_state(256)] given as two buffers (strided views of a wider
+    buffer for the hidden part) gives bit-identical logits to the contiguous probe."""
+    inp = synth.probe_inputs(512, 7424, seed=10)
+    full = torch.from_numpy(inp["hidden"]).cuda()
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    wide = torch.zeros((512, 7168 + 64), dtype=torch.float32, device="cuda")
+    wide[:, :7168] = full[:, :7168]
+    hidden = wide[:, :7168]                 # row stride 7232 floats
+    state = full[:, 7168:].contiguous()     # [512, 256]
+    z_split, g_split = api.conf_probe_split(wq, hidden, state, inp["bias"], 0.5)
+    z_full, g_full = api.conf_probe(wq, full, inp["bias"], 0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(z_split.view(torch.int32), z_full.view(torch.int32))
+    assert torch.equal(g_split, g_full)
+    parity.check_probe(inp, z_split.cpu().numpy(), g_split.cpu().numpy())
