@@ -29,6 +29,7 @@ import numpy as np
 _S_BASE, _S_W1, _S_W2, _S_PREV, _S_D2T, _S_TIES = 1, 2, 3, 4, 5, 6
 _S_QW, _S_QD, _S_HID, _S_BIAS = 11, 12, 13, 14
 _S_WSW, _S_WSX = 21, 22
+_S_Q8Q, _S_Q8D = 31, 32
 
 TARGET_VOCAB = 151936
 Q8_0_BLOCK = 32          # elements per Q8_0 block
@@ -169,3 +170,25 @@ def ws_inputs(M: int, N: int, K: int, *, seed: int = 0, w_sd: float = 0.02,
     W = f32_to_f16_bits(_normal(seed, _S_WSW, (N, K), w_sd))
     X = f32_to_f16_bits(_normal(seed, _S_WSX, (M, K), x_sd))
     return dict(W=W, X=X, M=M, N=N, K=K)
+
+
+def ws_q8_inputs(M: int, N: int, K: int, *, seed: int = 0, d_sd: float = 2e-4,
+                 power_of_two_scales: bool = False) -> dict:
+    """Inputs of a quantized weight-stationary matvec: W as Q8_0 blocks (row-major by weight
+    row: N x K/32 blocks of 34 bytes, q ~ U{-127..127}, fp16 scales |N(0, d_sd)|), X fp16 bits
+    [M, K] N(0,1).  With power_of_two_scales every scale is 2^-j (j in 8..12), so every
+    dequantized weight d*q is exactly representable in fp16."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // 32
+    q = _rng(seed, _S_Q8Q).integers(-127, 128, size=(N, nb, 32), dtype=np.int64).astype(np.int8)
+    if power_of_two_scales:
+        j = _rng(seed, _S_Q8D).integers(8, 13, size=(N, nb))
+        d = np.ldexp(1.0, -j).astype(np.float32)
+    else:
+        d = np.abs(_rng(seed, _S_Q8D).standard_normal((N, nb))).astype(np.float32) * np.float32(d_sd)
+    blocks = np.zeros((N, nb, 34), dtype=np.uint8)
+    blocks[:, :, 0:2] = f32_to_f16_bits(d).astype("<u2").view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:] = q.view(np.uint8)
+    X = f32_to_f16_bits(_normal(seed, _S_WSX, (M, K), 1.0))
+    return dict(Wq8=blocks.reshape(-1).copy(), X=X, M=M, N=N, K=K)

@@ -10,6 +10,7 @@ What each function follows:
   markov_draft  vllm.cpp issue #436 "SPEC-DSPARK W7", section "The fix"
   conf_probe    ds4 PR #772 "dspark: cut per-cycle CUDA overheads", section "Summary"
   ws_matvec     SharpInference issue #441, sections "Observation" / "Proposed work"
+  ws_matvec_q8  SharpInference issue #441, "Proposed work" (quantized WS weights)
 """
 from __future__ import annotations
 
@@ -57,6 +58,8 @@ def _load():
         lib.oracle_conf_probe.restype = i
         lib.oracle_ws_matvec.argtypes = [P, P, i, i, i, P, P]
         lib.oracle_ws_matvec.restype = i
+        lib.oracle_ws_matvec_q8.argtypes = [P, P, i, i, i, P]
+        lib.oracle_ws_matvec_q8.restype = i
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = d
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -141,6 +144,22 @@ def ws_matvec(W, X):
     if rc != 0:
         raise ValueError("oracle_ws_matvec rejected its arguments")
     return Y, Y16
+
+
+def ws_matvec_q8(Wq8, X):
+    """Y = X dequant(W)^T in fp64; Wq8 uint8 [N * K/32 * 34] (Q8_0 blocks, row-major by row),
+    X fp16 bits [M, K]; returns Y float64 [M, N]."""
+    lib = _load()
+    Wq8 = _c(Wq8, np.uint8).reshape(-1)
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    N = Wq8.size // ((K // 32) * 34)
+    assert Wq8.size == N * (K // 32) * 34
+    Y = np.empty((M, N), np.float64)
+    rc = lib.oracle_ws_matvec_q8(_ptr(Wq8), _ptr(X), M, N, K, _ptr(Y))
+    if rc != 0:
+        raise ValueError("oracle_ws_matvec_q8 rejected its arguments")
+    return Y
 
 
 def bf16_to_f64(bits: int) -> float:

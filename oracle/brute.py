@@ -81,3 +81,20 @@ def ws_matvec(W, X):
     Xf = [[f16_exact(X[m, kk]) for kk in range(K)] for m in range(M)]
     return [[sum((Xf[m][kk] * Wf[n][kk] for kk in range(K)), Fraction(0)) for n in range(N)]
             for m in range(M)]
+
+
+def ws_matvec_q8(Wq8, X, N, K):
+    """Exact Y[m][n] for Q8_0 weights (Fractions)."""
+    nb = K // 32
+    blocks = np.asarray(Wq8, dtype=np.uint8).reshape(N, nb, 34)
+    M = X.shape[0]
+    Xf = [[f16_exact(X[m, kk]) for kk in range(K)] for m in range(M)]
+    out = [[Fraction(0)] * N for _ in range(M)]
+    for n in range(N):
+        for b in range(nb):
+            d = f16_exact(int(blocks[n, b, 0]) | (int(blocks[n, b, 1]) << 8))
+            q = blocks[n, b, 2:].view(np.int8)
+            for m in range(M):
+                s = sum((int(q[j]) * Xf[m][32 * b + j] for j in range(32)), Fraction(0))
+                out[m][n] += d * s
+    return out

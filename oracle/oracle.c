@@ -22,7 +22,8 @@
  *    Q8_0 weights whose result gates the proposal length.
  *  - SharpInference issue #441 "DSpark GPU draft round runs ~3x the bandwidth
  *    floor", sections "Observation" and "Proposed work": the draft projections are
- *    fp16 GEMMs with M = B = 7 rows, Y = X W^T with the weight read once for all rows.
+ *    fp16 GEMMs with M = B = 7 rows, Y = X W^T with the weight read once for all rows;
+ *    the weight-stationary kernels it reuses read quantized (Q8_0) weights.
  *
  * Parity pins (tests/test_oracle_*.py): exact brute force with rational
  * arithmetic on tiny inputs, the zero-markov_w2 closed form, identity vs
@@ -241,5 +242,38 @@ int oracle_ws_matvec(const uint16_t *W, const uint16_t *X, int M, int N, int K, 
     }
     free(xd);
     free(wd);
+    return 0;
+}
+
+/* ---- quantized weight-stationary matvec ---------------------------------------- */
+
+/*
+ * SharpInference #441, "Proposed work": the weight-stationary kernels of #194 read
+ * quantized weights.  With Q8_0 weights (row n, block b: fp16 scale d_{n,b} and int8 q):
+ *   Y[m, n] = sum_b d_{n,b} * sum_{j<32} q_{n,b,j} * X[m, 32b + j]
+ * W_q8 is [N][K/32] blocks of 34 bytes (ggml layout, as in oracle_conf_probe); X fp16 [M, K];
+ * Y [M, N] double.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_ws_matvec_q8(const uint8_t *Wq8, const uint16_t *X, int M, int N, int K, double *Y)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 32 || !Wq8 || !X || !Y)
+        return -1;
+    int nb = K / 32;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                const uint8_t *blk = Wq8 + ((size_t)n * nb + b) * 34;
+                double d = oracle_f16_to_f64((uint16_t)(blk[0] | ((uint16_t)blk[1] << 8)));
+                double s = 0.0;
+                for (int j = 0; j < 32; ++j) {
+                    int8_t q;
+                    memcpy(&q, blk + 2 + j, 1);
+                    s += (double)q * oracle_f16_to_f64(X[(size_t)m * K + 32 * b + j]);
+                }
+                acc += d * s;
+            }
+            Y[(size_t)m * N + n] = acc;
+        }
     return 0;
 }

@@ -57,3 +57,41 @@ def test_fp16_output_is_rne_of_exact(oracle_lib):
     inp = synth.ws_inputs(4, 16, 64, seed=7)
     Y, Y16 = oracle.ws_matvec(inp["W"], inp["X"])
     np.testing.assert_array_equal(Y16, Y.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(2, 3, 64, 0), (3, 2, 96, 1)])
+def test_q8_brute_force(oracle_lib, M, N, K, seed):
+    inp = synth.ws_q8_inputs(M, N, K, seed=seed, d_sd=0.05)
+    Y = oracle.ws_matvec_q8(inp["Wq8"], inp["X"])
+    exact = brute.ws_matvec_q8(inp["Wq8"], inp["X"], N, K)
+    for m in range(M):
+        for n in range(N):
+            assert Y[m, n] == pytest.approx(float(exact[m][n]), rel=1e-13, abs=1e-13)
+
+
+def test_q8_reduces_to_fp16_matvec(oracle_lib):
+    """With power-of-two scales every d*q is an fp16 number, so the quantized matvec must
+    equal the fp16 matvec of the dequantized weight exactly."""
+    M, N, K = 5, 40, 256
+    inp = synth.ws_q8_inputs(M, N, K, seed=2, power_of_two_scales=True)
+    blk = inp["Wq8"].reshape(N, K // 32, 34)
+    d = blk[:, :, :2].copy().view("<u2").reshape(N, K // 32).view(np.float16).astype(np.float64)
+    q = blk[:, :, 2:].copy().view(np.int8).astype(np.float64)
+    Wd = (d[:, :, None] * q).reshape(N, K)
+    W16 = Wd.astype(np.float16)
+    assert np.array_equal(W16.astype(np.float64), Wd)
+    Yq = oracle.ws_matvec_q8(inp["Wq8"], inp["X"])
+    Yf, _ = oracle.ws_matvec(W16.view(np.uint16), inp["X"])
+    np.testing.assert_array_equal(Yq, Yf)
+
+
+def test_q8_one_hot_activation(oracle_lib):
+    M, N, K = 1, 6, 128
+    inp = synth.ws_q8_inputs(M, N, K, seed=3)
+    X = np.zeros((1, K), np.float32)
+    X[0, 70] = 1.0
+    Y = oracle.ws_matvec_q8(inp["Wq8"], synth.f32_to_f16_bits(X))
+    blk = inp["Wq8"].reshape(N, K // 32, 34)
+    d = blk[:, 2, :2].copy().view("<u2").reshape(N).view(np.float16).astype(np.float64)
+    q = blk[:, 2, 2 + 6].view(np.int8).astype(np.float64)
+    np.testing.assert_array_equal(Y[0], d * q)
