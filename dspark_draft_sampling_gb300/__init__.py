@@ -15,6 +15,9 @@ from .api import (  # noqa: F401
     load_library,
     markov_draft,
     markov_workspace_bytes,
+    q8_0_repack,
     ws_matvec,
+    ws_matvec_q8,
+    ws_matvec_q8_workspace_bytes,
     ws_matvec_workspace_bytes,
 )

@@ -46,6 +46,9 @@ SIGNATURES = {
                                      _I, _P, _P, _P]),
     "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "dspark_q8_0_repack": (_I, [_P, _P, _P, _I, _I, _P]),
+    "dspark_ws_matvec_q8_workspace_bytes": (_Z, [_I, _I, _I]),
+    "dspark_ws_matvec_q8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
 }
 
 _lock = threading.Lock()
@@ -395,5 +398,60 @@ def ws_matvec(W, X, *, out=None, out_fp32: bool = False, workspace=None, stream=
                               _ptr(out, "out", dtypes=(torch.float16, torch.float32)),
                               1 if y_fp32 else 0, M, N, K,
                               _ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def q8_0_repack(w_q8_0, N: int, K: int, *, stream=None):
+    """Split Q8_0 blocks (uint8 [N * K/32 * 34], row-major by weight row) into
+    (q int8 [N, K], d fp16-bit int16 [N, K/32]) on the device."""
+    lib = load_library()
+    if K <= 0 or K % 32:
+        raise ValueError("K must be a positive multiple of 32")
+    if w_q8_0.numel() != N * (K // 32) * 34:
+        raise ValueError("w_q8_0 does not hold N * K/32 Q8_0 blocks")
+    src = _ptr(w_q8_0, "w_q8_0", dtypes=(torch.uint8,))
+    q = torch.empty((N, K), dtype=torch.int8, device=w_q8_0.device)
+    d = torch.empty((N, K // 32), dtype=torch.int16, device=w_q8_0.device)
+    st = lib.dspark_q8_0_repack(src, _ptr(q, "q"), _ptr(d, "d"), N, K, _stream(stream))
+    _check(lib, st)
+    return q, d
+
+
+def ws_matvec_q8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().dspark_ws_matvec_q8_workspace_bytes(M, N, K))
+
+
+def new_ws_q8_workspace(M: int, N: int, K: int, device=None):
+    """Zero-filled scratch for ws_matvec_q8 (the kernel leaves it zero-filled after each call)."""
+    n = ws_matvec_q8_workspace_bytes(M, N, K)
+    if n == 0:
+        raise DsparkError(DSPARK_ERR_CUDA, "could not size the ws_matvec_q8 workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def ws_matvec_q8(Wq, Wd, X, *, out=None, out_fp32: bool = False, workspace=None, stream=None):
+    """Y = X dequant(W)^T.  Wq int8 [N, K], Wd fp16 bits [N, K/32] (from q8_0_repack),
+    X fp16 [M, K]; returns Y [M, N] (fp16, or fp32)."""
+    lib = load_library()
+    N, K = Wq.shape
+    M, K2 = X.shape
+    if K != K2:
+        raise ValueError("Wq and X disagree on K")
+    if tuple(Wd.shape) != (N, K // 32):
+        raise ValueError("Wd must be [N, K/32]")
+    q_p = _ptr(Wq, "Wq", dtypes=(torch.int8,))
+    d_p = _ptr(Wd, "Wd", itemsize=2, dtypes=_BITS16)
+    x_p = _ptr(X, "X", itemsize=2, dtypes=_BITS16)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32 if out_fp32 else torch.float16,
+                          device=Wq.device)
+    if workspace is None:
+        workspace = new_ws_q8_workspace(M, N, K, Wq.device)
+    y_fp32 = out.dtype == torch.float32
+    st = lib.dspark_ws_matvec_q8(q_p, d_p, x_p,
+                                 _ptr(out, "out", dtypes=(torch.float16, torch.float32)),
+                                 1 if y_fp32 else 0, M, N, K,
+                                 _ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
     _check(lib, st)
     return out

@@ -43,8 +43,10 @@ int current_sm_count(int *sm_count) {
     return DSPARK_OK;
 }
 
-dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
-                           uint32_t box_rows, uint32_t box_cols) {
+namespace {
+
+dspark_status encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void *base,
+                           uint32_t rank, const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
         void *fn = nullptr;
@@ -54,16 +56,43 @@ dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64
             return fail(DSPARK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(DSPARK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
     return DSPARK_OK;
+}
+
+dspark_status encode_tiled_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                              CUtensorMapSwizzle swizzle, const void *base, uint64_t rows, uint64_t cols,
+                              uint32_t box_rows, uint32_t box_cols) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * elem_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    return encode_tiled(map, dtype, swizzle, base, 2, dims, strides, box);
+}
+
+}  // namespace
+
+dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_cols) {
+    return encode_tiled_2d(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                           CU_TENSOR_MAP_SWIZZLE_128B, base, rows, cols, box_rows, box_cols);
+}
+
+dspark_status make_tmap_f16_kblocks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                                    uint32_t box_rows, uint32_t box_kblocks) {
+    const cuuint64_t dims[3] = {64, rows, cols / 64};
+    const cuuint64_t strides[2] = {cols * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, box_kblocks};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
+}
+
+dspark_status make_tmap_2d_u8_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                                    uint32_t box_rows, uint32_t box_cols) {
+    return encode_tiled_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, CU_TENSOR_MAP_SWIZZLE_128B, base, rows, cols,
+                           box_rows, box_cols);
 }
 
 }  // namespace dspark

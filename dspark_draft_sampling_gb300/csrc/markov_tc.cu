@@ -45,10 +45,6 @@ constexpr int kHMaxBytes = 4 * kHBlockBytes;       // rank <= 256
 constexpr uint32_t kTmemCols = 32;
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kBoxBytes + 2 * kHMaxBytes + 512;
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {

@@ -1,0 +1,528 @@
+// Weight-stationary small-M matvec with Q8_0 weights: Y[M, N] = X[M, K] . dequant(W)[N, K]^T.
+//
+// Method (SharpInference issue #441, "Proposed work"): the weight-stationary kernels of its
+// #194 read quantized weights, streaming each weight once for all M rows; the issue notes
+// that an SoA repack may be needed.  Weights here are Q8_0 (per 32 elements of a row: an
+// fp16 scale d and 32 int8 q; weight = d * q).
+//
+// Layout: dspark_q8_0_repack turns the ggml array of 34-byte blocks into two row-major
+// arrays, q int8 [N, K] and d fp16 [N, K/32], so the int8 tiles can be moved by 2-D TMA
+// tensor copies (the 34-byte blocks cannot).
+//
+// Arithmetic: the dequantized weight d * q has up to 18 significant bits, so it cannot be a
+// 16-bit tensor-core operand without rounding; q itself can (every int8 is an fp16 number).
+// The kernel therefore runs one tcgen05 MMA group per Q8_0 block:
+//     S[n, b, m] = sum_{j<32} q[n, 32b + j] * X[m, 32b + j]     (fp16 x fp16 products, exact;
+//                                                                 fp32 accumulation in TMEM)
+// and the epilogue applies the scale in fp32:  y[n, m] += d[n, b] * S[n, b, m], blocks in k
+// order.  Every output is summed in one fixed order (blocks, then split-K units in order), so
+// results are deterministic and row m's does not depend on M.
+//
+// GB300 design (one CTA per SM, 15 warps)
+//  * Work unit = (128 weight rows, a range of 256-k superblocks); K is split so that there is
+//    about one unit per SM.
+//  * Warp 12 (one thread) streams, per 128-k stage, the int8 tile [128 rows x 128 k] (16 KB,
+//    128-byte swizzle) and the X tile [16 rows x 128 k] (two 2 KB fp16 atoms in one 3-D copy;
+//    rows >= M read as zero) with TMA tensor copies through a 10-stage ring (200 KB).
+//  * Warps 4-7 take the even stages and warps 8-11 the odd ones: each thread converts one weight
+//    row's 128 int8 to fp16 (a byte permute puts q + 128 into the mantissa of 1024, one packed
+//    subtraction of 1152 leaves q exactly) and writes them with tcgen05.st straight into tensor
+//    memory, where the MMA takes its A operand: the fp16 copy never touches shared memory.
+//  * Warp 13 allocates all 512 TMEM columns (16 accumulator slots of 128 x 16 fp32 and a 4-slot
+//    ring of fp16 A tiles).  Warps 13 and 14 issue the MMAs of the even and odd stages: per
+//    Q8_0 block two tcgen05.mma kind::f16 (M=128, N=16, K=16; A from TMEM, B = X from shared
+//    memory) into a fresh accumulator slot.  Two issuers, 8 MMAs per barrier round trip and one
+//    tcgen05.commit per stage keep the single-thread issue cost below the weight stream's pace:
+//    that one commit hands the stage's 4 slots to the epilogue and frees its A tile and its
+//    shared-memory slot.
+//  * Warps 0-3 (one TMEM lane = one weight row per thread) read a stage's 4 x 16 sums with
+//    tcgen05.ld and fold them in with the row's scales (loaded 8 at a time from global memory,
+//    four loads ahead).
+//    With one unit per row block they write Y directly; otherwise they store fp32 partials and
+//    the last unit of the row block (a ticket counter) sums them in unit order.
+#include <cuda_fp16.h>
+
+#include "tc.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 480;          // warps 0-3 epilogue, 4-11 convert, 12 TMA, 13-14 MMA
+constexpr int kConvWarps = 8;          // two groups of 4, alternate stages
+constexpr int kTmaWarp = 4 + kConvWarps;
+constexpr int kMmaWarp = kTmaWarp + 1;  // and kMmaWarp + 1
+constexpr int kRows = 128;             // weight rows per unit: MMA M, TMEM lanes
+constexpr int kNPad = 16;              // MMA N: X rows padded to 16
+constexpr int kKS = 128;               // k per stage: 128 B of int8 per row (the 128-byte swizzle span)
+constexpr int kBlocksPerStage = kKS / 32;   // 4 Q8_0 blocks
+constexpr int kSuper = 2;              // stages per 256-k superblock (8 scales of a row)
+constexpr int kStages = 10;            // shared-memory ring (even, so each stage parity keeps its slots)
+constexpr int kQBytes = kRows * kKS;                // 16 KB int8 tile
+constexpr int kXAtomBytes = kNPad * 64 * 2;         // 2 KB: 16 rows x 64 fp16
+constexpr int kSlotBytes = kQBytes + 2 * kXAtomBytes;  // 20 KB (multiple of 1024)
+constexpr int kTSlots = 16;            // TMEM accumulator slots (4 stages x 4 blocks)
+constexpr int kTGroups = kTSlots / kBlocksPerStage;  // one group per stage
+constexpr int kASlots = 4;             // TMEM ring of fp16 A tiles
+constexpr uint32_t kACols = kKS / 2;   // 64 columns: 128 fp16 per lane
+constexpr uint32_t kAColBase = kTSlots * kNPad;                  // 256
+constexpr uint32_t kTmemCols = kAColBase + kASlots * kACols;     // 512
+constexpr int kNumBars = 2 * kStages + kASlots + kTGroups + 2;
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kSlotBytes + kNumBars * 8 + 16;
+constexpr size_t kTicketBytes = 65536;  // up to 16384 row blocks (N <= 2,097,152)
+static_assert(kTmemCols == 512, "the TMEM allocation must be a power of two <= 512");
+static_assert(kStages % 2 == 0 && kASlots % 2 == 0 && kTGroups % 2 == 0, "rings must keep stage parity");
+static_assert(kASlots == kTGroups && kASlots < kStages, "stage j uses A slot and accumulator group j % 4");
+
+struct Q8Args {
+    const uint16_t *d;  // [N, K/32] fp16 scales
+    void *Y;
+    float *partial;     // [units][128][16] fp32 (split-K only)
+    unsigned *tickets;  // [row blocks]
+    int y_fp32;
+    int M, N, K;
+    int nsb;  // 256-k superblocks
+    int S;    // units per row block
+    unsigned long long timeout_ns;
+};
+
+// Two int8 values (bytes of u selected by `sel`, already biased to q + 128) -> fp16x2 holding
+// q exactly: the byte permute builds the fp16 patterns 0x64XX = 1024 + XX.
+__device__ __forceinline__ uint32_t q8_pair_to_f16x2(uint32_t u, uint32_t sel) {
+    uint32_t h = __byte_perm(u, 0x64646464u, sel);
+    __half2 v = *reinterpret_cast<__half2 *>(&h);
+    v = __hsub2(v, __half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));  // - 1152
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint4 ldg_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ws_q8_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, Q8Args a) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    unsigned char *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);  // 1024-aligned slots
+    // Barriers.  done[j % kStages] completes once per stage j when the stage's MMAs have
+    // finished (one tcgen05.commit): its shared-memory slot may be refilled, its TMEM A slot
+    // reused and its accumulators read.
+    uint64_t *full_r = reinterpret_cast<uint64_t *>(ring + size_t(kStages) * kSlotBytes);  // TMA landed
+    uint64_t *done = full_r + kStages;
+    uint64_t *full_a = done + kStages;     // fp16 A tile written to TMEM (per A slot)
+    uint64_t *empty_t = full_a + kASlots;  // accumulator group drained by the epilogue
+    uint64_t *mma_done = empty_t + kTGroups;  // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
+    int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.x;
+    const int rb = unit / a.S;
+    const int sk = unit % a.S;
+    const int sb0 = static_cast<int>(static_cast<long long>(sk) * a.nsb / a.S);
+    const int sb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nsb / a.S);
+    const int nsup = sb1 - sb0;
+    const int nst = nsup * kSuper;  // 128-k stages of this unit
+    const int ks0 = sb0 * kSuper;   // its first 128-k stage index along K
+    const int n0 = rb * kRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_r[s], 1);
+            mbar_init(&done[s], 1);
+        }
+        for (int s = 0; s < kASlots; ++s) mbar_init(&full_a[s], 4);
+        for (int g = 0; g < kTGroups; ++g) mbar_init(&empty_t[g], 4);
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTmaWarp) {
+        // ---- TMA producer: int8 tile + two X atoms per stage ----
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int issued = 0, st = 0;
+            uint32_t ph = 0;
+            for (int j = 0; j < nst; ++j) {
+                if (!mbar_wait(&done[st], ph ^ 1u, a.timeout_ns)) break;  // stage j - kStages finished
+                unsigned char *slot = ring + size_t(st) * kSlotBytes;
+                const int k0 = (ks0 + j) * kKS;
+                mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
+                tma_load_2d(slot, &tmQ, k0, n0, &full_r[st], pol_q);
+                tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
+                ++issued;
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            // copies still in flight (possible only after a consumer gave up) land before exit
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.timeout_ns);
+        }
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ---- MMA issuers: warp 13 the even stages, warp 14 the odd ones ----
+        if (lane == 0) {
+            const int par = warp - kMmaWarp;
+            constexpr uint32_t idesc = idesc_f16(false, kRows, kNPad);
+            const uint64_t dX0 = smem_desc_sw128(smem_addr(ring + kQBytes));
+            // ring positions of stage j = par, par + 2, ...: slots advance by 2 and wrap
+            int st = par, g = par;  // stage j: shared-memory slot j % kStages, A slot = group = j % 4
+            uint32_t phg = 0;
+            for (int j = par; j < nst; j += 2) {
+                // the converters arrive on full_a only after the stage's TMA copies (X included)
+                // have landed, so this one wait orders both operands before the MMAs
+                if (!mbar_wait(&full_a[g], phg, a.timeout_ns)) break;
+                if (!mbar_wait(&empty_t[g], phg ^ 1u, a.timeout_ns)) break;
+                tc_fence_after();
+                const uint64_t dB = dX0 + static_cast<uint64_t>(st * (kSlotBytes >> 4));
+                const uint32_t ta = tmem + kAColBase + static_cast<uint32_t>(g) * kACols;
+                const uint32_t td = tmem + static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+#pragma unroll
+                for (int b = 0; b < kBlocksPerStage; ++b) {
+                    // block b = k 32b .. 32b + 31: A columns 16b (+8); X atom b/2, byte offset 64 (b%2) (+32)
+                    const uint64_t db = dB + static_cast<uint64_t>((b >> 1) * (kXAtomBytes >> 4) + (b & 1) * 4);
+                    tc_mma_f16_ts(td + b * kNPad, ta + 16 * b, db, idesc, 0u);
+                    tc_mma_f16_ts(td + b * kNPad, ta + 16 * b + 8, db + 2, idesc, 1u);
+                }
+                tc_commit(&done[st]);
+                if ((st += 2) >= kStages) st -= kStages;
+                if ((g += 2) >= kTGroups) {
+                    g -= kTGroups;
+                    phg ^= 1u;
+                }
+            }
+            tc_commit(&mma_done[par]);  // arrives once every MMA this thread issued has completed
+            mbar_wait(&mma_done[par], 0, a.timeout_ns);
+        }
+    } else if (warp >= 4) {
+        // ---- converters: one weight row's 128 int8 -> 128 fp16 in TMEM, alternate stages ----
+        const int par = (warp - 4) >> 2;  // 0: even stages, 1: odd stages
+        const int lg = warp & 3;          // TMEM lane quarter this warp may access
+        const int r = lg * 32 + lane;     // weight row within the tile
+        const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
+        int st = par, as = par;
+        uint32_t phr = 0;
+        bool broken = false;
+        for (int j = par; j < nst; j += 2) {
+            if (!broken && !mbar_wait(&full_r[st], phr, a.timeout_ns)) broken = true;
+            if (j >= kASlots) {  // A slot j % 4 was last read by stage j - 4
+                const int jp = j - kASlots;
+                if (!broken && !mbar_wait(&done[jp % kStages], static_cast<uint32_t>((jp / kStages) & 1), a.timeout_ns))
+                    broken = true;
+            }
+            broken = __any_sync(0xffffffffu, broken);
+            if (!broken) {
+                const unsigned char *rowp = ring + size_t(st) * kSlotBytes + r * kKS;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // two halves of 64 k: 32 TMEM columns each
+                    uint32_t v[32];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = 4 * h + cc;  // 16-byte chunk c = k 16c .. 16c + 15, stored at c ^ (r & 7)
+                        uint4 w = *reinterpret_cast<const uint4 *>(rowp + ((c ^ (r & 7)) << 4));
+                        w.x ^= 0x80808080u;
+                        w.y ^= 0x80808080u;
+                        w.z ^= 0x80808080u;
+                        w.w ^= 0x80808080u;
+                        v[8 * cc + 0] = q8_pair_to_f16x2(w.x, 0x4140);
+                        v[8 * cc + 1] = q8_pair_to_f16x2(w.x, 0x4342);
+                        v[8 * cc + 2] = q8_pair_to_f16x2(w.y, 0x4140);
+                        v[8 * cc + 3] = q8_pair_to_f16x2(w.y, 0x4342);
+                        v[8 * cc + 4] = q8_pair_to_f16x2(w.z, 0x4140);
+                        v[8 * cc + 5] = q8_pair_to_f16x2(w.z, 0x4342);
+                        v[8 * cc + 6] = q8_pair_to_f16x2(w.w, 0x4140);
+                        v[8 * cc + 7] = q8_pair_to_f16x2(w.w, 0x4342);
+                    }
+                    tmem_st_32(tmem + tlane + kAColBase + static_cast<uint32_t>(as) * kACols + 32u * h, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0 && !broken) mbar_arrive(&full_a[as]);
+            if ((st += 2) >= kStages) {
+                st -= kStages;
+                phr ^= 1u;
+            }
+            if ((as += 2) >= kASlots) as -= kASlots;
+        }
+    } else {
+        // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 ----
+        const int lrow = warp * 32 + lane;
+        const int row = n0 + lrow;
+        const bool rowok = row < a.N;
+        const uint16_t *drow = a.d + size_t(rowok ? row : 0) * (a.K / 32) + size_t(sb0) * 8;
+        // the row's scales, 8 per superblock, prefetched kDAhead superblocks ahead: a load issued
+        // while the weight stream saturates HBM takes microseconds to return
+        constexpr int kDAhead = 4;
+        uint4 dq[kDAhead];
+#pragma unroll
+        for (int i = 0; i < kDAhead; ++i)
+            dq[i] = (rowok && i < nsup) ? ldg_u4(drow + size_t(i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+        float acc[kNPad];
+#pragma unroll
+        for (int m = 0; m < kNPad; ++m) acc[m] = 0.f;
+        int g = 0, st = 0;  // stage j: accumulator group j % 4, done[j % kStages]
+        uint32_t phd = 0;
+        bool ok = true;
+        for (int s = 0; s < nsup; ++s) {
+            const uint32_t dw[4] = {dq[0].x, dq[0].y, dq[0].z, dq[0].w};
+#pragma unroll
+            for (int i = 0; i + 1 < kDAhead; ++i) dq[i] = dq[i + 1];
+            dq[kDAhead - 1] = (rowok && s + kDAhead < nsup) ? ldg_u4(drow + size_t(s + kDAhead) * 8)
+                                                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int h = 0; h < kSuper; ++h) {  // one stage = one group of 4 accumulator slots
+                if (ok) ok = mbar_wait(&done[st], phd, a.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                uint32_t v[kBlocksPerStage][16];
+                if (ok) {
+                    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
+                                        static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+#pragma unroll
+                    for (int u = 0; u < kBlocksPerStage; ++u) tmem_ld_16_async(ta + u * kNPad, v[u]);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kBlocksPerStage; ++u)
+#pragma unroll
+                        for (int m = 0; m < kNPad; ++m) v[u][m] = 0u;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
+#pragma unroll
+                for (int u = 0; u < kBlocksPerStage; ++u) {
+                    const int b = h * kBlocksPerStage + u;  // Q8_0 block within the superblock
+                    const float dsc = __half2float(__ushort_as_half(
+                        static_cast<unsigned short>((b & 1) ? (dw[b >> 1] >> 16) : (dw[b >> 1] & 0xffffu))));
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) acc[m] = fmaf(dsc, __uint_as_float(v[u][m]), acc[m]);
+                }
+                if (++g == kTGroups) g = 0;
+                if (++st == kStages) {
+                    st = 0;
+                    phd ^= 1u;
+                }
+            }
+        }
+        const int M = a.M;
+        if (a.S == 1) {
+            if (ok && rowok) {
+#pragma unroll
+                for (int m = 0; m < kNPad; ++m) {
+                    if (m < M) {
+                        const size_t o = size_t(m) * a.N + row;
+                        if (a.y_fp32)
+                            static_cast<float *>(a.Y)[o] = acc[m];
+                        else
+                            static_cast<__half *>(a.Y)[o] = __float2half_rn(acc[m]);
+                    }
+                }
+            }
+        } else {
+            float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(unit) * kRows + lrow) * kNPad);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) p[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (threadIdx.x == 0) *s_last = (atomicAdd(&a.tickets[rb], 1u) == static_cast<unsigned>(a.S - 1));
+            named_bar_sync(1, 128);
+            if (*s_last) {
+                __threadfence();
+                if (ok && rowok) {
+                    // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads issued four
+                    // units at a time so their latencies overlap, the sum order is fixed
+                    const float4 *base =
+                        reinterpret_cast<const float4 *>(a.partial + (size_t(rb) * a.S * kRows + lrow) * kNPad);
+                    constexpr size_t kUnitF4 = size_t(kRows) * kNPad / 4;
+                    float y[kNPad];
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
+                    int s = 0;
+                    for (; s + 4 <= a.S; s += 4) {
+                        float4 tq[4][4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) tq[u][q] = __ldcg(base + size_t(s + u) * kUnitF4 + q);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                y[4 * q] += tq[u][q].x;
+                                y[4 * q + 1] += tq[u][q].y;
+                                y[4 * q + 2] += tq[u][q].z;
+                                y[4 * q + 3] += tq[u][q].w;
+                            }
+                    }
+                    for (; s < a.S; ++s) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 tq = __ldcg(base + size_t(s) * kUnitF4 + q);
+                            y[4 * q] += tq.x;
+                            y[4 * q + 1] += tq.y;
+                            y[4 * q + 2] += tq.z;
+                            y[4 * q + 3] += tq.w;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) {
+                        if (m < M) {
+                            const size_t o = size_t(m) * a.N + row;
+                            if (a.y_fp32)
+                                static_cast<float *>(a.Y)[o] = y[m];
+                            else
+                                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+                        }
+                    }
+                }
+                if (threadIdx.x == 0) a.tickets[rb] = 0u;  // zero again for the next call
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+struct Plan {
+    int nrb, nsb, S;
+};
+
+Plan plan_for(int N, int K, int sms) {
+    Plan p;
+    p.nrb = (N + kRows - 1) / kRows;
+    p.nsb = K / (kKS * kSuper);
+    // about one unit per SM, each with at least one superblock
+    int S = sms / p.nrb;
+    if (S > p.nsb) S = p.nsb;
+    if (S < 1) S = 1;
+    p.S = S;
+    return p;
+}
+
+size_t workspace_bytes_for(const Plan &p) {
+    if (p.S == 1) return kTicketBytes;
+    return kTicketBytes + size_t(p.nrb) * p.S * kRows * kNPad * sizeof(float);
+}
+
+__global__ void q8_0_repack_kernel(const uint8_t *__restrict__ aos, int8_t *__restrict__ q, uint16_t *__restrict__ d,
+                                   long long nblocks) {
+    const long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t *src = aos + b * 34;
+    d[b] = static_cast<uint16_t>(src[0] | (src[1] << 8));
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = src[2 + 4 * i] | (src[3 + 4 * i] << 8) | (src[4 + 4 * i] << 16) | (uint32_t(src[5 + 4 * i]) << 24);
+    uint4 *dst = reinterpret_cast<uint4 *>(q + b * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status dspark_q8_0_repack(const void *w_q8_0, int8_t *q, uint16_t *d, int N, int K,
+                                            dspark_stream_t stream) {
+    using namespace dspark;
+    clear_error();
+    if (N < 0 || K <= 0 || (K % 32) != 0) return fail(DSPARK_ERR_INVALID, "q8_0_repack: bad sizes N=%d K=%d", N, K);
+    if (N == 0) return DSPARK_OK;
+    if (!w_q8_0 || !q || !d) return fail(DSPARK_ERR_INVALID, "q8_0_repack: null pointer argument");
+    if (!aligned(q, 16) || !aligned(d, 2)) return fail(DSPARK_ERR_INVALID, "q8_0_repack: misaligned output");
+    const long long nblocks = static_cast<long long>(N) * (K / 32);
+    const int threads = 256;
+    const long long grid = (nblocks + threads - 1) / threads;
+    q8_0_repack_kernel<<<static_cast<unsigned>(grid), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w_q8_0), q, d, nblocks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q8_0_repack launch");
+    return DSPARK_OK;
+}
+
+extern "C" size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K) {
+    (void)M;
+    int sms = 0;
+    if (N <= 0 || K < 256) return dspark::kTicketBytes;
+    if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
+    return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
+}
+
+extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
+                                             int y_is_fp32, int M, int N, int K, void *workspace,
+                                             size_t workspace_bytes, dspark_stream_t stream) {
+    using namespace dspark;
+    clear_error();
+    if (M < 0 || N < 0 || K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: negative size");
+    if (M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: M=%d > 16", M);
+    if (K == 0 || (K % 256) != 0) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: K=%d is not a multiple of 256", K);
+    if (M == 0 || N == 0) return DSPARK_OK;  // nothing to enqueue
+    if (!Wq || !Wd || !X || !Y || !workspace) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: null pointer argument");
+    if (!aligned(Wq, 16) || !aligned(Wd, 16) || !aligned(X, 16))
+        return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: Wq, Wd and X must be 16-byte aligned");
+    if (!aligned(Y, y_is_fp32 ? 4 : 2)) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: misaligned Y");
+    if (!aligned(workspace, 256)) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace must be 256-byte aligned");
+    int sms = 0;
+    int rc = current_sm_count(&sms);
+    if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
+    const Plan p = plan_for(N, K, sms);
+    if (size_t(p.nrb) * sizeof(unsigned) > kTicketBytes)
+        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: N=%d exceeds %zu rows", N, kTicketBytes / 4 * kRows);
+    const size_t need = workspace_bytes_for(p);
+    if (workspace_bytes < need)
+        return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
+
+    CUtensorMap tmQ, tmX;
+    dspark_status st = make_tmap_2d_u8_sw128(&tmQ, Wq, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRows, kKS);
+    if (st != DSPARK_OK) return st;
+    st = make_tmap_f16_kblocks(&tmX, X, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, 2);
+    if (st != DSPARK_OK) return st;
+
+    Q8Args args;
+    args.d = Wd;
+    args.Y = Y;
+    args.y_fp32 = y_is_fp32 ? 1 : 0;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.nsb = p.nsb;
+    args.S = p.S;
+    args.timeout_ns = kDefaultTimeoutNs;
+    args.partial = nullptr;
+    args.tickets = nullptr;
+    if (p.S > 1) {
+        unsigned char *ws = static_cast<unsigned char *>(workspace);
+        args.tickets = reinterpret_cast<unsigned *>(ws);
+        args.partial = reinterpret_cast<float *>(ws + kTicketBytes);
+    }
+
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(ws_q8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec_q8)");
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_q8_tc_kernel, kThreads, kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec_q8)");
+        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
+        configured_dev = dev;
+    }
+    const unsigned units = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
+    ws_q8_tc_kernel<<<units, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmQ, tmX, args);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
+    return DSPARK_OK;
+}

@@ -5,6 +5,7 @@
  *   dspark_markov_draft  the sequential Markov block-draft sampler
  *   dspark_conf_probe    the proposer's Q8_0 confidence probe and its gate
  *   dspark_ws_matvec     the weight-stationary small-M fp16 projection matvec
+ *   dspark_ws_matvec_q8  the same matvec over Q8_0 weights (after dspark_q8_0_repack)
  *
  * Conventions shared by every entry point
  *   - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations), owned
@@ -218,6 +219,43 @@ size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K);
 dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32,
                                int M, int N, int K, void *workspace, size_t workspace_bytes,
                                dspark_stream_t stream);
+
+/* =====================================================================================
+ * Weight-stationary small-M matvec with Q8_0 weights
+ *
+ * Source: SharpInference issue #441, "Proposed work": the weight-stationary kernels it
+ * reuses read quantized weights, and a structure-of-arrays repack of the quantized blocks
+ * may be needed.  Q8_0 (ggml): per 32 consecutive weights of a row, one fp16 scale d and 32
+ * int8 values q; the weight is d * q.
+ *
+ *   Y[m, n] = sum_b d[n, b] * sum_{j<32} q[n, 32b + j] * X[m, 32b + j]   (fp32 accumulation)
+ *
+ * dspark_q8_0_repack turns the ggml array of 34-byte blocks (row-major by weight row: the
+ * K/32 blocks of row 0, then row 1, ...) into the two arrays dspark_ws_matvec_q8 reads:
+ *   q  int8 [N, K]      the quantized values, 16-byte aligned
+ *   d  fp16 [N, K/32]   the block scales (bit patterns), 16-byte aligned for the matvec
+ * Supported: K % 32 == 0 (N == 0 enqueues nothing).
+ *
+ * dspark_ws_matvec_q8 runs on the tcgen05 tensor cores: q (exact in fp16) times X gives, per
+ * Q8_0 block, an fp32 partial sum that the kernel then scales by d in fp32, so the dequantized
+ * weight d * q is never rounded to a 16-bit type.
+ *   X          fp16 [M, K], 16-byte aligned
+ *   Y          [M, N]: fp32 if y_is_fp32, else fp16 rounded to nearest even
+ *   workspace  device scratch of at least dspark_ws_matvec_q8_workspace_bytes(M, N, K) bytes,
+ *              256-byte aligned and ZERO-FILLED before its first use; every call leaves it
+ *              zero-filled again.  Calls sharing a workspace must not overlap on the device.
+ *   Supported: 1 <= M <= 16, N >= 1, K a positive multiple of 256 (M == 0 or N == 0 enqueues
+ *   nothing).  Every output is summed in one fixed order, so row m's result does not depend
+ *   on M.
+ * ===================================================================================== */
+dspark_status dspark_q8_0_repack(const void *w_q8_0, int8_t *q, uint16_t *d, int N, int K,
+                                 dspark_stream_t stream);
+
+size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K);
+
+dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
+                                  int y_is_fp32, int M, int N, int K, void *workspace,
+                                  size_t workspace_bytes, dspark_stream_t stream);
 
 /* =====================================================================================
  * Draft step with device-side base logits

@@ -158,3 +158,21 @@ def check_ws(inp, y32=None, y16=None):
         rep["fp16_exact_rne"] = int((y16 == Y16).sum())
         rep["fp16_total"] = int(y16.size)
     return rep
+
+
+def check_ws_q8(inp, y32=None, y16=None):
+    """Quantized matvec outputs against the fp64 oracle (same tolerance as the fp16 matvec)."""
+    Y = oracle.ws_matvec_q8(inp["Wq8"], inp["X"])
+    rep = {}
+    if y32 is not None:
+        ok, err, nbad = within_tol(y32, Y)
+        assert ok, f"{nbad} fp32 outputs outside tolerance (max err {err:.3e})"
+        rep["max_err_fp32"] = err
+    if y16 is not None:
+        yf = y16.view(np.float16).astype(np.float64)
+        ok, err, nbad = within_tol(yf, Y)
+        assert ok, f"{nbad} fp16 outputs outside tolerance (max err {err:.3e})"
+        if y32 is not None:
+            np.testing.assert_array_equal(y16, y32.astype(np.float32).astype(np.float16)
+                                          .view(np.uint16))
+    return rep

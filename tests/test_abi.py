@@ -162,3 +162,47 @@ def test_python_binding_rejects_cpu_tensors(dspark_lib):
 
     with pytest.raises(ValueError):
         api.ws_matvec(torch.zeros(4, 8, dtype=torch.float16), torch.zeros(1, 8, dtype=torch.float16))
+
+
+def test_ws_q8_validation(dspark_lib):
+    lib = dspark_lib
+    f = lib.dspark_ws_matvec_q8
+    B = 1 << 20
+
+    def g(q=FAKE, d=FAKE, x=FAKE, y=FAKE, yf=0, M=7, N=64, K=256, ws=FAKE, wsb=B):
+        return f(q, d, x, y, yf, M, N, K, ws, wsb, NULL)
+
+    assert g(M=17) == UNSUPPORTED
+    assert g(K=288) == UNSUPPORTED   # K % 256 != 0
+    assert g(K=0) == UNSUPPORTED
+    assert g(M=-1) == INVALID
+    assert g(N=-1) == INVALID
+    assert g(q=NULL) == INVALID
+    assert g(d=NULL) == INVALID
+    assert g(y=NULL) == INVALID
+    assert g(ws=NULL) == INVALID
+    assert g(q=FAKE_ODD) == INVALID
+    assert g(d=FAKE_ODD) == INVALID
+    assert g(x=FAKE_ODD) == INVALID
+    assert g(y=ctypes.c_void_p(0x10002), yf=1) == INVALID
+    assert g(ws=FAKE_ODD) == INVALID
+    assert g(M=0) == 0
+    assert g(N=0) == 0
+    assert lib.dspark_ws_matvec_q8_workspace_bytes(7, 0, 256) == 65536
+    r = lib.dspark_q8_0_repack
+    assert r(FAKE, FAKE, FAKE, 4, 48, NULL) == INVALID
+    assert r(FAKE, FAKE, FAKE, -1, 64, NULL) == INVALID
+    assert r(NULL, FAKE, FAKE, 4, 64, NULL) == INVALID
+    assert r(FAKE, FAKE_ODD, FAKE, 4, 64, NULL) == INVALID
+    assert r(FAKE, FAKE, ctypes.c_void_p(0x10001), 4, 64, NULL) == INVALID
+    assert r(NULL, NULL, NULL, 0, 64, NULL) == 0
+
+
+def test_python_q8_binding_rejects_cpu_tensors(dspark_lib):
+    import torch
+
+    with pytest.raises(ValueError):
+        api.ws_matvec_q8(torch.zeros(4, 256, dtype=torch.int8), torch.zeros(4, 8, dtype=torch.int16),
+                         torch.zeros(1, 256, dtype=torch.float16), workspace=torch.zeros(16))
+    with pytest.raises(ValueError):
+        api.q8_0_repack(torch.zeros(4 * 2 * 34, dtype=torch.uint8), 4, 64)

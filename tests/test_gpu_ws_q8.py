@@ -1,0 +1,122 @@
+"""GPU quantized (Q8_0) weight-stationary matvec and its repack vs the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from dspark_draft_sampling_gb300 import api, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(dspark_lib):
+    return dspark_lib
+
+
+def _dev(inp):
+    raw = torch.from_numpy(inp["Wq8"]).cuda()
+    q, d = api.q8_0_repack(raw, inp["N"], inp["K"])
+    X = torch.from_numpy(inp["X"].view(np.int16)).cuda().view(torch.float16)
+    return q, d, X
+
+
+def _run(inp):
+    q, d, X = _dev(inp)
+    y32 = api.ws_matvec_q8(q, d, X, out_fp32=True)
+    y16 = api.ws_matvec_q8(q, d, X)
+    torch.cuda.synchronize()
+    return y32.cpu().numpy(), y16.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_repack_is_a_byte_exact_split():
+    N, K = 37, 1024
+    inp = synth.ws_q8_inputs(3, N, K, seed=1)
+    q, d, _ = _dev(inp)
+    blk = inp["Wq8"].reshape(N, K // 32, 34)
+    np.testing.assert_array_equal(q.cpu().numpy(), blk[:, :, 2:].view(np.int8).reshape(N, K))
+    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint16),
+                                  blk[:, :, :2].copy().view("<u2").reshape(N, K // 32))
+
+
+@pytest.mark.parametrize("K,N", synth.WS_SHAPES)
+def test_qwen3_8b_projection_shapes(K, N):
+    inp = synth.ws_q8_inputs(7, N, K, seed=K + N)
+    y32, y16 = _run(inp)
+    parity.check_ws_q8(inp, y32=y32, y16=y16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (2, 100, 512), (3, 1000, 2304), (5, 153, 4352),
+                                   (8, 4096, 256), (9, 300, 1024), (16, 777, 4096), (7, 1, 12288),
+                                   (4, 5000, 256), (6, 151, 6400)])
+def test_ragged_shapes(M, N, K):
+    inp = synth.ws_q8_inputs(M, N, K, seed=M * 7 + N)
+    y32, y16 = _run(inp)
+    parity.check_ws_q8(inp, y32=y32, y16=y16)
+
+
+def test_extreme_scales_and_codes():
+    """Largest fp16 scales next to subnormal ones, codes at +-127 and 0: the dequantized
+    weights must come out exactly (no overflow, no flush of subnormal scales)."""
+    M, N, K = 3, 64, 512
+    inp = synth.ws_q8_inputs(M, N, K, seed=9)
+    blk = inp["Wq8"].reshape(N, K // 32, 34)
+    d = np.abs(np.random.default_rng(9).standard_normal((N, K // 32))).astype(np.float32)
+    d[0::4] = 60000.0
+    d[1::4] = np.float32(2.0 ** -24) * 3.0
+    d[2::4] = 1.0
+    blk[:, :, 0:2] = synth.f32_to_f16_bits(d).astype("<u2").view(np.uint8).reshape(N, K // 32, 2)
+    blk[:, 0, 2:] = np.uint8(127)
+    blk[:, 1, 2:] = np.int8(-127).view(np.uint8)
+    blk[:, 2, 2:] = 0
+    inp["Wq8"] = blk.reshape(-1).copy()
+    x = np.zeros((M, K), np.float32)
+    x[:, 0:96] = np.random.default_rng(10).standard_normal((M, 96)).astype(np.float32) * 1e-3
+    inp["X"] = synth.f32_to_f16_bits(x)
+    y32, _ = _run(inp)
+    parity.check_ws_q8(inp, y32=y32)
+
+
+def test_rows_independent_of_m_bitwise():
+    inp = synth.ws_q8_inputs(16, 1000, 4096, seed=3)
+    q, d, X = _dev(inp)
+    full = api.ws_matvec_q8(q, d, X, out_fp32=True)
+    for M in (1, 2, 3, 7, 8, 9):
+        part = api.ws_matvec_q8(q, d, X[:M].contiguous(), out_fp32=True)
+        torch.cuda.synchronize()
+        assert torch.equal(part.view(torch.int32), full[:M].view(torch.int32)), M
+
+
+def test_repeat_is_bit_identical():
+    inp = synth.ws_q8_inputs(7, 4096, 4096, seed=4)
+    q, d, X = _dev(inp)
+    a = api.ws_matvec_q8(q, d, X, out_fp32=True)
+    b = api.ws_matvec_q8(q, d, X, out_fp32=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_close_to_dequantized_torch_reference():
+    """Plain PyTorch fp32 reference of the same op: dequantize, then matmul."""
+    inp = synth.ws_q8_inputs(7, 2048, 4096, seed=5)
+    q, d, X = _dev(inp)
+    y = api.ws_matvec_q8(q, d, X, out_fp32=True)
+    W = (q.float().view(2048, 128, 32) * d.view(torch.float16).float()[:, :, None]).view(2048, 4096)
+    ref = X.float() @ W.t()
+    torch.cuda.synchronize()
+    assert torch.allclose(y, ref, atol=2e-3, rtol=1e-3)
+
+
+def test_shared_workspace_across_shapes_and_repeats():
+    """One zero-filled workspace serves every shape in turn: each call leaves it zero-filled."""
+    shapes = [(7, 4096, 4096), (7, 1024, 4096), (3, 300, 12288), (7, 4096, 4096)]
+    nbytes = max(api.ws_matvec_q8_workspace_bytes(M, N, K) for M, N, K in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for i, (M, N, K) in enumerate(shapes):
+        inp = synth.ws_q8_inputs(M, N, K, seed=20 + i)
+        q, d, X = _dev(inp)
+        for _ in range(2):
+            y = api.ws_matvec_q8(q, d, X, out_fp32=True, workspace=ws)
+            torch.cuda.synchronize()
+            parity.check_ws_q8(inp, y32=y.cpu().numpy())
+    assert int(ws[:65536].count_nonzero()) == 0
