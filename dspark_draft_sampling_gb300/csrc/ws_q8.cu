@@ -18,9 +18,10 @@
 // order.  Every output is summed in one fixed order (blocks, then split-K units in order), so
 // results are deterministic and row m's does not depend on M.
 //
-// GB300 design (one CTA per SM, 15 warps)
+// GB300 design (persistent: one CTA per SM, 15 warps)
 //  * Work unit = (128 weight rows, a range of 256-k superblocks); K is split so that there is
-//    about one unit per SM.
+//    about one unit per SM.  Each CTA takes every gridDim.x-th unit and streams the stages of
+//    its units back to back, so one unit's epilogue overlaps the next unit's loads.
 //  * Warp 12 (one thread) streams, per 128-k stage, the int8 tile [128 rows x 128 k] (16 KB,
 //    128-byte swizzle) and the X tile [16 rows x 128 k] (two 2 KB fp16 atoms in one 3-D copy;
 //    rows >= M read as zero) with TMA tensor copies through a 10-stage ring (200 KB).
@@ -80,10 +81,28 @@ struct Q8Args {
     unsigned *tickets;  // [row blocks]
     int y_fp32;
     int M, N, K;
-    int nsb;  // 256-k superblocks
-    int S;    // units per row block
+    int nsb;    // 256-k superblocks
+    int S;      // units per row block
+    int units;  // row blocks x S; CTA c takes units c, c + gridDim.x, ...
     unsigned long long timeout_ns;
 };
+
+struct Unit {
+    int rb, sb0, nsup, nst, ks0, n0;
+};
+
+__device__ __forceinline__ Unit unit_geometry(const Q8Args &a, int u) {
+    Unit g;
+    g.rb = u / a.S;
+    const int sk = u % a.S;
+    g.sb0 = static_cast<int>(static_cast<long long>(sk) * a.nsb / a.S);
+    const int sb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nsb / a.S);
+    g.nsup = sb1 - g.sb0;
+    g.nst = g.nsup * kSuper;   // 128-k stages
+    g.ks0 = g.sb0 * kSuper;    // first 128-k stage index along K
+    g.n0 = g.rb * kRows;
+    return g;
+}
 
 // Two int8 values (bytes of u selected by `sel`, already biased to q + 128) -> fp16x2 holding
 // q exactly: the byte permute builds the fp16 patterns 0x64XX = 1024 + XX.
@@ -96,12 +115,15 @@ __device__ __forceinline__ uint32_t q8_pair_to_f16x2(uint32_t u, uint32_t sel) {
 
 __device__ __forceinline__ uint4 ldg_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// Stage J is the CTA's J-th 128-k stage over all its units, in order.  Ring positions:
+// shared-memory slot J % kStages, TMEM A slot and accumulator group J % kASlots, and the
+// phase of each ring's barrier is (J / ring size) & 1.
 __global__ void __launch_bounds__(kThreads, 1)
     ws_q8_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, Q8Args a) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     unsigned char *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);  // 1024-aligned slots
-    // Barriers.  done[j % kStages] completes once per stage j when the stage's MMAs have
+    // Barriers.  done[J % kStages] completes once per stage J when the stage's MMAs have
     // finished (one tcgen05.commit): its shared-memory slot may be refilled, its TMEM A slot
     // reused and its accumulators read.
     uint64_t *full_r = reinterpret_cast<uint64_t *>(ring + size_t(kStages) * kSlotBytes);  // TMA landed
@@ -114,15 +136,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int unit = blockIdx.x;
-    const int rb = unit / a.S;
-    const int sk = unit % a.S;
-    const int sb0 = static_cast<int>(static_cast<long long>(sk) * a.nsb / a.S);
-    const int sb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nsb / a.S);
-    const int nsup = sb1 - sb0;
-    const int nst = nsup * kSuper;  // 128-k stages of this unit
-    const int ks0 = sb0 * kSuper;   // its first 128-k stage index along K
-    const int n0 = rb * kRows;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -146,23 +159,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
-            int issued = 0, st = 0;
-            uint32_t ph = 0;
-            for (int j = 0; j < nst; ++j) {
-                if (!mbar_wait(&done[st], ph ^ 1u, a.timeout_ns)) break;  // stage j - kStages finished
-                unsigned char *slot = ring + size_t(st) * kSlotBytes;
-                const int k0 = (ks0 + j) * kKS;
-                mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
-                tma_load_2d(slot, &tmQ, k0, n0, &full_r[st], pol_q);
-                tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
-                ++issued;
-                if (++st == kStages) {
-                    st = 0;
-                    ph ^= 1u;
+            int J = 0;
+            bool stop = false;
+            for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
+                const Unit ug = unit_geometry(a, u);
+                for (int j = 0; j < ug.nst; ++j, ++J) {
+                    const int st = J % kStages;
+                    // slot st was last used by stage J - kStages
+                    if (!mbar_wait(&done[st], static_cast<uint32_t>(((J / kStages) & 1) ^ 1), a.timeout_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    unsigned char *slot = ring + size_t(st) * kSlotBytes;
+                    const int k0 = (ug.ks0 + j) * kKS;
+                    mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
+                    tma_load_2d(slot, &tmQ, k0, ug.n0, &full_r[st], pol_q);
+                    tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
                 }
             }
             // copies still in flight (possible only after a consumer gave up) land before exit
-            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+            for (int i = J > kStages ? J - kStages : 0; i < J; ++i)
                 mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.timeout_ns);
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
@@ -171,30 +187,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int par = warp - kMmaWarp;
             constexpr uint32_t idesc = idesc_f16(false, kRows, kNPad);
             const uint64_t dX0 = smem_desc_sw128(smem_addr(ring + kQBytes));
-            // ring positions of stage j = par, par + 2, ...: slots advance by 2 and wrap
-            int st = par, g = par;  // stage j: shared-memory slot j % kStages, A slot = group = j % 4
-            uint32_t phg = 0;
-            for (int j = par; j < nst; j += 2) {
-                // the converters arrive on full_a only after the stage's TMA copies (X included)
-                // have landed, so this one wait orders both operands before the MMAs
-                if (!mbar_wait(&full_a[g], phg, a.timeout_ns)) break;
-                if (!mbar_wait(&empty_t[g], phg ^ 1u, a.timeout_ns)) break;
-                tc_fence_after();
-                const uint64_t dB = dX0 + static_cast<uint64_t>(st * (kSlotBytes >> 4));
-                const uint32_t ta = tmem + kAColBase + static_cast<uint32_t>(g) * kACols;
-                const uint32_t td = tmem + static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+            int J = 0;
+            bool stop = false;
+            for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
+                const int nst = unit_geometry(a, u).nst;
+                for (int j = 0; j < nst; ++j, ++J) {
+                    if ((J & 1) != par) continue;
+                    const int st = J % kStages, g = J % kASlots;
+                    const uint32_t ph = static_cast<uint32_t>((J / kASlots) & 1);
+                    // the converters arrive on full_a only after the stage's TMA copies (X included)
+                    // have landed, so this one wait orders both operands before the MMAs
+                    if (!mbar_wait(&full_a[g], ph, a.timeout_ns) || !mbar_wait(&empty_t[g], ph ^ 1u, a.timeout_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t dB = dX0 + static_cast<uint64_t>(st * (kSlotBytes >> 4));
+                    const uint32_t ta = tmem + kAColBase + static_cast<uint32_t>(g) * kACols;
+                    const uint32_t td = tmem + static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
 #pragma unroll
-                for (int b = 0; b < kBlocksPerStage; ++b) {
-                    // block b = k 32b .. 32b + 31: A columns 16b (+8); X atom b/2, byte offset 64 (b%2) (+32)
-                    const uint64_t db = dB + static_cast<uint64_t>((b >> 1) * (kXAtomBytes >> 4) + (b & 1) * 4);
-                    tc_mma_f16_ts(td + b * kNPad, ta + 16 * b, db, idesc, 0u);
-                    tc_mma_f16_ts(td + b * kNPad, ta + 16 * b + 8, db + 2, idesc, 1u);
-                }
-                tc_commit(&done[st]);
-                if ((st += 2) >= kStages) st -= kStages;
-                if ((g += 2) >= kTGroups) {
-                    g -= kTGroups;
-                    phg ^= 1u;
+                    for (int b = 0; b < kBlocksPerStage; ++b) {
+                        // block b = k 32b .. 32b + 31: A columns 16b (+8); X atom b/2, byte offset 64 (b%2) (+32)
+                        const uint64_t db = dB + static_cast<uint64_t>((b >> 1) * (kXAtomBytes >> 4) + (b & 1) * 4);
+                        tc_mma_f16_ts(td + b * kNPad, ta + 16 * b, db, idesc, 0u);
+                        tc_mma_f16_ts(td + b * kNPad, ta + 16 * b + 8, db + 2, idesc, 1u);
+                    }
+                    tc_commit(&done[st]);
                 }
             }
             tc_commit(&mma_done[par]);  // arrives once every MMA this thread issued has completed
@@ -206,185 +224,185 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lg = warp & 3;          // TMEM lane quarter this warp may access
         const int r = lg * 32 + lane;     // weight row within the tile
         const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
-        int st = par, as = par;
-        uint32_t phr = 0;
         bool broken = false;
-        for (int j = par; j < nst; j += 2) {
-            if (!broken && !mbar_wait(&full_r[st], phr, a.timeout_ns)) broken = true;
-            if (j >= kASlots) {  // A slot j % 4 was last read by stage j - 4
-                const int jp = j - kASlots;
-                if (!broken && !mbar_wait(&done[jp % kStages], static_cast<uint32_t>((jp / kStages) & 1), a.timeout_ns))
+        int J = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+            const int nst = unit_geometry(a, u).nst;
+            for (int j = 0; j < nst; ++j, ++J) {
+                if ((J & 1) != par) continue;
+                const int st = J % kStages, as = J % kASlots;
+                if (!broken && !mbar_wait(&full_r[st], static_cast<uint32_t>((J / kStages) & 1), a.timeout_ns))
                     broken = true;
-            }
-            broken = __any_sync(0xffffffffu, broken);
-            if (!broken) {
-                const unsigned char *rowp = ring + size_t(st) * kSlotBytes + r * kKS;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {  // two halves of 64 k: 32 TMEM columns each
-                    uint32_t v[32];
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = 4 * h + cc;  // 16-byte chunk c = k 16c .. 16c + 15, stored at c ^ (r & 7)
-                        uint4 w = *reinterpret_cast<const uint4 *>(rowp + ((c ^ (r & 7)) << 4));
-                        w.x ^= 0x80808080u;
-                        w.y ^= 0x80808080u;
-                        w.z ^= 0x80808080u;
-                        w.w ^= 0x80808080u;
-                        v[8 * cc + 0] = q8_pair_to_f16x2(w.x, 0x4140);
-                        v[8 * cc + 1] = q8_pair_to_f16x2(w.x, 0x4342);
-                        v[8 * cc + 2] = q8_pair_to_f16x2(w.y, 0x4140);
-                        v[8 * cc + 3] = q8_pair_to_f16x2(w.y, 0x4342);
-                        v[8 * cc + 4] = q8_pair_to_f16x2(w.z, 0x4140);
-                        v[8 * cc + 5] = q8_pair_to_f16x2(w.z, 0x4342);
-                        v[8 * cc + 6] = q8_pair_to_f16x2(w.w, 0x4140);
-                        v[8 * cc + 7] = q8_pair_to_f16x2(w.w, 0x4342);
-                    }
-                    tmem_st_32(tmem + tlane + kAColBase + static_cast<uint32_t>(as) * kACols + 32u * h, v);
+                if (J >= kASlots) {  // A slot J % kASlots was last read by stage J - kASlots
+                    const int jp = J - kASlots;
+                    if (!broken &&
+                        !mbar_wait(&done[jp % kStages], static_cast<uint32_t>((jp / kStages) & 1), a.timeout_ns))
+                        broken = true;
                 }
-                tmem_wait_st();
-                tc_fence_before();
+                broken = __any_sync(0xffffffffu, broken);
+                if (!broken) {
+                    const unsigned char *rowp = ring + size_t(st) * kSlotBytes + r * kKS;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {  // two halves of 64 k: 32 TMEM columns each
+                        uint32_t v[32];
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int c = 4 * h + cc;  // 16-byte chunk c = k 16c .. 16c + 15, stored at c ^ (r & 7)
+                            uint4 w = *reinterpret_cast<const uint4 *>(rowp + ((c ^ (r & 7)) << 4));
+                            w.x ^= 0x80808080u;
+                            w.y ^= 0x80808080u;
+                            w.z ^= 0x80808080u;
+                            w.w ^= 0x80808080u;
+                            v[8 * cc + 0] = q8_pair_to_f16x2(w.x, 0x4140);
+                            v[8 * cc + 1] = q8_pair_to_f16x2(w.x, 0x4342);
+                            v[8 * cc + 2] = q8_pair_to_f16x2(w.y, 0x4140);
+                            v[8 * cc + 3] = q8_pair_to_f16x2(w.y, 0x4342);
+                            v[8 * cc + 4] = q8_pair_to_f16x2(w.z, 0x4140);
+                            v[8 * cc + 5] = q8_pair_to_f16x2(w.z, 0x4342);
+                            v[8 * cc + 6] = q8_pair_to_f16x2(w.w, 0x4140);
+                            v[8 * cc + 7] = q8_pair_to_f16x2(w.w, 0x4342);
+                        }
+                        tmem_st_32(tmem + tlane + kAColBase + static_cast<uint32_t>(as) * kACols + 32u * h, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0 && !broken) mbar_arrive(&full_a[as]);
             }
-            __syncwarp();
-            if (lane == 0 && !broken) mbar_arrive(&full_a[as]);
-            if ((st += 2) >= kStages) {
-                st -= kStages;
-                phr ^= 1u;
-            }
-            if ((as += 2) >= kASlots) as -= kASlots;
         }
     } else {
-        // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 ----
+        // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 of each unit ----
         const int lrow = warp * 32 + lane;
-        const int row = n0 + lrow;
-        const bool rowok = row < a.N;
-        const uint16_t *drow = a.d + size_t(rowok ? row : 0) * (a.K / 32) + size_t(sb0) * 8;
-        // the row's scales, 8 per superblock, prefetched kDAhead superblocks ahead: a load issued
-        // while the weight stream saturates HBM takes microseconds to return
-        constexpr int kDAhead = 4;
-        uint4 dq[kDAhead];
-#pragma unroll
-        for (int i = 0; i < kDAhead; ++i)
-            dq[i] = (rowok && i < nsup) ? ldg_u4(drow + size_t(i) * 8) : make_uint4(0u, 0u, 0u, 0u);
-        float acc[kNPad];
-#pragma unroll
-        for (int m = 0; m < kNPad; ++m) acc[m] = 0.f;
-        int g = 0, st = 0;  // stage j: accumulator group j % 4, done[j % kStages]
-        uint32_t phd = 0;
         bool ok = true;
-        for (int s = 0; s < nsup; ++s) {
-            const uint32_t dw[4] = {dq[0].x, dq[0].y, dq[0].z, dq[0].w};
+        int J = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+            const Unit ug = unit_geometry(a, u);
+            const int row = ug.n0 + lrow;
+            const bool rowok = row < a.N;
+            const uint16_t *drow = a.d + size_t(rowok ? row : 0) * (a.K / 32) + size_t(ug.sb0) * 8;
+            // the row's scales, 8 per superblock, prefetched kDAhead superblocks ahead: a load
+            // issued while the weight stream saturates HBM takes microseconds to return
+            constexpr int kDAhead = 4;
+            uint4 dq[kDAhead];
 #pragma unroll
-            for (int i = 0; i + 1 < kDAhead; ++i) dq[i] = dq[i + 1];
-            dq[kDAhead - 1] = (rowok && s + kDAhead < nsup) ? ldg_u4(drow + size_t(s + kDAhead) * 8)
-                                                            : make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < kDAhead; ++i)
+                dq[i] = (rowok && i < ug.nsup) ? ldg_u4(drow + size_t(i) * 8) : make_uint4(0u, 0u, 0u, 0u);
+            float acc[kNPad];
 #pragma unroll
-            for (int h = 0; h < kSuper; ++h) {  // one stage = one group of 4 accumulator slots
-                if (ok) ok = mbar_wait(&done[st], phd, a.timeout_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                tc_fence_after();
-                uint32_t v[kBlocksPerStage][16];
-                if (ok) {
-                    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
-                                        static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+            for (int m = 0; m < kNPad; ++m) acc[m] = 0.f;
+            for (int s = 0; s < ug.nsup; ++s) {
+                const uint32_t dw[4] = {dq[0].x, dq[0].y, dq[0].z, dq[0].w};
 #pragma unroll
-                    for (int u = 0; u < kBlocksPerStage; ++u) tmem_ld_16_async(ta + u * kNPad, v[u]);
-                    tmem_wait_ld();
-                } else {
+                for (int i = 0; i + 1 < kDAhead; ++i) dq[i] = dq[i + 1];
+                dq[kDAhead - 1] = (rowok && s + kDAhead < ug.nsup) ? ldg_u4(drow + size_t(s + kDAhead) * 8)
+                                                                   : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int u = 0; u < kBlocksPerStage; ++u)
+                for (int h = 0; h < kSuper; ++h, ++J) {  // one stage = one group of 4 accumulator slots
+                    const int st = J % kStages, g = J % kTGroups;
+                    if (ok) ok = mbar_wait(&done[st], static_cast<uint32_t>((J / kStages) & 1), a.timeout_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                    uint32_t v[kBlocksPerStage][16];
+                    if (ok) {
+                        const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
+                                            static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
 #pragma unroll
-                        for (int m = 0; m < kNPad; ++m) v[u][m] = 0u;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
+                        for (int q = 0; q < kBlocksPerStage; ++q) tmem_ld_16_async(ta + q * kNPad, v[q]);
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                for (int u = 0; u < kBlocksPerStage; ++u) {
-                    const int b = h * kBlocksPerStage + u;  // Q8_0 block within the superblock
-                    const float dsc = __half2float(__ushort_as_half(
-                        static_cast<unsigned short>((b & 1) ? (dw[b >> 1] >> 16) : (dw[b >> 1] & 0xffffu))));
+                        for (int q = 0; q < kBlocksPerStage; ++q)
 #pragma unroll
-                    for (int m = 0; m < kNPad; ++m) acc[m] = fmaf(dsc, __uint_as_float(v[u][m]), acc[m]);
-                }
-                if (++g == kTGroups) g = 0;
-                if (++st == kStages) {
-                    st = 0;
-                    phd ^= 1u;
-                }
-            }
-        }
-        const int M = a.M;
-        if (a.S == 1) {
-            if (ok && rowok) {
+                            for (int m = 0; m < kNPad; ++m) v[q][m] = 0u;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
 #pragma unroll
-                for (int m = 0; m < kNPad; ++m) {
-                    if (m < M) {
-                        const size_t o = size_t(m) * a.N + row;
-                        if (a.y_fp32)
-                            static_cast<float *>(a.Y)[o] = acc[m];
-                        else
-                            static_cast<__half *>(a.Y)[o] = __float2half_rn(acc[m]);
+                    for (int q = 0; q < kBlocksPerStage; ++q) {
+                        const int b = h * kBlocksPerStage + q;  // Q8_0 block within the superblock
+                        const float dsc = __half2float(__ushort_as_half(
+                            static_cast<unsigned short>((b & 1) ? (dw[b >> 1] >> 16) : (dw[b >> 1] & 0xffffu))));
+#pragma unroll
+                        for (int m = 0; m < kNPad; ++m) acc[m] = fmaf(dsc, __uint_as_float(v[q][m]), acc[m]);
                     }
                 }
             }
-        } else {
-            float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(unit) * kRows + lrow) * kNPad);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) p[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0) *s_last = (atomicAdd(&a.tickets[rb], 1u) == static_cast<unsigned>(a.S - 1));
-            named_bar_sync(1, 128);
-            if (*s_last) {
-                __threadfence();
+            const int M = a.M;
+            if (a.S == 1) {
                 if (ok && rowok) {
-                    // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads issued four
-                    // units at a time so their latencies overlap, the sum order is fixed
-                    const float4 *base =
-                        reinterpret_cast<const float4 *>(a.partial + (size_t(rb) * a.S * kRows + lrow) * kNPad);
-                    constexpr size_t kUnitF4 = size_t(kRows) * kNPad / 4;
-                    float y[kNPad];
-#pragma unroll
-                    for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
-                    int s = 0;
-                    for (; s + 4 <= a.S; s += 4) {
-                        float4 tq[4][4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) tq[u][q] = __ldcg(base + size_t(s + u) * kUnitF4 + q);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                y[4 * q] += tq[u][q].x;
-                                y[4 * q + 1] += tq[u][q].y;
-                                y[4 * q + 2] += tq[u][q].z;
-                                y[4 * q + 3] += tq[u][q].w;
-                            }
-                    }
-                    for (; s < a.S; ++s) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 tq = __ldcg(base + size_t(s) * kUnitF4 + q);
-                            y[4 * q] += tq.x;
-                            y[4 * q + 1] += tq.y;
-                            y[4 * q + 2] += tq.z;
-                            y[4 * q + 3] += tq.w;
-                        }
-                    }
 #pragma unroll
                     for (int m = 0; m < kNPad; ++m) {
                         if (m < M) {
                             const size_t o = size_t(m) * a.N + row;
                             if (a.y_fp32)
-                                static_cast<float *>(a.Y)[o] = y[m];
+                                static_cast<float *>(a.Y)[o] = acc[m];
                             else
-                                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+                                static_cast<__half *>(a.Y)[o] = __float2half_rn(acc[m]);
                         }
                     }
                 }
-                if (threadIdx.x == 0) a.tickets[rb] = 0u;  // zero again for the next call
+            } else {
+                float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(u) * kRows + lrow) * kNPad);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    p[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 0) *s_last = (atomicAdd(&a.tickets[ug.rb], 1u) == static_cast<unsigned>(a.S - 1));
+                named_bar_sync(1, 128);
+                if (*s_last) {
+                    __threadfence();
+                    if (ok && rowok) {
+                        // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads issued
+                        // four units at a time so their latencies overlap, the sum order is fixed
+                        const float4 *base =
+                            reinterpret_cast<const float4 *>(a.partial + (size_t(ug.rb) * a.S * kRows + lrow) * kNPad);
+                        constexpr size_t kUnitF4 = size_t(kRows) * kNPad / 4;
+                        float y[kNPad];
+#pragma unroll
+                        for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
+                        int s = 0;
+                        for (; s + 4 <= a.S; s += 4) {
+                            float4 tq[4][4];
+#pragma unroll
+                            for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) tq[q2][q] = __ldcg(base + size_t(s + q2) * kUnitF4 + q);
+#pragma unroll
+                            for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    y[4 * q] += tq[q2][q].x;
+                                    y[4 * q + 1] += tq[q2][q].y;
+                                    y[4 * q + 2] += tq[q2][q].z;
+                                    y[4 * q + 3] += tq[q2][q].w;
+                                }
+                        }
+                        for (; s < a.S; ++s) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float4 tq = __ldcg(base + size_t(s) * kUnitF4 + q);
+                                y[4 * q] += tq.x;
+                                y[4 * q + 1] += tq.y;
+                                y[4 * q + 2] += tq.z;
+                                y[4 * q + 3] += tq.w;
+                            }
+                        }
+#pragma unroll
+                        for (int m = 0; m < kNPad; ++m) {
+                            if (m < M) {
+                                const size_t o = size_t(m) * a.N + row;
+                                if (a.y_fp32)
+                                    static_cast<float *>(a.Y)[o] = y[m];
+                                else
+                                    static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+                            }
+                        }
+                    }
+                    if (threadIdx.x == 0) a.tickets[ug.rb] = 0u;  // zero again for the next call
+                }
             }
         }
     }
@@ -498,6 +516,7 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
     args.K = K;
     args.nsb = p.nsb;
     args.S = p.S;
+    args.units = p.nrb * p.S;
     args.timeout_ns = kDefaultTimeoutNs;
     args.partial = nullptr;
     args.tickets = nullptr;
@@ -520,8 +539,8 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
         if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
         configured_dev = dev;
     }
-    const unsigned units = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
-    ws_q8_tc_kernel<<<units, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmQ, tmX, args);
+    const int grid = args.units < sms ? args.units : sms;  // persistent: one CTA per SM
+    ws_q8_tc_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmQ, tmX, args);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
