@@ -334,6 +334,98 @@ def run_gpu(args, rank, world):
     return res
 
 
+def run_next_rows(dev, reps: int = 20):
+    """Device times of the rows built beyond the headline step, each timed alone after an L2
+    flush (median of `reps`): the Q8_0 weight-stationary matvec on the Qwen3-8B projection
+    shapes and on a 4096 -> 151936 lm_head, the lm_head -> Markov draft graph (Qwen3-8B lane),
+    and the probe-gated Markov draft (27B lane) with the gate open and closed.  Weights are
+    drawn on the device from a seeded generator: only timing is reported here, parity is
+    covered by the tests."""
+    import torch
+
+    from dspark_draft_sampling_gb300 import api
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = read_peak()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for r in range(reps):
+            flush.fill_(r & 0xFF)
+            torch.amax(flush.view(torch.int32), dim=0, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1000.0)
+        return statistics.median(ts)
+
+    def q8_weights(N, K):
+        q = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
+        d = (torch.rand((N, K // 32), generator=gen, device=dev) * 4e-4).half().view(torch.int16)
+        return q, d
+
+    def f16(shape, sd):
+        return (torch.randn(shape, generator=gen, device=dev) * sd).half()
+
+    out = {}
+    # Q8_0 projections, M = 7
+    q8_us, q8_bytes = 0.0, 0
+    for (K, N) in synth.WS_SHAPES:
+        q, d = q8_weights(N, K)
+        X = f16((7, K), 1.0)
+        Y = torch.empty((7, N), dtype=torch.float16, device=dev)
+        wsq = api.new_ws_q8_workspace(7, N, K, dev)
+        q8_us += timed(lambda: api.ws_matvec_q8(q, d, X, out=Y, workspace=wsq, stream=stream))
+        q8_bytes += N * K + N * (K // 32) * 2 + 7 * K * 2 + 7 * N * 2
+    out["ws_q8_qwen3_8b_4_shapes_us"] = q8_us
+    out["ws_q8_qwen3_8b_GBps"] = q8_bytes / (q8_us * 1e-6) / 1e9
+    K, N = 4096, 151936
+    q, d = q8_weights(N, K)
+    X = f16((7, K), 1.0)
+    Y = torch.empty((7, N), dtype=torch.float16, device=dev)
+    wsq = api.new_ws_q8_workspace(7, N, K, dev)
+    us = timed(lambda: api.ws_matvec_q8(q, d, X, out=Y, workspace=wsq, stream=stream))
+    byts = N * K + N * (K // 32) * 2 + 7 * K * 2 + 7 * N * 2
+    out["ws_q8_lm_head_4096x151936_us"] = us
+    out["ws_q8_lm_head_frac_of_hbm"] = byts / (us * 1e-6) / 1e9 / peak
+    del q, d, wsq
+    # lm_head (fp16) -> Markov draft, Qwen3-8B lane (num_reqs 1, k 7, vocab 151936, rank 256)
+    k, V, R, H = 7, 151936, 256, 4096
+    lm_head = f16((V, H), 0.02)
+    hidden = f16((k, H), 1.0)
+    w1 = f16((V, R), 0.02).view(torch.int16)
+    w2 = f16((V, R), 0.02).view(torch.int16)
+    prev = torch.zeros(1, dtype=torch.int64, device=dev)
+    dp = api.DraftPlan(lm_head, hidden, w1, w2, None, prev, k)
+    out["draft_plan_qwen3_8b_us"] = timed(lambda: dp.launch(stream))
+    dp.close()
+    del lm_head, dp
+    # probe-gated Markov draft, 27B lane
+    k, V = 15, 248320
+    base = torch.randn((1, k, V), generator=gen, device=dev) * 2.0
+    w1 = f16((V, R), 0.02).view(torch.int16)
+    w2 = f16((V, R), 0.02).view(torch.int16)
+    wq = torch.randint(0, 256, ((synth.PROBE_K // 32) * 34,), generator=gen, device=dev,
+                       dtype=torch.uint8)
+    wq.view(-1, 34)[:, 0] = 0x00
+    wq.view(-1, 34)[:, 1] = 0x14  # every block scale = fp16 0x1400 (2^-10)
+    pin = torch.randn(synth.PROBE_K, generator=gen, device=dev)
+    for name, bias in (("open", 100.0), ("closed", -100.0)):  # z = bias + w.x, |w.x| << 100
+        gp = api.GatedDraftPlan(wq, pin, bias, 0.5, base, w1, w2, None, prev)
+        out[f"gated_plan_gate_{name}_us"] = timed(lambda: gp.launch(stream))
+        gp.close()
+    return out
+
+
 def cpu_oracle_step(mk, pr, ws):
     """One step of the oracle on the host: the same three parts, single-threaded fp64."""
     import oracle
@@ -372,6 +464,8 @@ def main():
     ap.add_argument("--num-reqs", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the separately timed rows beyond the headline step")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -464,9 +558,9 @@ def main():
         "e2e": res["e2e"],
         "wall_s_timed_region": res["wall"],
     }
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(B)
-    elif not args.no_cpu_baseline:
+    if not args.no_next_rows:
+        line["next_rows"] = run_next_rows(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(B)
     print(json.dumps(line))
     if world > 1:
