@@ -219,6 +219,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         bool aborted = false;  // CTA-uniform: no more computing or grid barriers, keep draining
         bool broken = false;   // this thread's wait on an accumulator timed out
+        // Base logits do not depend on prev: they are loaded kBaseAhead tiles ahead of use
+        // (across position boundaries), so a tile's epilogue never waits on a DRAM round trip.
+        constexpr int kBaseAhead = 4;
+        float bq[kBaseAhead][NB];
+        int ip = 0, tp = 0;  // the next tile to prefetch, as (position, tile)
+        auto load_base = [&](float (&dst)[NB]) {
+            const int rowp = tile_at(ip, tp) * kTileRows + et;
+            const bool in = ntiles > 0 && ip < a.k && rowp < a.V;
+#pragma unroll
+            for (int r = 0; r < NB; ++r)
+                dst[r] = (in && r < a.B) ? __ldg(a.base + (size_t(r) * a.k + ip) * a.V + rowp) : 0.f;
+            if (++tp >= ntiles) {
+                tp = 0;
+                ++ip;
+            }
+        };
+#pragma unroll
+        for (int q = 0; q < kBaseAhead; ++q) load_base(bq[q]);
         int tc = 0;
         for (int i = 0; i < a.k; ++i) {
             unsigned long long best[NB];
@@ -230,10 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = row < a.V && !aborted;
                 float bv[NB];
 #pragma unroll
-                for (int r = 0; r < NB; ++r) {
-                    bv[r] = 0.f;
-                    if (valid && r < a.B) bv[r] = __ldg(a.base + (size_t(r) * a.k + i) * a.V + row);
-                }
+                for (int r = 0; r < NB; ++r) bv[r] = bq[0][r];
+#pragma unroll
+                for (int q = 0; q + 1 < kBaseAhead; ++q)
+#pragma unroll
+                    for (int r = 0; r < NB; ++r) bq[q][r] = bq[q + 1][r];
+                load_base(bq[kBaseAhead - 1]);
                 if (!broken && !mbar_wait(&acc_full[ab], (tc >> 1) & 1, a.timeout_ns)) {
                     broken = true;
                     atomicOr(a.status, kStatusTimeout);
