@@ -81,12 +81,13 @@ dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64
                            CU_TENSOR_MAP_SWIZZLE_128B, base, rows, cols, box_rows, box_cols);
 }
 
-dspark_status make_tmap_f16_kblocks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                                    uint32_t box_rows, uint32_t box_kblocks) {
+dspark_status make_tmap_kblocks(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
+                                uint32_t box_rows, uint32_t box_kblocks) {
     const cuuint64_t dims[3] = {64, rows, cols / 64};
     const cuuint64_t strides[2] = {cols * 2, 128};
     const cuuint32_t box[3] = {64, box_rows, box_kblocks};
-    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
+    return encode_tiled(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
 }
 
 dspark_status make_tmap_2d_u8_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,

@@ -13,13 +13,16 @@
 // GB300 design (one persistent CTA per SM, cooperative launch for the step barrier)
 //  * CTA c owns a contiguous range of 128-row tiles of markov_w2 for every position; odd
 //    positions walk it backwards so each position starts on rows still in L2.
-//  * Warp 4 (one thread): 2-D TMA tensor copies of [128 rows x 64 k] bf16 boxes (16 KB,
-//    128-byte swizzle) into a 12-stage ring.  markov_w2 does not depend on prev, so it
-//    runs ahead across position boundaries.
-//  * Warp 5: allocates 32 TMEM columns (two 128 x 16 fp32 accumulators); one thread
-//    issues, per box, four tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows,
+//  * Warp 4 (one thread): one 3-D TMA tensor copy per tile, the whole [128 rows x rank] bf16
+//    tile (64 KB at rank 256: rank/64 blocks of [128 x 64] in the 128-byte swizzle) into a
+//    192 KB ring of tile slots.  markov_w2 does not depend on prev, so it runs ahead across
+//    position boundaries.
+//  * Warp 5: allocates 32 TMEM columns (two 128 x 16 fp32 accumulators); one thread issues,
+//    per tile, rank/16 tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows,
 //    N = 16 request slots, K = 16) against H, which the epilogue warps write into shared
-//    memory in the same swizzled layout (rows >= num_reqs stay zero).
+//    memory in the same swizzled layout (rows >= num_reqs stay zero), then one
+//    tcgen05.commit that both frees the tile slot and hands the accumulator to the epilogue.
+//    One barrier round trip per 64 KB keeps the single issuing thread ahead of the stream.
 //  * Warps 0-3 (thread = TMEM lane = vocab row of the tile): tcgen05.ld the accumulator,
 //    add the base logits, keep the best (value, lowest index) key per request; at the end
 //    of a position reduce keys (warp shuffles, shared atomicMax, one global atomicMax per
@@ -37,13 +40,14 @@ constexpr int kThreads = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
 constexpr int kEpiThreads = 128;
 constexpr int kTileRows = 128;
 constexpr int kKB = 64;                            // k per box (128 B of bf16)
-constexpr int kBoxBytes = kTileRows * kKB * 2;     // 16 KB
-constexpr int kStages = 12;
+constexpr int kBoxBytes = kTileRows * kKB * 2;     // 16 KB: one 64-k block of a tile
+constexpr int kRingBytes = 12 * kBoxBytes;         // 192 KB of tile slots
+constexpr int kMaxSlots = kRingBytes / kBoxBytes;  // rank 64: 12 slots; rank 256: 3
 constexpr int kNPad = 16;                          // MMA N: request slots
 constexpr int kHBlockBytes = kNPad * kKB * 2;      // 2 KB per k-block of H
 constexpr int kHMaxBytes = 4 * kHBlockBytes;       // rank <= 256
 constexpr uint32_t kTmemCols = 32;
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kBoxBytes + 2 * kHMaxBytes + 512;
+constexpr size_t kSmemBytes = 1024 + size_t(kRingBytes) + 2 * kHMaxBytes + 512;
 
 __device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
 #pragma unroll
@@ -61,11 +65,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     unsigned char *ring = smem;
-    unsigned char *hbuf = smem + size_t(kStages) * kBoxBytes;  // 2 buffers
+    unsigned char *hbuf = smem + size_t(kRingBytes);  // 2 buffers
+    // full[s]: tile slot s landed.  empty[s]: the MMAs of the tile in slot s are done (one
+    // tcgen05.commit): the slot may be refilled and the tile's accumulator read.
     uint64_t *full = reinterpret_cast<uint64_t *>(hbuf + 2 * kHMaxBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;  // [2]
-    uint64_t *acc_empty = acc_full + 2;    // [2]
+    uint64_t *empty = full + kMaxSlots;
+    uint64_t *acc_empty = empty + kMaxSlots;  // [2] accumulator drained by the epilogue
     uint64_t *h_full = acc_empty + 2;      // [2]
     unsigned long long *s_best = reinterpret_cast<unsigned long long *>(h_full + 2);  // [kMaxReqs]
     int *s_cur = reinterpret_cast<int *>(s_best + kMaxReqs);                          // [kMaxReqs]
@@ -77,6 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nctas = gridDim.x;
     const int cta = blockIdx.x;
     const int nkb = R / kKB;
+    const int slot_bytes = nkb * kBoxBytes;
+    const int nslots = kRingBytes / slot_bytes;
     const int T = (a.V + kTileRows - 1) / kTileRows;
     const int t0 = static_cast<int>(static_cast<long long>(cta) * T / nctas);
     const int t1 = static_cast<int>(static_cast<long long>(cta + 1) * T / nctas);
@@ -91,12 +98,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kMaxSlots; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kEpiThreads / 32);
             mbar_init(&h_full[b], kEpiThreads);
         }
@@ -130,17 +136,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < a.k; ++i)
                 for (int t = 0; t < ntiles; ++t) {
                     const int y = tile_at(i, t) * kTileRows;
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) {
-                            atomicOr(a.status, kStatusTimeout);
-                            goto producer_done;
-                        }
-                        mbar_arrive_expect_tx(&full[st], kBoxBytes);
-                        tma_load_2d(ring + size_t(st) * kBoxBytes, &tmW2, kb * kKB, y, &full[st], pol);
-                        if (++st == kStages) {
-                            st = 0;
-                            ph ^= 1u;
-                        }
+                    if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) {
+                        atomicOr(a.status, kStatusTimeout);
+                        goto producer_done;
+                    }
+                    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(slot_bytes));
+                    tma_load_3d(ring + size_t(st) * slot_bytes, &tmW2, 0, y, 0, &full[st], pol);  // whole tile
+                    if (++st == nslots) {
+                        st = 0;
+                        ph ^= 1u;
                     }
                 }
         producer_done:;
@@ -168,27 +172,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         broken = true;
                         break;
                     }
+                    if (!mbar_wait(&full[st], ph, a.timeout_ns)) {
+                        broken = true;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t d = tmem + ab * kNPad;
+                    const uint64_t dT = dA0 + static_cast<uint64_t>(st * (slot_bytes >> 4));
                     for (int kb = 0; kb < nkb; ++kb) {
-                        if (!mbar_wait(&full[st], ph, a.timeout_ns)) {
-                            broken = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t dA = dA0 + static_cast<uint64_t>(st * (kBoxBytes >> 4));
+                        const uint64_t dA = dT + static_cast<uint64_t>(kb * (kBoxBytes >> 4));
                         const uint64_t dB = dH + static_cast<uint64_t>(kb * (kHBlockBytes >> 4));
                         tc_mma_f16(d, dA, dB, idesc, kb != 0);  // K = 16 per MMA, 32 B apart
                         tc_mma_f16(d, dA + 2, dB + 2, idesc, 1u);
                         tc_mma_f16(d, dA + 4, dB + 4, idesc, 1u);
                         tc_mma_f16(d, dA + 6, dB + 6, idesc, 1u);
-                        tc_commit(&empty[st]);
-                        if (++st == kStages) {
-                            st = 0;
-                            ph ^= 1u;
-                        }
                     }
-                    tc_commit(&acc_full[ab]);
+                    tc_commit(&empty[st]);  // frees the slot and hands the accumulator over
+                    if (++st == nslots) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                     if (++ab == 2) {
                         ab = 0;
                         aph ^= 1u;
@@ -238,6 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < kBaseAhead; ++q) load_base(bq[q]);
         int tc = 0;
+        int es = 0;  // slot of tile tc, and the phase of its empty barrier
+        uint32_t eph = 0;
         for (int i = 0; i < a.k; ++i) {
             unsigned long long best[NB];
 #pragma unroll
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < NB; ++r) bq[q][r] = bq[q + 1][r];
                 load_base(bq[kBaseAhead - 1]);
-                if (!broken && !mbar_wait(&acc_full[ab], (tc >> 1) & 1, a.timeout_ns)) {
+                if (!broken && !mbar_wait(&empty[es], eph, a.timeout_ns)) {
                     broken = true;
                     atomicOr(a.status, kStatusTimeout);
                     *reinterpret_cast<volatile int *>(s_abort) = 1;
@@ -265,6 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                if (++es == nslots) {
+                    es = 0;
+                    eph ^= 1u;
+                }
                 if (valid && !broken) {
 #pragma unroll
                     for (int r = 0; r < NB; ++r) {
@@ -405,8 +414,8 @@ dspark_status launch_dbg(const CUtensorMap &tm, const MarkovArgs &args, int R, i
 dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
     if (R % kKB != 0 || R > 256) return fail(DSPARK_ERR_UNSUPPORTED, "markov_tc: rank %d", R);
     CUtensorMap tm;
-    dspark_status st = make_tmap_2d(&tm, args.w2, true, static_cast<uint64_t>(args.V), static_cast<uint64_t>(R),
-                                    kTileRows, kKB);
+    dspark_status st = make_tmap_kblocks(&tm, args.w2, true, static_cast<uint64_t>(args.V), static_cast<uint64_t>(R),
+                                         kTileRows, static_cast<uint32_t>(R / kKB));
     if (st != DSPARK_OK) return st;
     if (args.dbg_logits || args.dbg_bias) return launch_dbg<true>(tm, args, R, nctas, stream);
     return launch_dbg<false>(tm, args, R, nctas, stream);

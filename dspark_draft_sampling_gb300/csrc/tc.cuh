@@ -19,11 +19,11 @@ dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64
 dspark_status make_tmap_2d_u8_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                                     uint32_t box_rows, uint32_t box_cols);
 
-// 3-D view of a row-major [rows, cols] fp16 matrix (cols a multiple of 64) as
+// 3-D view of a row-major [rows, cols] 16-bit matrix (cols a multiple of 64) as
 // [cols / 64][rows][64]: one box = box_kblocks consecutive 64-column blocks of box_rows rows,
 // stored block after block, each in the 128-byte-swizzled layout of make_tmap_2d.
-dspark_status make_tmap_f16_kblocks(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                                    uint32_t box_rows, uint32_t box_kblocks);
+dspark_status make_tmap_kblocks(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
+                                uint32_t box_rows, uint32_t box_kblocks);
 
 // ---- device ----------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy

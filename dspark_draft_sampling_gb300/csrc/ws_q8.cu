@@ -504,7 +504,7 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
     CUtensorMap tmQ, tmX;
     dspark_status st = make_tmap_2d_u8_sw128(&tmQ, Wq, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRows, kKS);
     if (st != DSPARK_OK) return st;
-    st = make_tmap_f16_kblocks(&tmX, X, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, 2);
+    st = make_tmap_kblocks(&tmX, X, false, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, 2);
     if (st != DSPARK_OK) return st;
 
     Q8Args args;
