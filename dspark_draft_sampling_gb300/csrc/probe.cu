@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kProbeThreads)
     conf_probe_kernel(const uint8_t *__restrict__ wq, const float *__restrict__ xa, long long lda, int nchunks_a,
                       const float *__restrict__ xb, long long ldb, int nchunks_b, float bias, float t_logit,
                       float *logit_out, int32_t *gate_out, cudaGraphConditionalHandle cond, int set_cond) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float warp_sum[kProbeWarps];
     const float *pa = xa + size_t(blockIdx.x) * lda;
     const float *pb = xb ? xb + size_t(blockIdx.x) * ldb : nullptr;
@@ -99,10 +101,17 @@ dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long lo
     // logit(t) on the host in double: sigmoid(z) >= t  <=>  z >= log(t / (1 - t)).
     const double t = static_cast<double>(threshold);
     const float t_logit = static_cast<float>(std::log(t / (1.0 - t)));
-    conf_probe_kernel<<<n_probes, kProbeThreads, 0, stream>>>(static_cast<const uint8_t *>(w_q8_0), xa, lda, Ka / 4,
-                                                              Kb > 0 ? xb : nullptr, ldb, Kb / 4, bias, t_logit,
-                                                              logit_out, gate_out, cond, set_cond);
-    cudaError_t e = cudaGetLastError();
+    const uint8_t *wb = static_cast<const uint8_t *>(w_q8_0);
+    const float *xbp = Kb > 0 ? xb : nullptr;
+    cudaError_t e;
+    if (set_cond) {  // inside a conditional graph: plain launch
+        conf_probe_kernel<<<n_probes, kProbeThreads, 0, stream>>>(wb, xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit,
+                                                                  logit_out, gate_out, cond, set_cond);
+        e = cudaGetLastError();
+    } else {
+        e = launch_pdl(conf_probe_kernel, dim3(static_cast<unsigned>(n_probes)), dim3(kProbeThreads), 0, stream, wb,
+                       xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit, logit_out, gate_out, cond, set_cond);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "conf_probe launch");
     return DSPARK_OK;
 }

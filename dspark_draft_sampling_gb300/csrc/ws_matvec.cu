@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait();  // no global-memory access before this point
 
     if (warp == 4) {
         // ---- TMA producer ----
@@ -322,8 +324,7 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
         configured_dev = dev;
     }
     const unsigned units = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
-    ws_matvec_tc_kernel<<<units, kThreads, kSmemBytes, s>>>(tmW, tmX, args);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), kSmemBytes, s, tmW, tmX, args);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;
 }

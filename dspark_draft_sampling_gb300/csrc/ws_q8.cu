@@ -153,6 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait();  // no global-memory access before this point
 
     if (warp == kTmaWarp) {
         // ---- TMA producer: int8 tile + two X atoms per stage ----
@@ -540,8 +542,8 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
         configured_dev = dev;
     }
     const int grid = args.units < sms ? args.units : sms;  // persistent: one CTA per SM
-    ws_q8_tc_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmQ, tmX, args);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(ws_q8_tc_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+                               reinterpret_cast<cudaStream_t>(stream), tmQ, tmX, args);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
 }
