@@ -55,6 +55,8 @@ def test_full_vocab_27b_lane(B):
     (8, 2, 153, 64, "injective"),
     (6, 4, 20000, 256, "injective"),
     (2, 6, 3001, 128, "identity"),
+    (1, 9, 60000, 128, "identity"),   # rank 128: 6 tile slots, wrapped many times
+    (4, 5, 100000, 64, "injective"),  # rank 64: 12 tile slots
 ])
 def test_ragged_shapes(B, k, V, R, d2t):
     inp = synth.markov_inputs(B, k, V, R, base_sd=1.0, w_sd=0.3, d2t=d2t, seed=B * 100 + k)
