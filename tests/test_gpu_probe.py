@@ -88,3 +88,21 @@ def test_split_input_matches_concatenated():
     assert torch.equal(z_split.view(torch.int32), z_full.view(torch.int32))
     assert torch.equal(g_split, g_full)
     parity.check_probe(inp, z_split.cpu().numpy(), g_split.cpu().numpy())
+
+
+def test_odd_aligned_weight_row():
+    """Q8_0 rows are 34-byte blocks with no alignment requirement: a row starting at an odd
+    address must give the same logits, bit for bit, as an aligned copy."""
+    inp = synth.probe_inputs(6, 7424, seed=8, random_scales=True, scale=0.01)
+    hid = torch.from_numpy(inp["hidden"]).cuda()
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    buf = torch.zeros(wq.numel() + 1, dtype=torch.uint8, device="cuda")
+    buf[1:] = wq
+    odd = buf[1:]
+    assert odd.data_ptr() % 2 == 1
+    z1, g1 = api.conf_probe(wq, hid, inp["bias"], inp["threshold"])
+    z2, g2 = api.conf_probe(odd, hid, inp["bias"], inp["threshold"])
+    torch.cuda.synchronize()
+    assert torch.equal(z1.view(torch.int32), z2.view(torch.int32))
+    assert torch.equal(g1, g2)
+    parity.check_probe(inp, z2.cpu().numpy(), g2.cpu().numpy())
