@@ -49,13 +49,13 @@ constexpr int kHMaxBytes = 4 * kHBlockBytes;       // rank <= 256
 constexpr uint32_t kTmemCols = 32;
 constexpr size_t kSmemBytes = 1024 + size_t(kRingBytes) + 2 * kHMaxBytes + 512;
 
-__device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
+// Warp-wide max of 64-bit keys with two 32-bit redux.sync reductions: the max high word,
+// then the max low word among the lanes holding it.
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+    const unsigned hi = static_cast<unsigned>(v >> 32);
+    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? static_cast<unsigned>(v) : 0u);
+    return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
 template <int NB, bool DBG>
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- end of position: CTA max, global max, grid barrier, winner ----
 #pragma unroll
                 for (int r = 0; r < NB; ++r) {
-                    const unsigned long long k_w = shfl_max_u64(best[r]);
+                    const unsigned long long k_w = warp_max_u64(best[r]);
                     if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
                 }
                 named_bar_sync(1, kEpiThreads);
