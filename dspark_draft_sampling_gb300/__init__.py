@@ -10,13 +10,16 @@ from .api import (  # noqa: F401
     GatedDraftPlan,
     MarkovPlan,
     conf_probe,
+    conf_probe_host,
     conf_probe_split,
     lib_path,
     load_library,
     markov_draft,
+    markov_draft_host,
     markov_workspace_bytes,
     q8_0_repack,
     ws_matvec,
+    ws_matvec_host,
     ws_matvec_q8,
     ws_matvec_q8_workspace_bytes,
     ws_matvec_workspace_bytes,

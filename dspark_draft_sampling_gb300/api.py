@@ -47,6 +47,12 @@ SIGNATURES = {
     "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "dspark_q8_0_repack": (_I, [_P, _P, _P, _I, _I, _P]),
+    "dspark_markov_draft_host_scratch_bytes": (_Z, [_I, _I, _I, _I]),
+    "dspark_markov_draft_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
+    "dspark_conf_probe_host_scratch_bytes": (_Z, [_I, _I]),
+    "dspark_conf_probe_host": (_I, [_P, _P, _F, _F, _I, _I, _P, _P, _P, _Z, _P, _P]),
+    "dspark_ws_matvec_host_scratch_bytes": (_Z, [_I, _I, _I]),
+    "dspark_ws_matvec_host": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P, _P]),
     "dspark_ws_matvec_q8_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec_q8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
 }
@@ -455,3 +461,87 @@ def ws_matvec_q8(Wq, Wd, X, *, out=None, out_fp32: bool = False, workspace=None,
                                  _ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
     _check(lib, st)
     return out
+
+
+# ---- host-buffer forms: per-call inputs and outputs in (pinned) host memory ----
+
+def _host_ptr(t, name: str, *, dtypes=None, itemsize=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor, ideally pinned")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise ValueError(f"{name} must have {itemsize}-byte elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def markov_draft_host_scratch_bytes(num_reqs: int, k: int, vocab: int, rank: int) -> int:
+    return int(load_library().dspark_markov_draft_host_scratch_bytes(num_reqs, k, vocab, rank))
+
+
+def conf_probe_host_scratch_bytes(K: int, n_probes: int) -> int:
+    return int(load_library().dspark_conf_probe_host_scratch_bytes(K, n_probes))
+
+
+def ws_matvec_host_scratch_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().dspark_ws_matvec_host_scratch_bytes(M, N, K))
+
+
+def _event(ev):
+    return None if ev is None else ctypes.c_void_p(ev.cuda_event)
+
+
+def markov_draft_host(base_h, w1, w2, d2t, prev_h, out_ids_h, scratch, *, inputs_copied=None,
+                      stream=None):
+    """Markov draft from host inputs: base_h float [B,k,V] and prev_h int64 [B] (updated in
+    place) on the host, w1/w2/d2t on the device; fills out_ids_h int64 [B,k] on the host
+    once `stream` is synchronized."""
+    lib = load_library()
+    B, k, V = base_h.shape
+    R = w2.shape[1]
+    st = lib.dspark_markov_draft_host(
+        _host_ptr(base_h, "base_h", dtypes=(torch.float32,)),
+        _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16), _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
+        _ptr(d2t, "d2t", dtypes=(torch.int32,), allow_none=True),
+        _host_ptr(prev_h, "prev_h", dtypes=(torch.int64,)), B, k, V, R,
+        _host_ptr(out_ids_h, "out_ids_h", dtypes=(torch.int64,)),
+        _ptr(scratch, "scratch"), scratch.numel() * scratch.element_size(), _event(inputs_copied),
+        _stream(stream))
+    _check(lib, st)
+    return out_ids_h
+
+
+def conf_probe_host(wq, hidden_h, bias: float, threshold: float, gate_h, scratch, *, logit_h=None,
+                    inputs_copied=None, stream=None):
+    """Confidence probes from host inputs: hidden_h float [n, K] on the host, wq on the
+    device; fills gate_h int32 [n] (and logit_h float [n]) on the host."""
+    lib = load_library()
+    n, K = hidden_h.shape
+    st = lib.dspark_conf_probe_host(
+        _ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)), _host_ptr(hidden_h, "hidden_h", dtypes=(torch.float32,)),
+        float(bias), float(threshold), K, n, _host_ptr(logit_h, "logit_h", dtypes=(torch.float32,), allow_none=True),
+        _host_ptr(gate_h, "gate_h", dtypes=(torch.int32,)), _ptr(scratch, "scratch"),
+        scratch.numel() * scratch.element_size(), _event(inputs_copied), _stream(stream))
+    _check(lib, st)
+    return gate_h
+
+
+def ws_matvec_host(W, X_h, Y_h, scratch, *, inputs_copied=None, stream=None):
+    """Y_h = X_h W^T with X_h fp16 [M, K] and Y_h [M, N] (fp16 or fp32) on the host, W on the
+    device; `scratch` must be zero-filled before its first use."""
+    lib = load_library()
+    N, K = W.shape
+    M = X_h.shape[0]
+    st = lib.dspark_ws_matvec_host(
+        _ptr(W, "W", itemsize=2, dtypes=_BITS16), _host_ptr(X_h, "X_h", itemsize=2, dtypes=_BITS16),
+        _host_ptr(Y_h, "Y_h", dtypes=(torch.float16, torch.float32)), 1 if Y_h.dtype == torch.float32 else 0,
+        M, N, K, _ptr(scratch, "scratch"), scratch.numel() * scratch.element_size(), _event(inputs_copied),
+        _stream(stream))
+    _check(lib, st)
+    return Y_h

@@ -16,7 +16,7 @@ SRC_DIR = os.path.join(PKG_DIR, "csrc")
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libdspark.so"
-SOURCES = ["common.cu", "markov.cu", "markov_tc.cu", "probe.cu", "ws_matvec.cu", "draft_plan.cu", "gated_plan.cu", "ws_q8.cu"]
+SOURCES = ["common.cu", "markov.cu", "markov_tc.cu", "probe.cu", "ws_matvec.cu", "draft_plan.cu", "gated_plan.cu", "ws_q8.cu", "host_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

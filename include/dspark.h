@@ -258,6 +258,57 @@ dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const ui
                                   size_t workspace_bytes, dspark_stream_t stream);
 
 /* =====================================================================================
+ * Host-buffer forms
+ *
+ * The three operations above with their per-call inputs read from host memory and their
+ * outputs written to host memory: the host-to-device copies, the same kernel, and the
+ * device-to-host copies are enqueued in that order on `stream` (cudaMemcpyAsync), so a cycle
+ * that starts from host data is one call per operation and one stream synchronization.
+ * Resident tensors (markov_w1/w2, d2t, the Q8_0 probe row, projection weights) stay device
+ * pointers.  Host buffers should be page-locked for the copies to be asynchronous.  Results
+ * are bit-identical to the device-pointer forms.
+ *
+ * device_scratch: caller-owned device memory of at least the matching *_scratch_bytes(),
+ * 256-byte aligned; it holds the device copies of the inputs and outputs and the operation's
+ * workspace.  For dspark_ws_matvec_host the scratch must be ZERO-FILLED before first use
+ * (its first part is the matvec workspace; every call leaves it zero-filled again).  Calls
+ * sharing a scratch must not overlap on the device.
+ *
+ *   dspark_markov_draft_host: base_host float [num_reqs, k, vocab]; prev_host int64
+ *     [num_reqs] in/out (read before the draft, overwritten with each request's last draft
+ *     id); out_ids_host int64 [num_reqs, k].
+ *   dspark_conf_probe_host: hidden_host float [n_probes, K]; gate_host int32 [n_probes];
+ *     logit_host float [n_probes] or NULL.
+ *   dspark_ws_matvec_host: X_host fp16 [M, K]; Y_host [M, N] fp32 if y_is_fp32 else fp16.
+ * inputs_copied: optional cudaEvent_t (NULL for none) recorded on `stream` right after the
+ *   host-to-device copies.  Pinned copies queued on several streams are served in the order
+ *   they become ready, not interleaved; a caller overlapping two operations can make the
+ *   second one's stream wait on the first one's event so a small input is not queued behind
+ *   a large one.
+ * Argument errors are reported before anything is enqueued; a *_scratch_bytes() of 0 means
+ * the sizes are invalid (or, for the matvec, that no CUDA device could be queried).
+ * ===================================================================================== */
+size_t dspark_markov_draft_host_scratch_bytes(int num_reqs, int k, int vocab, int rank);
+dspark_status dspark_markov_draft_host(const float *base_host, const uint16_t *markov_w1,
+                                       const uint16_t *markov_w2, const int32_t *d2t,
+                                       int64_t *prev_host, int num_reqs, int k, int vocab, int rank,
+                                       int64_t *out_ids_host, void *device_scratch,
+                                       size_t scratch_bytes, void *inputs_copied,
+                                       dspark_stream_t stream);
+
+size_t dspark_conf_probe_host_scratch_bytes(int K, int n_probes);
+dspark_status dspark_conf_probe_host(const void *w_q8_0, const float *hidden_host, float bias,
+                                     float threshold, int K, int n_probes, float *logit_host,
+                                     int32_t *gate_host, void *device_scratch, size_t scratch_bytes,
+                                     void *inputs_copied, dspark_stream_t stream);
+
+size_t dspark_ws_matvec_host_scratch_bytes(int M, int N, int K);
+dspark_status dspark_ws_matvec_host(const uint16_t *W, const uint16_t *X_host, void *Y_host,
+                                    int y_is_fp32, int M, int N, int K, void *device_scratch,
+                                    size_t scratch_bytes, void *inputs_copied,
+                                    dspark_stream_t stream);
+
+/* =====================================================================================
  * Draft step with device-side base logits
  *
  * Source: vllm.cpp issue #436, "W7 LANDED": the half W7 deferred is a block-forward

@@ -206,3 +206,34 @@ def test_python_q8_binding_rejects_cpu_tensors(dspark_lib):
                          torch.zeros(1, 256, dtype=torch.float16), workspace=torch.zeros(16))
     with pytest.raises(ValueError):
         api.q8_0_repack(torch.zeros(4 * 2 * 34, dtype=torch.uint8), 4, 64)
+
+
+def test_host_form_validation(dspark_lib):
+    """Argument errors of the host-buffer forms are caught before any copy is enqueued."""
+    lib = dspark_lib
+    m = lib.dspark_markov_draft_host
+    nb = lib.dspark_markov_draft_host_scratch_bytes(1, 4, 4096, 64)
+    assert nb >= 4 * 4096 * 4 and nb % 256 == 0
+    assert m(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 100, FAKE, FAKE, nb, NULL, NULL) == UNSUPPORTED
+    assert m(FAKE, FAKE, FAKE, NULL, FAKE, 9, 4, 4096, 64, FAKE, FAKE, nb, NULL, NULL) == UNSUPPORTED
+    assert m(NULL, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 64, FAKE, FAKE, nb, NULL, NULL) == INVALID
+    assert m(FAKE, FAKE, FAKE, NULL, NULL, 1, 4, 4096, 64, FAKE, FAKE, nb, NULL, NULL) == INVALID
+    assert m(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 64, FAKE, FAKE_ODD, nb, NULL, NULL) == INVALID
+    assert m(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 64, FAKE, FAKE, nb - 256, NULL, NULL) == INVALID
+    assert "scratch" in lib.dspark_last_error().decode()
+    assert m(FAKE, FAKE, FAKE, NULL, FAKE, 1, 0, 4096, 64, FAKE, FAKE, nb, NULL, NULL) == 0
+    p = lib.dspark_conf_probe_host
+    pb = lib.dspark_conf_probe_host_scratch_bytes(7424, 3)
+    assert pb >= 3 * 7424 * 4
+    assert p(FAKE, FAKE, 0.0, 0.5, 48, 3, NULL, FAKE, FAKE, pb, NULL, NULL) == INVALID
+    assert p(FAKE, FAKE, 0.0, 1.5, 7424, 3, NULL, FAKE, FAKE, pb, NULL, NULL) == INVALID
+    assert p(FAKE, NULL, 0.0, 0.5, 7424, 3, NULL, FAKE, FAKE, pb, NULL, NULL) == INVALID
+    assert p(FAKE, FAKE, 0.0, 0.5, 7424, 3, NULL, NULL, FAKE, pb, NULL, NULL) == INVALID
+    assert p(FAKE, FAKE, 0.0, 0.5, 7424, 3, NULL, FAKE, FAKE, pb - 1, NULL, NULL) == INVALID
+    assert p(FAKE, FAKE, 0.0, 0.5, 7424, 0, NULL, FAKE, FAKE, pb, NULL, NULL) == 0
+    w = lib.dspark_ws_matvec_host
+    assert w(FAKE, FAKE, FAKE, 0, 17, 64, 64, FAKE, 1 << 20, NULL, NULL) == UNSUPPORTED
+    assert w(FAKE, FAKE, FAKE, 0, 7, 64, 12, FAKE, 1 << 20, NULL, NULL) == INVALID
+    assert w(FAKE, NULL, FAKE, 0, 7, 64, 64, FAKE, 1 << 20, NULL, NULL) == INVALID
+    assert w(FAKE, FAKE, FAKE, 0, 7, 64, 64, FAKE_ODD, 1 << 20, NULL, NULL) == INVALID
+    assert w(FAKE, FAKE, FAKE, 0, 0, 64, 64, FAKE, 1 << 20, NULL, NULL) == 0
