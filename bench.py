@@ -49,10 +49,17 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ---------------------------------------------------------------- workload ---------------
+_WORKLOADS = {}
+
+
 def make_workload(num_reqs: int, seed: int = 0):
+    """The step's synthetic inputs (cached: the 27B lane takes seconds to draw)."""
+    if (num_reqs, seed) in _WORKLOADS:
+        return _WORKLOADS[(num_reqs, seed)]
     mk = synth.markov_config("full_vocab_27b", num_reqs=num_reqs, seed=seed)
     pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=seed)
     ws = [synth.ws_inputs(7, N, K, seed=seed + K + N) for (K, N) in synth.WS_SHAPES]
+    _WORKLOADS[(num_reqs, seed)] = (mk, pr, ws)
     return mk, pr, ws
 
 
@@ -438,6 +445,110 @@ def run_next_rows(dev, reps: int = 20):
     return out
 
 
+def run_configs(dev, mk27, reps: int = 30):
+    """Every configuration of the workload table timed on its own: median / p10 / p90 of
+    `reps` single calls with the L2 flushed before each (cold) and without (warm, back to
+    back), plus the algorithmic GB/s and the fraction of the measured HBM bandwidth (cold
+    median).  Markov lanes tiny / reduced_vocab / qwen3_8b / full_vocab_27b (num_reqs 1, 4,
+    8), the probe in latency mode (one probe, 4-byte readback, stream synchronization; host
+    clock) and batched (2048), and the four M = 7 WS matvecs."""
+    import torch
+
+    from dspark_draft_sampling_gb300 import api
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = read_peak()
+
+    def stats(ts):
+        ts = sorted(ts)
+        q = lambda f: ts[min(len(ts) - 1, int(round(f * (len(ts) - 1))))]
+        return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9)}
+
+    def timed(fn, cold):
+        for _ in range(3):
+            fn()
+        ts = []
+        for r in range(reps):
+            if cold:
+                flush.fill_(r & 0xFF)
+                torch.amax(flush.view(torch.int32), dim=0, out=sink)
+            else:
+                # keep the GPU busy while the host enqueues the call, so the events time the
+                # kernel and not the host's enqueue latency (the flush does this when cold)
+                torch.cuda._sleep(100000)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1000.0)
+        return stats(ts)
+
+    def entry(fn, nbytes):
+        cold, warm = timed(fn, True), timed(fn, False)
+        return {"us_cold": cold, "us_warm": warm, "algorithmic_bytes": nbytes,
+                "GBps_cold": nbytes / (cold["median"] * 1e-6) / 1e9,
+                "frac_of_hbm_cold": nbytes / (cold["median"] * 1e-6) / 1e9 / peak}
+
+    out = {}
+    w1_27 = torch.from_numpy(mk27["w1"].view(np.int16)).to(dev)
+    w2_27 = torch.from_numpy(mk27["w2"].view(np.int16)).to(dev)
+    lanes = [(name, None) for name in ("tiny", "reduced_vocab", "qwen3_8b")] + [("full_vocab_27b", b) for b in (1, 4, 8)]
+    for name, nreq in lanes:
+        if name == "full_vocab_27b":
+            c = synth.MARKOV_CONFIGS[name]
+            base = torch.from_numpy(synth.markov_base(nreq, c["k"], c["vocab"], base_sd=c["base_sd"])).to(dev)
+            w1, w2, d2t = w1_27, w2_27, None
+            prev = torch.from_numpy(np.random.default_rng(nreq).integers(0, c["vocab"], nreq)).to(dev)
+            B, k, V, R = nreq, c["k"], c["vocab"], c["rank"]
+            key = f"markov_{name}_num_reqs_{nreq}"
+        else:
+            mk = synth.markov_config(name)
+            base = torch.from_numpy(mk["base"]).to(dev)
+            w1 = torch.from_numpy(mk["w1"].view(np.int16)).to(dev)
+            w2 = torch.from_numpy(mk["w2"].view(np.int16)).to(dev)
+            d2t = None if mk["d2t"] is None else torch.from_numpy(mk["d2t"]).to(dev)
+            prev = torch.from_numpy(mk["prev0"].copy()).to(dev)
+            B, k, V, R = mk["num_reqs"], mk["k"], mk["vocab"], mk["rank"]
+            key = f"markov_{name}"
+        plan = api.MarkovPlan(base, w1, w2, d2t, prev)
+        out[key] = entry(lambda: plan.launch(stream), markov_bytes(B, k, V, R, d2t is not None))
+        out[key]["us_per_position_cold"] = out[key]["us_cold"]["median"] / k
+        plan.close()
+        del plan, base
+    pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=0)
+    wq = torch.from_numpy(pr["wq"]).to(dev)
+    hid = torch.from_numpy(pr["hidden"]).to(dev)
+    z = torch.empty(N_PROBES, dtype=torch.float32, device=dev)
+    g = torch.empty(N_PROBES, dtype=torch.int32, device=dev)
+    out["probe_batched_2048"] = entry(
+        lambda: api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=g, stream=stream),
+        probe_bytes(N_PROBES, synth.PROBE_K))
+    g_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    h1 = hid[:1].contiguous()
+    lat = []
+    for r in range(reps + 3):
+        t0 = time.perf_counter()
+        api.conf_probe(wq, h1, pr["bias"], pr["threshold"], gate_out=g[:1], stream=stream)
+        g_h.copy_(g[:1], non_blocking=True)
+        stream.synchronize()
+        if r >= 3:
+            lat.append((time.perf_counter() - t0) * 1e6)
+    out["probe_latency_1_with_4B_readback"] = {"us_host_clock": stats(lat)}
+    for (K, N) in synth.WS_SHAPES:
+        w = synth.ws_inputs(7, N, K)
+        W = torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16)
+        X = torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16)
+        Y = torch.empty((7, N), dtype=torch.float16, device=dev)
+        wsp = api.new_ws_workspace(7, N, K, dev)
+        out[f"ws_matvec_m7_{K}x{N}"] = entry(lambda: api.ws_matvec(W, X, out=Y, workspace=wsp, stream=stream),
+                                             ws_bytes(7, N, K))
+    return out
+
+
 def cpu_oracle_step(mk, pr, ws):
     """One step of the oracle on the host: the same three parts, single-threaded fp64."""
     import oracle
@@ -478,6 +589,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the separately timed rows beyond the headline step")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sweep (median/p10/p90, cold and warm L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -572,6 +685,9 @@ def main():
     }
     if not args.no_next_rows:
         line["next_rows"] = run_next_rows(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    if not args.no_configs:
+        line["configs"] = run_configs(torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))),
+                                      make_workload(B, seed=0)[0])
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(B)
     print(json.dumps(line))

@@ -96,7 +96,7 @@ def markov_inputs(num_reqs: int, k: int, vocab: int, rank: int, *, base_sd: floa
     """
     if d2t not in ("identity", "injective"):
         raise ValueError("d2t must be 'identity' or 'injective'")
-    base = _normal(seed, _S_BASE, (num_reqs, k, vocab), base_sd)
+    base = markov_base(num_reqs, k, vocab, base_sd=base_sd, seed=seed)
     w1 = f32_to_bf16_bits(_normal(seed, _S_W1, (vocab, rank), w_sd))
     w2 = f32_to_bf16_bits(_normal(seed, _S_W2, (vocab, rank), w_sd))
     prev0 = _rng(seed, _S_PREV).integers(0, vocab, size=num_reqs, dtype=np.int64)
@@ -123,6 +123,12 @@ def markov_inputs(num_reqs: int, k: int, vocab: int, rank: int, *, base_sd: floa
             spiked.append(i)
     return dict(base=base, w1=w1, w2=w2, d2t=d2t_arr, prev0=prev0, ties=ties,
                 spiked_steps=spiked, num_reqs=num_reqs, k=k, vocab=vocab, rank=rank)
+
+
+def markov_base(num_reqs: int, k: int, vocab: int, *, base_sd: float = 2.0, seed: int = 0) -> np.ndarray:
+    """The base logits of markov_inputs alone (same stream, same values; request r's rows do
+    not depend on num_reqs)."""
+    return _normal(seed, _S_BASE, (num_reqs, k, vocab), base_sd)
 
 
 def markov_config(name: str, *, num_reqs: int | None = None, seed: int = 0) -> dict:
