@@ -46,6 +46,9 @@ SIGNATURES = {
                                      _I, _P, _P, _P]),
     "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "dspark_ws_matvec_status": (_I, [_P, _P]),
+    "dspark_ws_matvec_debug": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _U, _P]),
+    "dspark_ws_matvec_q8_debug": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _U, _P]),
     "dspark_q8_0_repack": (_I, [_P, _P, _P, _I, _I, _P]),
     "dspark_markov_draft_host_scratch_bytes": (_Z, [_I, _I, _I, _I]),
     "dspark_markov_draft_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
@@ -545,3 +548,10 @@ def ws_matvec_host(W, X_h, Y_h, scratch, *, inputs_copied=None, stream=None):
         _stream(stream))
     _check(lib, st)
     return Y_h
+
+
+def ws_matvec_status(workspace, *, stream=None) -> int:
+    """Status of a WS (fp16 or Q8_0) workspace after its calls: DSPARK_OK or
+    DSPARK_ERR_TIMEOUT (reported once, then cleared)."""
+    lib = load_library()
+    return int(lib.dspark_ws_matvec_status(_ptr(workspace, "workspace"), _stream(stream)))

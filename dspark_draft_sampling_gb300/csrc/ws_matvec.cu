@@ -51,7 +51,10 @@ struct WsArgs {
     int M, N, K;
     int nkb;  // k-blocks
     int S;    // units per row block
+    unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
+    unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
+                                  // this long on a barrier that nothing signals
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -62,7 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(kStages) * kStageBytes);
     uint64_t *empty = full + kStages;
     uint64_t *done = empty + kStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *never = done + 1;  // signalled by nobody: the fault-injection hook waits on it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
     int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -81,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
+        mbar_init(never, 1);
         fence_mbar_init();
     }
     if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
@@ -99,7 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) break;
+                if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) {
+                    atomicOr(a.status, kWsStatusTimeout);
+                    break;
+                }
                 unsigned char *sa = smem + size_t(st) * kStageBytes;
                 mbar_arrive_expect_tx(&full[st], kStageBytes);
                 tma_load_2d(sa, &tmW, (kb0 + j) * kKB, n0, &full[st], pol_w);
@@ -119,7 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                if (!mbar_wait(&full[st], ph, a.timeout_ns)) break;
+                if (!mbar_wait(&full[st], ph, a.timeout_ns)) {
+                    atomicOr(a.status, kWsStatusTimeout);
+                    break;
+                }
                 tc_fence_after();
                 const uint64_t dA = dA0 + static_cast<uint64_t>(st * (kStageBytes >> 4));
                 const uint64_t dB = dA + static_cast<uint64_t>(kABytes >> 4);
@@ -137,7 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 ----
+        if (a.stall_ns && !mbar_wait(never, 0, a.stall_ns) && threadIdx.x == 0) atomicOr(a.status, kWsStatusTimeout);
         const bool ok = mbar_wait(done, 0, a.timeout_ns);
+        if (!ok) atomicOr(a.status, kWsStatusTimeout);
         tc_fence_after();
         uint32_t v[16];
         tmem_ld_16(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
@@ -246,11 +259,10 @@ Plan plan_for(int N, int K, int sms) {
 
 // Workspace: a fixed ticket area first (so tickets stay at the same place and stay zero
 // whatever shapes share the workspace), then the partial tiles.
-constexpr size_t kTicketBytes = 65536;  // up to 16384 row blocks (N <= 2,097,152)
-
 size_t workspace_bytes_for(const Plan &p) {
-    if (p.S == 1) return kTicketBytes;
-    return kTicketBytes + size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
+    const size_t fixed = kWsHeaderBytes + kWsTicketBytes;
+    if (p.S == 1) return fixed;
+    return fixed + size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
 }
 
 }  // namespace
@@ -259,13 +271,15 @@ size_t workspace_bytes_for(const Plan &p) {
 extern "C" size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K) {
     (void)M;
     int sms = 0;
-    if (N <= 0 || K <= 0) return dspark::kTicketBytes;
+    if (N <= 0 || K <= 0) return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
     if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
     return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
 }
 
-extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
-                                          int K, void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
+namespace {
+
+dspark_status ws_enqueue(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N, int K,
+                         void *workspace, size_t workspace_bytes, unsigned long long stall_ns, dspark_stream_t stream) {
     using namespace dspark;
     clear_error();
     if (M < 0 || N < 0 || K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec: negative size");
@@ -280,8 +294,8 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
     const Plan p = plan_for(N, K, sms);
-    if (size_t(p.nrb) * sizeof(unsigned) > kTicketBytes)
-        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: N=%d exceeds %zu rows", N, kTicketBytes / 4 * kRowsPerUnit);
+    if (size_t(p.nrb) * sizeof(unsigned) > kWsTicketBytes)
+        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: N=%d exceeds %zu rows", N, kWsTicketBytes / 4 * kRowsPerUnit);
     const size_t need = workspace_bytes_for(p);
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec: workspace of %zu bytes < required %zu", workspace_bytes, need);
@@ -304,10 +318,12 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     args.timeout_ns = kDefaultTimeoutNs;
     args.partial = nullptr;
     args.tickets = nullptr;
+    args.status = static_cast<unsigned *>(workspace);
+    args.stall_ns = stall_ns;
     if (p.S > 1) {
         unsigned char *ws = static_cast<unsigned char *>(workspace);
-        args.tickets = reinterpret_cast<unsigned *>(ws);
-        args.partial = reinterpret_cast<float *>(ws + kTicketBytes);
+        args.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes);
+        args.partial = reinterpret_cast<float *>(ws + kWsHeaderBytes + kWsTicketBytes);
     }
 
     static int configured_dev = -1;
@@ -327,4 +343,35 @@ extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, 
     cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), kSmemBytes, s, tmW, tmX, args);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
+                                          int K, void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
+    return ws_enqueue(W, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 0ull, stream);
+}
+
+extern "C" dspark_status dspark_ws_matvec_debug(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M,
+                                                int N, int K, void *workspace, size_t workspace_bytes,
+                                                unsigned stall_us, dspark_stream_t stream) {
+    if (stall_us == 0) return dspark::fail(DSPARK_ERR_INVALID, "ws_matvec_debug: stall_us must be > 0");
+    return ws_enqueue(W, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 1000ull * stall_us, stream);
+}
+
+extern "C" dspark_status dspark_ws_matvec_status(void *workspace, dspark_stream_t stream) {
+    using namespace dspark;
+    clear_error();
+    if (!workspace) return fail(DSPARK_ERR_INVALID, "ws_matvec_status: null workspace");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned st = 0;
+    e = cudaMemcpy(&st, workspace, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(ws status)");
+    if (st == 0) return DSPARK_OK;
+    // report once, and leave the workspace zero-filled again
+    e = cudaMemset(workspace, 0, sizeof st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(ws status)");
+    return fail(DSPARK_ERR_TIMEOUT, "ws_matvec: a device-side wait timed out");
 }

@@ -67,9 +67,8 @@ constexpr int kASlots = 4;             // TMEM ring of fp16 A tiles
 constexpr uint32_t kACols = kKS / 2;   // 64 columns: 128 fp16 per lane
 constexpr uint32_t kAColBase = kTSlots * kNPad;                  // 256
 constexpr uint32_t kTmemCols = kAColBase + kASlots * kACols;     // 512
-constexpr int kNumBars = 2 * kStages + kASlots + kTGroups + 2;
+constexpr int kNumBars = 2 * kStages + kASlots + kTGroups + 3;
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kSlotBytes + kNumBars * 8 + 16;
-constexpr size_t kTicketBytes = 65536;  // up to 16384 row blocks (N <= 2,097,152)
 static_assert(kTmemCols == 512, "the TMEM allocation must be a power of two <= 512");
 static_assert(kStages % 2 == 0 && kASlots % 2 == 0 && kTGroups % 2 == 0, "rings must keep stage parity");
 static_assert(kASlots == kTGroups && kASlots < kStages, "stage j uses A slot and accumulator group j % 4");
@@ -84,7 +83,10 @@ struct Q8Args {
     int nsb;    // 256-k superblocks
     int S;      // units per row block
     int units;  // row blocks x S; CTA c takes units c, c + gridDim.x, ...
+    unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
+    unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
+                                  // this long on a barrier that nothing signals
 };
 
 struct Unit {
@@ -131,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full_a = done + kStages;     // fp16 A tile written to TMEM (per A slot)
     uint64_t *empty_t = full_a + kASlots;  // accumulator group drained by the epilogue
     uint64_t *mma_done = empty_t + kTGroups;  // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
+    uint64_t *never = mma_done + 2;           // signalled by nobody: the fault-injection hook waits on it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
     int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < kTGroups; ++g) mbar_init(&empty_t[g], 4);
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
+        mbar_init(never, 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
@@ -169,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = J % kStages;
                     // slot st was last used by stage J - kStages
                     if (!mbar_wait(&done[st], static_cast<uint32_t>(((J / kStages) & 1) ^ 1), a.timeout_ns)) {
+                        atomicOr(a.status, kWsStatusTimeout);
                         stop = true;
                         break;
                     }
@@ -200,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the converters arrive on full_a only after the stage's TMA copies (X included)
                     // have landed, so this one wait orders both operands before the MMAs
                     if (!mbar_wait(&full_a[g], ph, a.timeout_ns) || !mbar_wait(&empty_t[g], ph ^ 1u, a.timeout_ns)) {
+                        atomicOr(a.status, kWsStatusTimeout);
                         stop = true;
                         break;
                     }
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_commit(&mma_done[par]);  // arrives once every MMA this thread issued has completed
-            mbar_wait(&mma_done[par], 0, a.timeout_ns);
+            if (!mbar_wait(&mma_done[par], 0, a.timeout_ns)) atomicOr(a.status, kWsStatusTimeout);
         }
     } else if (warp >= 4) {
         // ---- converters: one weight row's 128 int8 -> 128 fp16 in TMEM, alternate stages ----
@@ -242,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         broken = true;
                 }
                 broken = __any_sync(0xffffffffu, broken);
+                if (broken && lane == 0) atomicOr(a.status, kWsStatusTimeout);
                 if (!broken) {
                     const unsigned char *rowp = ring + size_t(st) * kSlotBytes + r * kKS;
 #pragma unroll
@@ -276,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 of each unit ----
         const int lrow = warp * 32 + lane;
+        if (a.stall_ns && !mbar_wait(never, 0, a.stall_ns) && threadIdx.x == 0) atomicOr(a.status, kWsStatusTimeout);
         bool ok = true;
         int J = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
@@ -304,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = J % kStages, g = J % kTGroups;
                     if (ok) ok = mbar_wait(&done[st], static_cast<uint32_t>((J / kStages) & 1), a.timeout_ns);
                     ok = __all_sync(0xffffffffu, ok);
+                    if (!ok && lane == 0) atomicOr(a.status, kWsStatusTimeout);
                     tc_fence_after();
                     uint32_t v[kBlocksPerStage][16];
                     if (ok) {
@@ -431,8 +440,9 @@ Plan plan_for(int N, int K, int sms) {
 }
 
 size_t workspace_bytes_for(const Plan &p) {
-    if (p.S == 1) return kTicketBytes;
-    return kTicketBytes + size_t(p.nrb) * p.S * kRows * kNPad * sizeof(float);
+    const size_t fixed = kWsHeaderBytes + kWsTicketBytes;
+    if (p.S == 1) return fixed;
+    return fixed + size_t(p.nrb) * p.S * kRows * kNPad * sizeof(float);
 }
 
 __global__ void q8_0_repack_kernel(const uint8_t *__restrict__ aos, int8_t *__restrict__ q, uint16_t *__restrict__ d,
@@ -474,14 +484,16 @@ extern "C" dspark_status dspark_q8_0_repack(const void *w_q8_0, int8_t *q, uint1
 extern "C" size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K) {
     (void)M;
     int sms = 0;
-    if (N <= 0 || K < 256) return dspark::kTicketBytes;
+    if (N <= 0 || K < 256) return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
     if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
     return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
 }
 
-extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
-                                             int y_is_fp32, int M, int N, int K, void *workspace,
-                                             size_t workspace_bytes, dspark_stream_t stream) {
+namespace {
+
+dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
+                         int K, void *workspace, size_t workspace_bytes, unsigned long long stall_ns,
+                         dspark_stream_t stream) {
     using namespace dspark;
     clear_error();
     if (M < 0 || N < 0 || K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: negative size");
@@ -497,8 +509,8 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
     const Plan p = plan_for(N, K, sms);
-    if (size_t(p.nrb) * sizeof(unsigned) > kTicketBytes)
-        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: N=%d exceeds %zu rows", N, kTicketBytes / 4 * kRows);
+    if (size_t(p.nrb) * sizeof(unsigned) > kWsTicketBytes)
+        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: N=%d exceeds %zu rows", N, kWsTicketBytes / 4 * kRows);
     const size_t need = workspace_bytes_for(p);
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
@@ -522,10 +534,12 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
     args.timeout_ns = kDefaultTimeoutNs;
     args.partial = nullptr;
     args.tickets = nullptr;
+    args.status = static_cast<unsigned *>(workspace);
+    args.stall_ns = stall_ns;
     if (p.S > 1) {
         unsigned char *ws = static_cast<unsigned char *>(workspace);
-        args.tickets = reinterpret_cast<unsigned *>(ws);
-        args.partial = reinterpret_cast<float *>(ws + kTicketBytes);
+        args.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes);
+        args.partial = reinterpret_cast<float *>(ws + kWsHeaderBytes + kWsTicketBytes);
     }
 
     static int configured_dev = -1;
@@ -546,4 +560,19 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
                                reinterpret_cast<cudaStream_t>(stream), tmQ, tmX, args);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
+                                             int y_is_fp32, int M, int N, int K, void *workspace,
+                                             size_t workspace_bytes, dspark_stream_t stream) {
+    return q8_enqueue(Wq, Wd, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 0ull, stream);
+}
+
+extern "C" dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
+                                                   int y_is_fp32, int M, int N, int K, void *workspace,
+                                                   size_t workspace_bytes, unsigned stall_us, dspark_stream_t stream) {
+    if (stall_us == 0) return dspark::fail(DSPARK_ERR_INVALID, "ws_matvec_q8_debug: stall_us must be > 0");
+    return q8_enqueue(Wq, Wd, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 1000ull * stall_us, stream);
 }

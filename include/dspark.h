@@ -15,7 +15,7 @@
  *   - The return value reports argument checking and launch errors only.  Faults
  *     that can only be seen on the device (an out-of-range prev or d2t entry, a
  *     device-side wait that gave up) are recorded in the workspace and reported by
- *     dspark_markov_status().
+ *     dspark_markov_status() / dspark_ws_matvec_status().
  *   - dspark_last_error() returns a message for the last non-OK status returned on
  *     the calling thread.  No call aborts, exits or traps.
  */
@@ -220,6 +220,21 @@ dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, in
                                int M, int N, int K, void *workspace, size_t workspace_bytes,
                                dspark_stream_t stream);
 
+/* Synchronizes `stream`, then reads the status word of a dspark_ws_matvec or
+ * dspark_ws_matvec_q8 workspace (its first 4 bytes): DSPARK_OK, or DSPARK_ERR_TIMEOUT if a
+ * device-side wait of a call on it gave up since the last check (the kernel then skipped
+ * the affected outputs and returned).  A reported timeout is cleared, leaving the workspace
+ * zero-filled again. */
+dspark_status dspark_ws_matvec_status(void *workspace, dspark_stream_t stream);
+
+/* Fault-injection hook for testing the device-side wait limit: the same launch as
+ * dspark_ws_matvec, except that the epilogue first waits `stall_us` microseconds on a
+ * barrier that nothing signals; the wait gives up, the kernel records DSPARK_ERR_TIMEOUT in
+ * the workspace status word and finishes normally.  Not for production use. */
+dspark_status dspark_ws_matvec_debug(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32,
+                                     int M, int N, int K, void *workspace, size_t workspace_bytes,
+                                     unsigned stall_us, dspark_stream_t stream);
+
 /* =====================================================================================
  * Weight-stationary small-M matvec with Q8_0 weights
  *
@@ -256,6 +271,12 @@ size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K);
 dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,
                                   int y_is_fp32, int M, int N, int K, void *workspace,
                                   size_t workspace_bytes, dspark_stream_t stream);
+
+/* As dspark_ws_matvec_debug, for the Q8_0 matvec (status read by dspark_ws_matvec_status). */
+dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X,
+                                        void *Y, int y_is_fp32, int M, int N, int K,
+                                        void *workspace, size_t workspace_bytes, unsigned stall_us,
+                                        dspark_stream_t stream);
 
 /* =====================================================================================
  * Host-buffer forms

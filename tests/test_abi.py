@@ -188,7 +188,7 @@ def test_ws_q8_validation(dspark_lib):
     assert g(ws=FAKE_ODD) == INVALID
     assert g(M=0) == 0
     assert g(N=0) == 0
-    assert lib.dspark_ws_matvec_q8_workspace_bytes(7, 0, 256) == 65536
+    assert lib.dspark_ws_matvec_q8_workspace_bytes(7, 0, 256) == 65536 + 256
     r = lib.dspark_q8_0_repack
     assert r(FAKE, FAKE, FAKE, 4, 48, NULL) == INVALID
     assert r(FAKE, FAKE, FAKE, -1, 64, NULL) == INVALID
@@ -237,3 +237,12 @@ def test_host_form_validation(dspark_lib):
     assert w(FAKE, NULL, FAKE, 0, 7, 64, 64, FAKE, 1 << 20, NULL, NULL) == INVALID
     assert w(FAKE, FAKE, FAKE, 0, 7, 64, 64, FAKE_ODD, 1 << 20, NULL, NULL) == INVALID
     assert w(FAKE, FAKE, FAKE, 0, 0, 64, 64, FAKE, 1 << 20, NULL, NULL) == 0
+
+
+def test_ws_status_and_debug_validation(dspark_lib):
+    lib = dspark_lib
+    assert lib.dspark_ws_matvec_status(NULL, NULL) == INVALID
+    assert lib.dspark_ws_matvec_debug(FAKE, FAKE, FAKE, 0, 7, 64, 64, FAKE, 1 << 20, 0, NULL) == INVALID
+    assert lib.dspark_ws_matvec_debug(NULL, FAKE, FAKE, 0, 7, 64, 64, FAKE, 1 << 20, 100, NULL) == INVALID
+    assert lib.dspark_ws_matvec_q8_debug(FAKE, FAKE, FAKE, FAKE, 0, 7, 64, 256, FAKE, 1 << 20, 0, NULL) == INVALID
+    assert lib.dspark_ws_matvec_q8_debug(FAKE, FAKE, FAKE, FAKE, 0, 17, 64, 256, FAKE, 1 << 20, 100, NULL) == UNSUPPORTED

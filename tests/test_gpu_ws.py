@@ -87,3 +87,24 @@ def test_workspace_shared_across_shapes():
             ref = api.ws_matvec(W, X, out_fp32=True)  # its own fresh workspace
             torch.cuda.synchronize()
             assert torch.equal(y.view(torch.int32), ref.view(torch.int32)), (M, N, K)
+
+
+def test_workspace_status_reports_a_wait_that_gave_up():
+    """Failure detection without a fault: the debug launch makes the epilogue wait 2 ms on a
+    barrier nothing signals; the kernel records a timeout in the workspace status word and
+    returns.  The status is read once, then cleared, and the context stays usable."""
+    inp = synth.ws_inputs(7, 1024, 4096, seed=11)
+    W, X = _dev(inp)
+    ws = api.new_ws_workspace(7, 1024, 4096)
+    y = torch.empty((7, 1024), dtype=torch.float32, device="cuda")
+    lib = api.load_library()
+    st = lib.dspark_ws_matvec_debug(api._ptr(W, "W"), api._ptr(X, "X"), api._ptr(y, "y"), 1, 7, 1024, 4096,
+                                    api._ptr(ws, "ws"), ws.numel(), 2000, api._stream(None))
+    assert st == 0
+    assert api.ws_matvec_status(ws) == api.DSPARK_ERR_TIMEOUT
+    assert "timed out" in lib.dspark_last_error().decode()
+    assert api.ws_matvec_status(ws) == 0  # reported once
+    y2 = api.ws_matvec(W, X, out_fp32=True, workspace=ws)
+    assert api.ws_matvec_status(ws) == 0
+    parity.check_ws(inp, y32=y2.cpu().numpy())
+    assert int(ws[:65536 + 256].count_nonzero()) == 0

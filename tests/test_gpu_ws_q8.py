@@ -119,4 +119,22 @@ def test_shared_workspace_across_shapes_and_repeats():
             y = api.ws_matvec_q8(q, d, X, out_fp32=True, workspace=ws)
             torch.cuda.synchronize()
             parity.check_ws_q8(inp, y32=y.cpu().numpy())
-    assert int(ws[:65536].count_nonzero()) == 0
+    assert int(ws[:65536 + 256].count_nonzero()) == 0
+
+
+def test_workspace_status_reports_a_wait_that_gave_up():
+    """As for the fp16 matvec: a debug launch whose epilogue first waits 2 ms on a barrier
+    nothing signals records a timeout, reports it once and leaves the context usable."""
+    inp = synth.ws_q8_inputs(7, 1024, 4096, seed=12)
+    q, d, X = _dev(inp)
+    ws = api.new_ws_q8_workspace(7, 1024, 4096)
+    y = torch.empty((7, 1024), dtype=torch.float32, device="cuda")
+    lib = api.load_library()
+    st = lib.dspark_ws_matvec_q8_debug(api._ptr(q, "q"), api._ptr(d, "d"), api._ptr(X, "X"), api._ptr(y, "y"), 1,
+                                       7, 1024, 4096, api._ptr(ws, "ws"), ws.numel(), 2000, api._stream(None))
+    assert st == 0
+    assert api.ws_matvec_status(ws) == api.DSPARK_ERR_TIMEOUT
+    assert api.ws_matvec_status(ws) == 0
+    y2 = api.ws_matvec_q8(q, d, X, out_fp32=True, workspace=ws)
+    assert api.ws_matvec_status(ws) == 0
+    parity.check_ws_q8(inp, y32=y2.cpu().numpy())
