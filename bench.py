@@ -6,13 +6,13 @@ One step = one pass of the whole hot path over one batch of synthetic input:
      rank 256, bf16 markov weights, fp32 base logits, identity d2t) -- one graph launch
   2. 2048 confidence probes (2 per cycle x 1024 cycles), 7424-wide Q8_0, threshold 0.5
   3. the four M=7 fp16 weight-stationary projections of a Qwen3-8B-shaped draft
-     (K,N) = (4096,4096), (4096,1024), (4096,12288), (12288,4096)
+     (K,N) = (4096,4096), (4096,1024), (4096,12288), (12288,4096), as one grouped launch
 
 value = microseconds per step (lower is better), device time from CUDA events around
 each step's work; L2 is flushed before every step (256 MiB write, then a read of the
 buffer so the write-back of dirty lines is not charged to the step), outside the events.
-`e2e` times the same step through the public API with the step's inputs copied from
-pinned host memory and its outputs copied back, inside the events.  `roofline` is for
+`e2e` times the same step through the C ABI's host-buffer forms: the step's inputs copied
+from pinned host memory and its outputs copied back, inside the events.  `roofline` is for
 the Markov kernel (the dominant one): algorithmic bytes per launch / mean launch time.
 
 --impl reference times the CPU oracle on the host (the reference arm of this method).
@@ -84,7 +84,7 @@ def config_dict(B):
                      f"vocab={V}, rank={R}, bf16 markov_w1/w2, fp32 base, identity d2t) + "
                      f"{N_PROBES} Q8_0 confidence probes (K=7424, threshold 0.5) + 4 M=7 fp16 "
                      "weight-stationary matvecs (K,N)=(4096,4096),(4096,1024),(4096,12288),"
-                     "(12288,4096)"),
+                     "(12288,4096) in one grouped launch"),
         "num_reqs": B, "k": k, "vocab": V, "rank": R, "probes": N_PROBES, "probe_K": 7424,
         "ws_M": 7, "ws_shapes_KN": [list(s) for s in synth.WS_SHAPES],
         "l2": ("flushed before every step: 256 MiB write then a read of the same buffer, "
@@ -226,6 +226,8 @@ def run_gpu(args, rank, world):
     Xs = [torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16) for w in ws]
     Ys = [torch.empty((7, w["N"]), dtype=torch.float16, device=dev) for w in ws]
     WSs = [api.new_ws_workspace(7, w["N"], w["K"], dev) for w in ws]
+    ws_group = list(zip(Ws, Xs, Ys))  # the four projections as one grouped launch
+    ws_group_ws = torch.zeros(api.ws_matvec_grouped_workspace_bytes(ws_group), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_sink = torch.empty((), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -241,10 +243,9 @@ def run_gpu(args, rank, world):
         plan.launch(stream)
         api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
                        stream=stream)
-        for W, X, Y, WS in zip(Ws, Xs, Ys, WSs):
-            api.ws_matvec(W, X, out=Y, workspace=WS, stream=stream)
+        api.ws_matvec_grouped(ws_group, workspace=ws_group_ws, stream=stream)
 
-    kernels_per_step = 1 + 1 + len(Ws)
+    kernels_per_step = 3  # Markov draft, probe batch, grouped WS matvec
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     for _ in range(args.warmup):
@@ -274,8 +275,7 @@ def run_gpu(args, rank, world):
         api.conf_probe(wq, hid, pr["bias"], pr["threshold"], logit_out=z, gate_out=gate,
                        stream=stream)
         e[2].record(stream)
-        for W, X, Y, WS in zip(Ws, Xs, Ys, WSs):
-            api.ws_matvec(W, X, out=Y, workspace=WS, stream=stream)
+        api.ws_matvec_grouped(ws_group, workspace=ws_group_ws, stream=stream)
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -675,7 +675,7 @@ def main():
             "conf_probe_batch_us": res["probe_ms"] * 1000.0,
             "conf_probe_us_per_probe": res["probe_ms"] * 1000.0 / N_PROBES,
             "conf_probe_GBps": pb / (res["probe_ms"] * 1e-3) / 1e9,
-            "ws_matvec_4_shapes_us": res["ws_ms"] * 1000.0,
+            "ws_matvec_4_shapes_grouped_us": res["ws_ms"] * 1000.0,
             "ws_matvec_GBps": wb / (res["ws_ms"] * 1e-3) / 1e9,
         },
         "gpu_launches": res["kernels"],

@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     markov_workspace_bytes,
     q8_0_repack,
     ws_matvec,
+    ws_matvec_grouped,
     ws_matvec_host,
     ws_matvec_q8,
     ws_matvec_q8_workspace_bytes,

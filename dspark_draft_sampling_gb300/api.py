@@ -47,6 +47,8 @@ SIGNATURES = {
     "dspark_ws_matvec_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "dspark_ws_matvec_status": (_I, [_P, _P]),
+    "dspark_ws_matvec_grouped_workspace_bytes": (_Z, [_P, _I]),
+    "dspark_ws_matvec_grouped": (_I, [_P, _I, _P, _Z, _P]),
     "dspark_ws_matvec_debug": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _U, _P]),
     "dspark_ws_matvec_q8_debug": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _U, _P]),
     "dspark_q8_0_repack": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -555,3 +557,43 @@ def ws_matvec_status(workspace, *, stream=None) -> int:
     DSPARK_ERR_TIMEOUT (reported once, then cleared)."""
     lib = load_library()
     return int(lib.dspark_ws_matvec_status(_ptr(workspace, "workspace"), _stream(stream)))
+
+
+class WsProblem(ctypes.Structure):
+    """Mirror of dspark_ws_problem."""
+    _fields_ = [("W", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("y_is_fp32", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+def _ws_problems(problems):
+    arr = (WsProblem * len(problems))()
+    for i, (W, X, Y) in enumerate(problems):
+        N, K = W.shape
+        M, K2 = X.shape
+        if K != K2 or tuple(Y.shape) != (M, N):
+            raise ValueError(f"problem {i}: W [N,K], X [M,K] and Y [M,N] disagree")
+        arr[i] = WsProblem(_ptr(W, "W", itemsize=2, dtypes=_BITS16), _ptr(X, "X", itemsize=2, dtypes=_BITS16),
+                           _ptr(Y, "Y", dtypes=(torch.float16, torch.float32)),
+                           1 if Y.dtype == torch.float32 else 0, M, N, K)
+    return arr
+
+
+def ws_matvec_grouped_workspace_bytes(problems) -> int:
+    arr = _ws_problems(problems)
+    return int(load_library().dspark_ws_matvec_grouped_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(arr)))
+
+
+def ws_matvec_grouped(problems, *, workspace=None, stream=None):
+    """Several independent Y = X W^T in one launch.  problems: list of (W [N,K] fp16,
+    X [M,K] fp16, Y [M,N] fp16 or fp32) device tensors; Y is written in place."""
+    lib = load_library()
+    arr = _ws_problems(problems)
+    if workspace is None:
+        n = int(lib.dspark_ws_matvec_grouped_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(arr)))
+        if n == 0:
+            raise DsparkError(DSPARK_ERR_CUDA, "could not size the grouped ws_matvec workspace")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=problems[0][0].device)
+    st = lib.dspark_ws_matvec_grouped(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(workspace, "workspace"),
+                                      workspace.numel(), _stream(stream))
+    _check(lib, st)
+    return [Y for (_, _, Y) in problems]

@@ -43,22 +43,34 @@ constexpr int kStageBytes = kABytes + kBBytes;   // 18 KB (multiple of 1024)
 constexpr uint32_t kTmemCols = 32;
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 256;
 
-struct WsArgs {
+constexpr int kMaxProblems = 8;
+
+struct WsProblem {
     void *Y;
     float *partial;     // [units][128][16] fp32 (split-K only)
     unsigned *tickets;  // [row blocks]
     int y_fp32;
     int M, N, K;
-    int nkb;  // k-blocks
-    int S;    // units per row block
+    int nkb;    // k-blocks
+    int S;      // units per row block
+    int unit0;  // first CTA of this problem in the grid
+};
+
+// Kernel parameters: up to kMaxProblems independent problems share one launch, CTA b taking
+// unit b - unit0 of the problem whose range holds it.  The tensor maps stay in parameter
+// space (__grid_constant__), where TMA reads them.
+struct WsGroup {
+    CUtensorMap tmW[kMaxProblems];
+    CUtensorMap tmX[kMaxProblems];
+    WsProblem prob[kMaxProblems];
+    int nprob;
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
                                   // this long on a barrier that nothing signals
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-    ws_matvec_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, WsArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_constant__ WsGroup g) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-aligned tiles
@@ -71,7 +83,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int unit = blockIdx.x;
+    int pi = 0;
+    while (pi + 1 < g.nprob && static_cast<int>(blockIdx.x) >= g.prob[pi + 1].unit0) ++pi;
+    const WsProblem &a = g.prob[pi];
+    const CUtensorMap *tmW = &g.tmW[pi];
+    const CUtensorMap *tmX = &g.tmX[pi];
+    const int unit = static_cast<int>(blockIdx.x) - a.unit0;
     const int rb = unit / a.S;
     const int sk = unit % a.S;
     const int kb0 = static_cast<int>(static_cast<long long>(sk) * a.nkb / a.S);
@@ -104,14 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                if (!mbar_wait(&empty[st], ph ^ 1u, a.timeout_ns)) {
-                    atomicOr(a.status, kWsStatusTimeout);
+                if (!mbar_wait(&empty[st], ph ^ 1u, g.timeout_ns)) {
+                    atomicOr(g.status, kWsStatusTimeout);
                     break;
                 }
                 unsigned char *sa = smem + size_t(st) * kStageBytes;
                 mbar_arrive_expect_tx(&full[st], kStageBytes);
-                tma_load_2d(sa, &tmW, (kb0 + j) * kKB, n0, &full[st], pol_w);
-                tma_load_2d(sa + kABytes, &tmX, (kb0 + j) * kKB, 0, &full[st], pol_x);
+                tma_load_2d(sa, tmW, (kb0 + j) * kKB, n0, &full[st], pol_w);
+                tma_load_2d(sa + kABytes, tmX, (kb0 + j) * kKB, 0, &full[st], pol_x);
                 if (++st == kStages) {
                     st = 0;
                     ph ^= 1u;
@@ -127,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             for (int j = 0; j < nk; ++j) {
-                if (!mbar_wait(&full[st], ph, a.timeout_ns)) {
-                    atomicOr(a.status, kWsStatusTimeout);
+                if (!mbar_wait(&full[st], ph, g.timeout_ns)) {
+                    atomicOr(g.status, kWsStatusTimeout);
                     break;
                 }
                 tc_fence_after();
@@ -148,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 ----
-        if (a.stall_ns && !mbar_wait(never, 0, a.stall_ns) && threadIdx.x == 0) atomicOr(a.status, kWsStatusTimeout);
-        const bool ok = mbar_wait(done, 0, a.timeout_ns);
-        if (!ok) atomicOr(a.status, kWsStatusTimeout);
+        if (g.stall_ns && !mbar_wait(never, 0, g.stall_ns) && threadIdx.x == 0) atomicOr(g.status, kWsStatusTimeout);
+        const bool ok = mbar_wait(done, 0, g.timeout_ns);
+        if (!ok) atomicOr(g.status, kWsStatusTimeout);
         tc_fence_after();
         uint32_t v[16];
         tmem_ld_16(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
@@ -278,52 +295,98 @@ extern "C" size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K) {
 
 namespace {
 
-dspark_status ws_enqueue(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N, int K,
-                         void *workspace, size_t workspace_bytes, unsigned long long stall_ns, dspark_stream_t stream) {
+// Checks one problem; returns DSPARK_OK with *skip set when it has nothing to do.
+dspark_status check_problem(const dspark_ws_problem &q, bool *skip) {
+    using namespace dspark;
+    *skip = false;
+    if (q.M < 0 || q.N < 0 || q.K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec: negative size");
+    if (q.M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: M=%d > 16", q.M);
+    if (q.K < 8 || (q.K % 8) != 0) return fail(DSPARK_ERR_INVALID, "ws_matvec: K=%d must be a positive multiple of 8", q.K);
+    if (q.M == 0 || q.N == 0) {
+        *skip = true;
+        return DSPARK_OK;
+    }
+    if (!q.W || !q.X || !q.Y) return fail(DSPARK_ERR_INVALID, "ws_matvec: null pointer argument");
+    if (!aligned(q.W, 16) || !aligned(q.X, 16)) return fail(DSPARK_ERR_INVALID, "ws_matvec: W and X must be 16-byte aligned");
+    if (!aligned(q.Y, q.y_is_fp32 ? 4 : 2)) return fail(DSPARK_ERR_INVALID, "ws_matvec: misaligned Y");
+    return DSPARK_OK;
+}
+
+// Workspace of a group: header, one ticket area (the problems' row blocks one after the
+// other), then each split problem's partial tiles.  0 when the sizes are invalid.
+size_t group_workspace_bytes(const dspark_ws_problem *probs, int n, int sms) {
+    using namespace dspark;
+    size_t bytes = dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
+    for (int i = 0; i < n; ++i) {
+        if (probs[i].N <= 0 || probs[i].K <= 0 || probs[i].M <= 0) continue;
+        const Plan p = plan_for(probs[i].N, probs[i].K, sms);
+        if (p.S > 1) bytes += size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
+    }
+    return bytes;
+}
+
+dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *workspace, size_t workspace_bytes,
+                               unsigned long long stall_ns, dspark_stream_t stream) {
     using namespace dspark;
     clear_error();
-    if (M < 0 || N < 0 || K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec: negative size");
-    if (M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: M=%d > 16", M);
-    if (K < 8 || (K % 8) != 0) return fail(DSPARK_ERR_INVALID, "ws_matvec: K=%d must be a positive multiple of 8", K);
-    if (M == 0 || N == 0) return DSPARK_OK;  // nothing to enqueue
-    if (!W || !X || !Y || !workspace) return fail(DSPARK_ERR_INVALID, "ws_matvec: null pointer argument");
-    if (!aligned(W, 16) || !aligned(X, 16)) return fail(DSPARK_ERR_INVALID, "ws_matvec: W and X must be 16-byte aligned");
-    if (!aligned(Y, y_is_fp32 ? 4 : 2)) return fail(DSPARK_ERR_INVALID, "ws_matvec: misaligned Y");
+    if (n < 0 || n > kMaxProblems) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: %d problems (at most %d)", n, kMaxProblems);
+    if (n > 0 && !probs) return fail(DSPARK_ERR_INVALID, "ws_matvec: null problem array");
+    int live = 0;
+    for (int i = 0; i < n; ++i) {
+        bool skip = false;
+        const dspark_status st = check_problem(probs[i], &skip);
+        if (st != DSPARK_OK) return st;
+        live += skip ? 0 : 1;
+    }
+    if (live == 0) return DSPARK_OK;  // nothing to enqueue
+    if (!workspace) return fail(DSPARK_ERR_INVALID, "ws_matvec: null workspace");
     if (!aligned(workspace, 256)) return fail(DSPARK_ERR_INVALID, "ws_matvec: workspace must be 256-byte aligned");
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
-    const Plan p = plan_for(N, K, sms);
-    if (size_t(p.nrb) * sizeof(unsigned) > kWsTicketBytes)
-        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: N=%d exceeds %zu rows", N, kWsTicketBytes / 4 * kRowsPerUnit);
-    const size_t need = workspace_bytes_for(p);
+    const size_t need = group_workspace_bytes(probs, n, sms);
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec: workspace of %zu bytes < required %zu", workspace_bytes, need);
 
-    CUtensorMap tmW, tmX;
-    dspark_status st = make_tmap_2d(&tmW, W, false, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRowsPerUnit, kKB);
-    if (st != DSPARK_OK) return st;
-    st = make_tmap_2d(&tmX, X, false, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, kKB);
-    if (st != DSPARK_OK) return st;
-
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    WsArgs args;
-    args.Y = Y;
-    args.y_fp32 = y_is_fp32 ? 1 : 0;
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.nkb = p.nkb;
-    args.S = p.S;
-    args.timeout_ns = kDefaultTimeoutNs;
-    args.partial = nullptr;
-    args.tickets = nullptr;
-    args.status = static_cast<unsigned *>(workspace);
-    args.stall_ns = stall_ns;
-    if (p.S > 1) {
-        unsigned char *ws = static_cast<unsigned char *>(workspace);
-        args.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes);
-        args.partial = reinterpret_cast<float *>(ws + kWsHeaderBytes + kWsTicketBytes);
+    WsGroup g;
+    g.nprob = 0;
+    g.status = static_cast<unsigned *>(workspace);
+    g.timeout_ns = kDefaultTimeoutNs;
+    g.stall_ns = stall_ns;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    size_t ticket_off = 0;  // in row blocks
+    size_t partial_off = kWsHeaderBytes + kWsTicketBytes;
+    unsigned units = 0;
+    for (int i = 0; i < n; ++i) {
+        const dspark_ws_problem &q = probs[i];
+        if (q.M == 0 || q.N == 0) continue;
+        const Plan p = plan_for(q.N, q.K, sms);
+        if ((ticket_off + p.nrb) * sizeof(unsigned) > kWsTicketBytes)
+            return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: more than %zu rows in one call", kWsTicketBytes / 4 * kRowsPerUnit);
+        const int j = g.nprob++;
+        dspark_status st = make_tmap_2d(&g.tmW[j], q.W, false, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K),
+                                        kRowsPerUnit, kKB);
+        if (st != DSPARK_OK) return st;
+        st = make_tmap_2d(&g.tmX[j], q.X, false, static_cast<uint64_t>(q.M), static_cast<uint64_t>(q.K), kNPad, kKB);
+        if (st != DSPARK_OK) return st;
+        WsProblem &a = g.prob[j];
+        a.Y = q.Y;
+        a.y_fp32 = q.y_is_fp32 ? 1 : 0;
+        a.M = q.M;
+        a.N = q.N;
+        a.K = q.K;
+        a.nkb = p.nkb;
+        a.S = p.S;
+        a.unit0 = static_cast<int>(units);
+        a.tickets = nullptr;
+        a.partial = nullptr;
+        if (p.S > 1) {
+            a.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes) + ticket_off;
+            a.partial = reinterpret_cast<float *>(ws + partial_off);
+            ticket_off += p.nrb;
+            partial_off += size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
+        }
+        units += static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
     }
 
     static int configured_dev = -1;
@@ -339,10 +402,16 @@ dspark_status ws_enqueue(const uint16_t *W, const uint16_t *X, void *Y, int y_is
         if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
         configured_dev = dev;
     }
-    const unsigned units = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
-    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), kSmemBytes, s, tmW, tmX, args);
+    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), kSmemBytes,
+                               reinterpret_cast<cudaStream_t>(stream), g);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;
+}
+
+dspark_status ws_enqueue(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N, int K,
+                         void *workspace, size_t workspace_bytes, unsigned long long stall_ns, dspark_stream_t stream) {
+    const dspark_ws_problem q = {W, X, Y, y_is_fp32, M, N, K};
+    return ws_enqueue_group(&q, 1, workspace, workspace_bytes, stall_ns, stream);
 }
 
 }  // namespace
@@ -350,6 +419,18 @@ dspark_status ws_enqueue(const uint16_t *W, const uint16_t *X, void *Y, int y_is
 extern "C" dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
                                           int K, void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
     return ws_enqueue(W, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 0ull, stream);
+}
+
+extern "C" size_t dspark_ws_matvec_grouped_workspace_bytes(const dspark_ws_problem *problems, int n_problems) {
+    if (n_problems < 0 || (n_problems > 0 && !problems)) return 0;
+    int sms = 0;
+    if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
+    return group_workspace_bytes(problems, n_problems, sms);
+}
+
+extern "C" dspark_status dspark_ws_matvec_grouped(const dspark_ws_problem *problems, int n_problems, void *workspace,
+                                                  size_t workspace_bytes, dspark_stream_t stream) {
+    return ws_enqueue_group(problems, n_problems, workspace, workspace_bytes, 0ull, stream);
 }
 
 extern "C" dspark_status dspark_ws_matvec_debug(const uint16_t *W, const uint16_t *X, void *Y, int y_is_fp32, int M,

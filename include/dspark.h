@@ -220,6 +220,28 @@ dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, in
                                int M, int N, int K, void *workspace, size_t workspace_bytes,
                                dspark_stream_t stream);
 
+/* Grouped form: up to 8 independent problems (e.g. the q, k and v projections of a layer,
+ * or gate and up) in one launch, so their fixed launch and pipeline costs are paid once and
+ * the SMs left idle by one problem's tail take the next one's units.  Each problem has the
+ * arguments and limits of dspark_ws_matvec; its results are bit-identical to a separate
+ * dspark_ws_matvec call.  Problems with M == 0 or N == 0 are skipped.  The workspace
+ * (dspark_ws_matvec_grouped_workspace_bytes(problems, n), zero-filled before first use, left
+ * zero-filled) is laid out like dspark_ws_matvec's, with the problems' tickets and partial
+ * tiles one after the other; at most 16384 row blocks of 128 rows in one call.
+ * More than 8 problems: DSPARK_ERR_UNSUPPORTED. */
+typedef struct dspark_ws_problem {
+    const uint16_t *W;  /* fp16 [N, K] */
+    const uint16_t *X;  /* fp16 [M, K] */
+    void *Y;            /* [M, N], fp32 if y_is_fp32 else fp16 */
+    int y_is_fp32;
+    int M, N, K;
+} dspark_ws_problem;
+
+size_t dspark_ws_matvec_grouped_workspace_bytes(const dspark_ws_problem *problems, int n_problems);
+dspark_status dspark_ws_matvec_grouped(const dspark_ws_problem *problems, int n_problems,
+                                       void *workspace, size_t workspace_bytes,
+                                       dspark_stream_t stream);
+
 /* Synchronizes `stream`, then reads the status word of a dspark_ws_matvec or
  * dspark_ws_matvec_q8 workspace (its first 4 bytes): DSPARK_OK, or DSPARK_ERR_TIMEOUT if a
  * device-side wait of a call on it gave up since the last check (the kernel then skipped

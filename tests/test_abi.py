@@ -246,3 +246,24 @@ def test_ws_status_and_debug_validation(dspark_lib):
     assert lib.dspark_ws_matvec_debug(NULL, FAKE, FAKE, 0, 7, 64, 64, FAKE, 1 << 20, 100, NULL) == INVALID
     assert lib.dspark_ws_matvec_q8_debug(FAKE, FAKE, FAKE, FAKE, 0, 7, 64, 256, FAKE, 1 << 20, 0, NULL) == INVALID
     assert lib.dspark_ws_matvec_q8_debug(FAKE, FAKE, FAKE, FAKE, 0, 17, 64, 256, FAKE, 1 << 20, 100, NULL) == UNSUPPORTED
+
+
+def test_ws_grouped_validation(dspark_lib):
+    lib = dspark_lib
+    arr = (api.WsProblem * 9)()
+    for i in range(9):
+        arr[i] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 64)
+    g = lib.dspark_ws_matvec_grouped
+    p = ctypes.cast(arr, ctypes.c_void_p)
+    assert g(p, 9, FAKE, 1 << 20, NULL) == UNSUPPORTED
+    assert g(NULL, 2, FAKE, 1 << 20, NULL) == INVALID
+    assert g(p, 0, NULL, 0, NULL) == 0
+    arr[1] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 17, 64, 64)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == UNSUPPORTED
+    arr[1] = api.WsProblem(FAKE.value, None, FAKE.value, 0, 7, 64, 64)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == INVALID
+    arr[0] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 0, 64, 64)
+    arr[1] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 7, 0, 64)
+    assert g(p, 2, NULL, 0, NULL) == 0  # every problem empty: nothing to enqueue
+    arr[0] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 64)
+    assert g(p, 1, NULL, 1 << 20, NULL) == INVALID

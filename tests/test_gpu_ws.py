@@ -108,3 +108,49 @@ def test_workspace_status_reports_a_wait_that_gave_up():
     assert api.ws_matvec_status(ws) == 0
     parity.check_ws(inp, y32=y2.cpu().numpy())
     assert int(ws[:65536 + 256].count_nonzero()) == 0
+
+
+def _problems(shapes, seed, fp32):
+    probs, inps = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        inp = synth.ws_inputs(M, N, K, seed=seed + i)
+        W, X = _dev(inp)
+        Y = torch.empty((M, N), dtype=torch.float32 if fp32 else torch.float16, device="cuda")
+        probs.append((W, X, Y))
+        inps.append(inp)
+    return probs, inps
+
+
+@pytest.mark.parametrize("shapes", [
+    [(7, N, K) for (K, N) in synth.WS_SHAPES],
+    [(3, 100, 64), (16, 777, 4096), (1, 1, 8), (9, 4099, 2056), (7, 12288, 4096)],
+])
+def test_grouped_matches_separate_calls_bitwise(shapes):
+    for fp32 in (True, False):
+        probs, inps = _problems(shapes, seed=50, fp32=fp32)
+        api.ws_matvec_grouped(probs)
+        torch.cuda.synchronize()
+        for (W, X, Y), inp in zip(probs, inps):
+            ref = api.ws_matvec(W, X, out_fp32=fp32)
+            torch.cuda.synchronize()
+            view = torch.int32 if fp32 else torch.int16
+            assert torch.equal(Y.view(view), ref.view(view))
+            if fp32:
+                parity.check_ws(inp, y32=Y.cpu().numpy())
+
+
+def test_grouped_workspace_reuse_and_empty_problems():
+    shapes = [(7, N, K) for (K, N) in synth.WS_SHAPES]
+    probs, inps = _problems(shapes, seed=60, fp32=True)
+    empty = (probs[0][0], probs[0][1][:0], torch.empty((0, probs[0][0].shape[0]), dtype=torch.float32, device="cuda"))
+    group = probs[:2] + [empty] + probs[2:]
+    ws = torch.zeros(api.ws_matvec_grouped_workspace_bytes(group), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        for (_, _, Y) in probs:
+            Y.zero_()
+        api.ws_matvec_grouped(group, workspace=ws)
+        torch.cuda.synchronize()
+        for (W, X, Y), inp in zip(probs, inps):
+            parity.check_ws(inp, y32=Y.cpu().numpy())
+    assert api.ws_matvec_status(ws) == 0
+    assert int(ws[:65536 + 256].count_nonzero()) == 0
