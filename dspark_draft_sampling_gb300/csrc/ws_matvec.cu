@@ -357,9 +357,25 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
     size_t ticket_off = 0;  // in row blocks
     size_t partial_off = kWsHeaderBytes + kWsTicketBytes;
     unsigned units = 0;
-    for (int i = 0; i < n; ++i) {
-        const dspark_ws_problem &q = probs[i];
-        if (q.M == 0 || q.N == 0) continue;
+    // The grid takes the problems with the longest units first (longest-processing-time
+    // order), so the last wave holds short units and the tail stays short.  The order changes
+    // no result: every problem keeps its own split and summation order.
+    int order[kMaxProblems];
+    int norder = 0;
+    for (int i = 0; i < n; ++i)
+        if (probs[i].M != 0 && probs[i].N != 0) order[norder++] = i;
+    auto unit_blocks = [&](int i) {
+        const Plan p = plan_for(probs[i].N, probs[i].K, sms);
+        return (p.nkb + p.S - 1) / p.S;
+    };
+    for (int a = 1; a < norder; ++a)  // stable insertion sort, longest units first
+        for (int b = a; b > 0 && unit_blocks(order[b]) > unit_blocks(order[b - 1]); --b) {
+            const int t = order[b];
+            order[b] = order[b - 1];
+            order[b - 1] = t;
+        }
+    for (int oi = 0; oi < norder; ++oi) {
+        const dspark_ws_problem &q = probs[order[oi]];
         const Plan p = plan_for(q.N, q.K, sms);
         if ((ticket_off + p.nrb) * sizeof(unsigned) > kWsTicketBytes)
             return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: more than %zu rows in one call", kWsTicketBytes / 4 * kRowsPerUnit);
