@@ -58,6 +58,8 @@ SIGNATURES = {
     "dspark_conf_probe_host": (_I, [_P, _P, _F, _F, _I, _I, _P, _P, _P, _Z, _P, _P]),
     "dspark_ws_matvec_host_scratch_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec_host": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P, _P]),
+    "dspark_ws_matvec_grouped_host_scratch_bytes": (_Z, [_P, _I]),
+    "dspark_ws_matvec_grouped_host": (_I, [_P, _I, _P, _Z, _P, _P]),
     "dspark_ws_matvec_q8_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec_q8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
 }
@@ -499,7 +501,16 @@ def ws_matvec_host_scratch_bytes(M: int, N: int, K: int) -> int:
 
 
 def _event(ev):
-    return None if ev is None else ctypes.c_void_p(ev.cuda_event)
+    """Raw handle of a torch.cuda.Event.  torch creates the CUDA event on its first record, so
+    an event that was never recorded is recorded once here to create it (the library then
+    records it again where it belongs)."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record(torch.cuda.current_stream())
+    if not ev.cuda_event:
+        raise DsparkError(DSPARK_ERR_CUDA, "could not create the CUDA event")
+    return ctypes.c_void_p(ev.cuda_event)
 
 
 def markov_draft_host(base_h, w1, w2, d2t, prev_h, out_ids_h, scratch, *, inputs_copied=None,
@@ -595,5 +606,36 @@ def ws_matvec_grouped(problems, *, workspace=None, stream=None):
         workspace = torch.zeros(n, dtype=torch.uint8, device=problems[0][0].device)
     st = lib.dspark_ws_matvec_grouped(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(workspace, "workspace"),
                                       workspace.numel(), _stream(stream))
+    _check(lib, st)
+    return [Y for (_, _, Y) in problems]
+
+
+def _ws_problems_host(problems):
+    arr = (WsProblem * len(problems))()
+    for i, (W, X_h, Y_h) in enumerate(problems):
+        N, K = W.shape
+        M, K2 = X_h.shape
+        if K != K2 or tuple(Y_h.shape) != (M, N):
+            raise ValueError(f"problem {i}: W [N,K], X [M,K] and Y [M,N] disagree")
+        arr[i] = WsProblem(_ptr(W, "W", itemsize=2, dtypes=_BITS16), _host_ptr(X_h, "X_h", itemsize=2, dtypes=_BITS16),
+                           _host_ptr(Y_h, "Y_h", dtypes=(torch.float16, torch.float32)),
+                           1 if Y_h.dtype == torch.float32 else 0, M, N, K)
+    return arr
+
+
+def ws_matvec_grouped_host_scratch_bytes(problems) -> int:
+    arr = _ws_problems_host(problems)
+    return int(load_library().dspark_ws_matvec_grouped_host_scratch_bytes(ctypes.cast(arr, ctypes.c_void_p),
+                                                                          len(arr)))
+
+
+def ws_matvec_grouped_host(problems, scratch, *, inputs_copied=None, stream=None):
+    """Grouped matvec from host buffers: problems = list of (W device [N,K], X_h host [M,K],
+    Y_h host [M,N]); `scratch` zero-filled before first use."""
+    lib = load_library()
+    arr = _ws_problems_host(problems)
+    st = lib.dspark_ws_matvec_grouped_host(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(scratch, "scratch"),
+                                           scratch.numel() * scratch.element_size(), _event(inputs_copied),
+                                           _stream(stream))
     _check(lib, st)
     return [Y for (_, _, Y) in problems]

@@ -160,3 +160,74 @@ extern "C" dspark_status dspark_ws_matvec_host(const uint16_t *W, const uint16_t
     if (st == DSPARK_OK) st = copy(Y_host, y_d, ybytes, cudaMemcpyDeviceToHost, s, "ws_matvec_host: Y copy");
     return st;
 }
+
+extern "C" size_t dspark_ws_matvec_grouped_host_scratch_bytes(const dspark_ws_problem *problems, int n_problems) {
+    if (n_problems < 0 || (n_problems > 0 && !problems)) return 0;
+    const size_t ws = dspark_ws_matvec_grouped_workspace_bytes(problems, n_problems);
+    if (ws == 0) return 0;
+    size_t bytes = up256(ws);
+    for (int i = 0; i < n_problems; ++i) {
+        const dspark_ws_problem &q = problems[i];
+        if (q.M <= 0 || q.N <= 0 || q.K <= 0) continue;
+        bytes += up256(static_cast<size_t>(q.M) * q.K * 2) + up256(static_cast<size_t>(q.M) * q.N * 4);
+    }
+    return bytes;
+}
+
+extern "C" dspark_status dspark_ws_matvec_grouped_host(const dspark_ws_problem *problems, int n_problems,
+                                                       void *device_scratch, size_t scratch_bytes,
+                                                       void *inputs_copied, dspark_stream_t stream) {
+    using namespace dspark;
+    clear_error();
+    if (n_problems < 0 || n_problems > 8)
+        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_grouped_host: %d problems (at most 8)", n_problems);
+    if (n_problems > 0 && !problems) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: null problem array");
+    int live = 0;
+    for (int i = 0; i < n_problems; ++i) {
+        const dspark_ws_problem &q = problems[i];
+        if (q.M < 0 || q.N < 0 || q.K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: negative size");
+        if (q.M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_grouped_host: M=%d > 16", q.M);
+        if (q.K < 8 || (q.K % 8) != 0)
+            return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: K=%d must be a positive multiple of 8", q.K);
+        if (q.M == 0 || q.N == 0) continue;
+        if (!q.W || !q.X || !q.Y) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: null pointer argument");
+        if (!aligned(q.W, 16)) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: W must be 16-byte aligned");
+        ++live;
+    }
+    if (live == 0) return DSPARK_OK;
+    if (!device_scratch) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: null scratch");
+    if (!aligned(device_scratch, 256)) return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: scratch must be 256-byte aligned");
+    const size_t need = dspark_ws_matvec_grouped_host_scratch_bytes(problems, n_problems);
+    if (need == 0) return fail(DSPARK_ERR_CUDA, "ws_matvec_grouped_host: could not size the scratch");
+    if (scratch_bytes < need)
+        return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: scratch of %zu bytes < required %zu", scratch_bytes, need);
+    // the grouped workspace first (its zero-filled ticket area at offset 0), then per problem
+    // the device copies of X and Y
+    const size_t ws = dspark_ws_matvec_grouped_workspace_bytes(problems, n_problems);
+    unsigned char *p = static_cast<unsigned char *>(device_scratch) + up256(ws);
+    dspark_ws_problem dev[8];
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dspark_status st = DSPARK_OK;
+    for (int i = 0; i < n_problems; ++i) {
+        dev[i] = problems[i];
+        const dspark_ws_problem &q = problems[i];
+        if (q.M == 0 || q.N == 0) continue;
+        const size_t xb = static_cast<size_t>(q.M) * q.K * 2;
+        dev[i].X = reinterpret_cast<const uint16_t *>(p);
+        p += up256(xb);
+        dev[i].Y = p;
+        p += up256(static_cast<size_t>(q.M) * q.N * 4);
+        if (st == DSPARK_OK) st = copy(const_cast<uint16_t *>(dev[i].X), q.X, xb, cudaMemcpyHostToDevice, s,
+                                       "ws_matvec_grouped_host: X copy");
+    }
+    if (st == DSPARK_OK) st = mark_copied(inputs_copied, s);
+    if (st == DSPARK_OK) st = dspark_ws_matvec_grouped(dev, n_problems, device_scratch, ws, stream);
+    for (int i = 0; i < n_problems && st == DSPARK_OK; ++i) {
+        const dspark_ws_problem &q = problems[i];
+        if (q.M == 0 || q.N == 0) continue;
+        st = copy(q.Y, dev[i].Y, static_cast<size_t>(q.M) * q.N * (q.y_is_fp32 ? 4 : 2), cudaMemcpyDeviceToHost, s,
+                  "ws_matvec_grouped_host: Y copy");
+    }
+    return st;
+}
+

@@ -351,6 +351,17 @@ dspark_status dspark_ws_matvec_host(const uint16_t *W, const uint16_t *X_host, v
                                     size_t scratch_bytes, void *inputs_copied,
                                     dspark_stream_t stream);
 
+/* Grouped host-buffer form of dspark_ws_matvec_grouped: in `problems`, W is a device pointer
+ * and X / Y are HOST pointers.  All X copies are enqueued first (then inputs_copied is
+ * recorded), then the one grouped launch, then the Y copies.  Scratch: at least
+ * dspark_ws_matvec_grouped_host_scratch_bytes(problems, n), 256-byte aligned, zero-filled
+ * before first use (its first part is the grouped workspace). */
+size_t dspark_ws_matvec_grouped_host_scratch_bytes(const dspark_ws_problem *problems,
+                                                   int n_problems);
+dspark_status dspark_ws_matvec_grouped_host(const dspark_ws_problem *problems, int n_problems,
+                                            void *device_scratch, size_t scratch_bytes,
+                                            void *inputs_copied, dspark_stream_t stream);
+
 /* =====================================================================================
  * Draft step with device-side base logits
  *

@@ -267,3 +267,18 @@ def test_ws_grouped_validation(dspark_lib):
     assert g(p, 2, NULL, 0, NULL) == 0  # every problem empty: nothing to enqueue
     arr[0] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 64)
     assert g(p, 1, NULL, 1 << 20, NULL) == INVALID
+
+
+def test_ws_grouped_host_validation(dspark_lib):
+    lib = dspark_lib
+    arr = (api.WsProblem * 2)()
+    arr[0] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 64)
+    arr[1] = api.WsProblem(FAKE.value, FAKE.value, FAKE.value, 0, 17, 64, 64)
+    g = lib.dspark_ws_matvec_grouped_host
+    p = ctypes.cast(arr, ctypes.c_void_p)
+    assert g(p, 9, FAKE, 1 << 20, NULL, NULL) == UNSUPPORTED
+    assert g(NULL, 1, FAKE, 1 << 20, NULL, NULL) == INVALID
+    assert g(p, 2, FAKE, 1 << 20, NULL, NULL) == UNSUPPORTED
+    assert g(p, 1, NULL, 1 << 20, NULL, NULL) == INVALID
+    assert g(p, 1, FAKE_ODD, 1 << 20, NULL, NULL) == INVALID
+    assert g(p, 0, NULL, 0, NULL, NULL) == 0

@@ -72,3 +72,49 @@ def test_ws_matvec_host_matches_device_form_and_shares_scratch():
             assert torch.equal(Y_h.view(torch.int16 if dt == torch.float16 else torch.int32),
                                Y_d.cpu().view(torch.int16 if dt == torch.float16 else torch.int32))
     assert int(scratch[:65536 + 256].count_nonzero()) == 0
+
+
+def test_inputs_copied_event_orders_another_stream():
+    """The optional event is recorded after the input copies: a second stream waiting on it
+    starts only then (a never-recorded torch event is created by the binding first)."""
+    inp = synth.markov_config("tiny")
+    B, k, V = inp["base"].shape
+    base_h = torch.from_numpy(inp["base"]).pin_memory()
+    prev_h = torch.from_numpy(inp["prev0"].copy()).pin_memory()
+    ids_h = torch.empty((B, k), dtype=torch.int64).pin_memory()
+    w1 = torch.from_numpy(inp["w1"].view(np.int16)).cuda()
+    w2 = torch.from_numpy(inp["w2"].view(np.int16)).cuda()
+    scratch = _scratch(api.markov_draft_host_scratch_bytes(B, k, V, inp["rank"]))
+    ev = torch.cuda.Event()
+    assert not ev.cuda_event
+    api.markov_draft_host(base_h, w1, w2, None, prev_h, ids_h, scratch, inputs_copied=ev)
+    assert ev.cuda_event
+    other = torch.cuda.Stream()
+    other.wait_event(ev)
+    marker = torch.zeros(1, device="cuda")
+    with torch.cuda.stream(other):
+        marker += 1
+    torch.cuda.synchronize()
+    assert ev.query() and float(marker.item()) == 1.0
+
+
+def test_ws_matvec_grouped_host_matches_grouped_device_form():
+    shapes = [(7, N, K) for (K, N) in synth.WS_SHAPES] + [(3, 300, 12288)]
+    host_probs, dev_probs = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        inp = synth.ws_inputs(M, N, K, seed=80 + i)
+        W = torch.from_numpy(inp["W"].view(np.int16)).cuda().view(torch.float16)
+        X_h = torch.from_numpy(inp["X"].view(np.int16)).view(torch.float16).pin_memory()
+        dt = torch.float32 if i % 2 else torch.float16
+        host_probs.append((W, X_h, torch.empty((M, N), dtype=dt).pin_memory()))
+        dev_probs.append((W, X_h.cuda(), torch.empty((M, N), dtype=dt, device="cuda")))
+    scratch = _scratch(api.ws_matvec_grouped_host_scratch_bytes(host_probs), zero=True)
+    for _ in range(2):
+        api.ws_matvec_grouped_host(host_probs, scratch)
+        api.ws_matvec_grouped(dev_probs)
+        torch.cuda.synchronize()
+        for (_, _, Yh), (_, _, Yd) in zip(host_probs, dev_probs):
+            v = torch.int32 if Yh.dtype == torch.float32 else torch.int16
+            assert torch.equal(Yh.view(v), Yd.cpu().view(v))
+    assert api.ws_matvec_status(scratch) == 0
+    assert int(scratch[:65536 + 256].count_nonzero()) == 0
