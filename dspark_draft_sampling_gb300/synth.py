@@ -187,7 +187,8 @@ def ws_q8_inputs(M: int, N: int, K: int, *, seed: int = 0, d_sd: float = 2e-4,
     if K % 32:
         raise ValueError("K must be a multiple of 32")
     nb = K // 32
-    q = _rng(seed, _S_Q8Q).integers(-127, 128, size=(N, nb, 32), dtype=np.int64).astype(np.int8)
+    # drawn as int16 (exact for this range, a quarter of int64's memory at N ~ 2M rows)
+    q = _rng(seed, _S_Q8Q).integers(-127, 128, size=(N, nb, 32), dtype=np.int16).astype(np.int8)
     if power_of_two_scales:
         j = _rng(seed, _S_Q8D).integers(8, 13, size=(N, nb))
         d = np.ldexp(1.0, -j).astype(np.float32)

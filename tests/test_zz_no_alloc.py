@@ -56,6 +56,20 @@ def test_noalloc_matches_workspace_entry_two_calls(dspark_lib, lane, num_reqs):
     parity.check_markov(inp, first, values=False)
 
 
+def test_noalloc_at_its_limits(dspark_lib):
+    """k = 64 positions (the static scratch's limit) and num_reqs = 8 (the kernel's limit)."""
+    lib = dspark_lib
+    inp = synth.markov_inputs(8, 64, 5000, 128, base_sd=1.0, w_sd=0.3, d2t="injective", seed=5)
+    B, k, V = inp["base"].shape
+    a = parity.markov_to_device(inp)
+    out = torch.full((B, k), -7, dtype=torch.int64, device="cuda")
+    _noalloc(lib, a, B, k, V, 128, out)
+    torch.cuda.synchronize()
+    rep = parity.check_markov(inp, dict(out_ids=out.cpu().numpy(), prev=a["prev"].cpu().numpy(), logits=None,
+                                        bias=None, status=0), values=False)
+    assert rep["n_exempt"] <= 2
+
+
 def test_noalloc_rejects_too_many_positions(dspark_lib):
     lib = dspark_lib
     inp = synth.markov_inputs(1, 65, 64, 64, seed=2)
