@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // A kernel launched after this one with programmatic dependent launch may start its
+    // prologue now; it reads and writes global memory only after this grid has completed.
+    pdl_launch_dependents();
 
     if (warp == 4) {
         // ---------------- TMA producer ----------------
