@@ -90,10 +90,12 @@ dspark_status make_tmap_kblocks(CUtensorMap *map, const void *base, bool bf16, u
                         CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
 }
 
-dspark_status make_tmap_2d_u8_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                                    uint32_t box_rows, uint32_t box_cols) {
-    return encode_tiled_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, CU_TENSOR_MAP_SWIZZLE_128B, base, rows, cols,
-                           box_rows, box_cols);
+dspark_status make_tmap_kblocks_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                                  uint32_t box_katoms) {
+    const cuuint64_t dims[3] = {128, rows, cols / 128};
+    const cuuint64_t strides[2] = {cols, 128};
+    const cuuint32_t box[3] = {128, box_rows, box_katoms};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
 }
 
 }  // namespace dspark

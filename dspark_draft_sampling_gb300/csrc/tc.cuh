@@ -13,11 +13,13 @@ namespace dspark {
 dspark_status make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
                            uint32_t box_rows, uint32_t box_cols);
 
-// Box = box_cols x box_rows bytes of a row-major [rows, cols] 8-bit matrix with the 128-byte
-// swizzle (box_cols must be 128: within each 1024-byte group of 8 rows, 16-byte chunk c of row r
-// is stored at chunk c ^ (r & 7)).  Out-of-bounds elements of a box read as zero.
-dspark_status make_tmap_2d_u8_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                                    uint32_t box_rows, uint32_t box_cols);
+// 3-D view of a row-major [rows, cols] 8-bit matrix (cols a multiple of 128) as
+// [cols / 128][rows][128]: one box = box_katoms consecutive 128-byte column atoms of box_rows
+// rows, stored atom after atom, each atom with the 128-byte swizzle (within each 1024-byte group
+// of 8 rows, 16-byte chunk c of row r is stored at chunk c ^ (r & 7)).  One copy then reads
+// box_katoms * 128 contiguous bytes of each row.  Out-of-bounds rows read as zero.
+dspark_status make_tmap_kblocks_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                                  uint32_t box_katoms);
 
 // 3-D view of a row-major [rows, cols] 16-bit matrix (cols a multiple of 64) as
 // [cols / 64][rows][64]: one box = box_kblocks consecutive 64-column blocks of box_rows rows,

@@ -12,7 +12,8 @@
 //    that there is about one unit per SM.
 //  * Warp 4 (one thread) streams, per k-block, the W tile [128 rows x 64 k] (16 KB) and
 //    the X tile [16 rows x 64 k] (2 KB; rows >= M read as zero) with 2-D TMA tensor copies
-//    in the 128-byte-swizzled layout, through a 10-stage mbarrier ring (180 KB).
+//    in the 128-byte-swizzled layout, through an mbarrier ring: 10 stages (180 KB, one CTA
+//    per SM) when the launch has at most one unit per SM, else 5 (two CTAs per SM).
 //  * Warp 5 allocates 32 TMEM columns and one thread issues, per k-block, four
 //    tcgen05.mma kind::f16 (M=128, N=16, K=16; fp16 in, fp32 accumulate) into TMEM.
 //    tcgen05.commit frees each stage once its MMAs are done, and signals the epilogue
@@ -30,9 +31,15 @@ namespace dspark {
 namespace {
 
 constexpr int kThreads = 192;      // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
-// 10 x 18 KB stages, one CTA per SM and about one unit per SM: measured best on GB300 among
-// {5, 8, 10, 12} stages x {1, 2, 4} units per SM for the four Qwen3-8B projection shapes.
-constexpr int kStages = 10;
+// Ring depth, chosen per launch.  With at most one unit per SM, 10 x 18 KB stages and one CTA
+// per SM (measured best on GB300 among {5, 8, 10, 12} stages x {1, 2, 4} units per SM for the
+// four Qwen3-8B projection shapes).  With more units than SMs (a grouped launch, a large N)
+// each SM runs several CTAs in turn, and each CTA spends microseconds on its setup, its first
+// copies and its epilogue with the stream idle; 5 stages let two CTAs share an SM, so one
+// streams while the other starts or finishes (measured on the grouped projections: 53.0 ->
+// 48.7 us; on a 151936 x 4096 matrix 187 -> 182 us).
+constexpr int kStagesSolo = 10;
+constexpr int kStagesShared = 5;
 constexpr int kUnitsPerSm = 1;
 constexpr int kRowsPerUnit = 128;  // MMA M
 constexpr int kNPad = 16;          // MMA N: X rows padded to 16
@@ -41,7 +48,7 @@ constexpr int kABytes = kRowsPerUnit * kKB * 2;  // 16 KB
 constexpr int kBBytes = kNPad * kKB * 2;         // 2 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 18 KB (multiple of 1024)
 constexpr uint32_t kTmemCols = 32;
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 256;
+constexpr size_t smem_bytes_for(int nst) { return 1024 + size_t(nst) * kStageBytes + 256; }
 
 constexpr int kMaxProblems = 8;
 
@@ -64,6 +71,7 @@ struct WsGroup {
     CUtensorMap tmX[kMaxProblems];
     WsProblem prob[kMaxProblems];
     int nprob;
+    int nst;            // ring stages (kStagesSolo or kStagesShared)
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
@@ -74,9 +82,10 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-aligned tiles
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(kStages) * kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *done = empty + kStages;
+    const int nst = g.nst;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(nst) * kStageBytes);
+    uint64_t *empty = full + nst;
+    uint64_t *done = empty + nst;
     uint64_t *never = done + 1;  // signalled by nobody: the fault-injection hook waits on it
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
     int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
@@ -97,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     const int n0 = rb * kRowsPerUnit;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
                 mbar_arrive_expect_tx(&full[st], kStageBytes);
                 tma_load_2d(sa, tmW, (kb0 + j) * kKB, n0, &full[st], pol_w);
                 tma_load_2d(sa + kABytes, tmX, (kb0 + j) * kKB, 0, &full[st], pol_x);
-                if (++st == kStages) {
+                if (++st == nst) {
                     st = 0;
                     ph ^= 1u;
                 }
@@ -156,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
                 tc_mma_f16(tmem, dA + 4, dB + 4, idesc, 1u);
                 tc_mma_f16(tmem, dA + 6, dB + 6, idesc, 1u);
                 tc_commit(&empty[st]);
-                if (++st == kStages) {
+                if (++st == nst) {
                     st = 0;
                     ph ^= 1u;
                 }
@@ -410,15 +419,18 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(ws_matvec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+                                             static_cast<int>(smem_bytes_for(kStagesSolo)));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_matvec_tc_kernel, kThreads, kSmemBytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_matvec_tc_kernel, kThreads,
+                                                          smem_bytes_for(kStagesSolo));
         if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
         if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
         configured_dev = dev;
     }
-    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), kSmemBytes,
+    // more units than SMs: two CTAs per SM with the shallower ring
+    g.nst = units > static_cast<unsigned>(sms) ? kStagesShared : kStagesSolo;
+    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), smem_bytes_for(g.nst),
                                reinterpret_cast<cudaStream_t>(stream), g);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;

@@ -18,24 +18,26 @@
 // order.  Every output is summed in one fixed order (blocks, then split-K units in order), so
 // results are deterministic and row m's does not depend on M.
 //
-// GB300 design (persistent: one CTA per SM, 15 warps)
+// GB300 design (persistent: one CTA per SM, 16 warps)
 //  * Work unit = (128 weight rows, a range of 256-k superblocks); K is split so that there is
 //    about one unit per SM.  Each CTA takes every gridDim.x-th unit and streams the stages of
 //    its units back to back, so one unit's epilogue overlaps the next unit's loads.
 //  * Warp 12 (one thread) streams, per 128-k stage, the int8 tile [128 rows x 128 k] (16 KB,
-//    128-byte swizzle) and the X tile [16 rows x 128 k] (two 2 KB fp16 atoms in one 3-D copy;
+//    128-byte swizzle, one 3-D copy of a single 128-byte column atom) and the X tile [16 rows x 128 k] (two 2 KB fp16 atoms in one 3-D copy;
 //    rows >= M read as zero) with TMA tensor copies through a 10-stage ring (200 KB).
 //  * Warps 4-7 take the even stages and warps 8-11 the odd ones: each thread converts one weight
 //    row's 128 int8 to fp16 (a byte permute puts q + 128 into the mantissa of 1024, one packed
 //    subtraction of 1152 leaves q exactly) and writes them with tcgen05.st straight into tensor
 //    memory, where the MMA takes its A operand: the fp16 copy never touches shared memory.
 //  * Warp 13 allocates all 512 TMEM columns (16 accumulator slots of 128 x 16 fp32 and a 4-slot
-//    ring of fp16 A tiles).  Warps 13 and 14 issue the MMAs of the even and odd stages: per
-//    Q8_0 block two tcgen05.mma kind::f16 (M=128, N=16, K=16; A from TMEM, B = X from shared
-//    memory) into a fresh accumulator slot.  Two issuers, 8 MMAs per barrier round trip and one
-//    tcgen05.commit per stage keep the single-thread issue cost below the weight stream's pace:
-//    that one commit hands the stage's 4 slots to the epilogue and frees its A tile and its
-//    shared-memory slot.
+//    ring of fp16 A tiles).  Warps 13-15 issue the MMAs, warp 13 + i those of the stages
+//    J = i mod 3: per Q8_0 block two tcgen05.mma kind::f16 (M=128, N=16, K=16; A from TMEM,
+//    B = X from shared memory) into a fresh accumulator slot, and one tcgen05.commit per stage,
+//    which hands the stage's 4 slots to the epilogue and frees its A tile and its
+//    shared-memory slot.  A single issuing thread spends far longer per MMA than the tensor
+//    pipe does (the barrier waits and the commit of each stage, slowed further while the
+//    converters stream tcgen05.st), and issuers in separate warps proceed in parallel.  A
+//    fourth issuer would need a 17th warp, which lowers every thread's register budget to 96.
 //  * Warps 0-3 (one TMEM lane = one weight row per thread) read a stage's 4 x 16 sums with
 //    tcgen05.ld and fold them in with the row's scales (loaded 8 at a time from global memory,
 //    four loads ahead).
@@ -48,10 +50,11 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 480;          // warps 0-3 epilogue, 4-11 convert, 12 TMA, 13-14 MMA
 constexpr int kConvWarps = 8;          // two groups of 4, alternate stages
 constexpr int kTmaWarp = 4 + kConvWarps;
-constexpr int kMmaWarp = kTmaWarp + 1;  // and kMmaWarp + 1
+constexpr int kMmaWarp = kTmaWarp + 1;  // first of kMmaIssuers warps
+constexpr int kMmaIssuers = 3;         // issuer i takes the stages J = i mod 3
+constexpr int kThreads = 32 * (kMmaWarp + kMmaIssuers);  // 512: warps 0-3 epilogue, 4-11 convert, 12 TMA, 13-15 MMA
 constexpr int kRows = 128;             // weight rows per unit: MMA M, TMEM lanes
 constexpr int kNPad = 16;              // MMA N: X rows padded to 16
 constexpr int kKS = 128;               // k per stage: 128 B of int8 per row (the 128-byte swizzle span)
@@ -67,7 +70,7 @@ constexpr int kASlots = 4;             // TMEM ring of fp16 A tiles
 constexpr uint32_t kACols = kKS / 2;   // 64 columns: 128 fp16 per lane
 constexpr uint32_t kAColBase = kTSlots * kNPad;                  // 256
 constexpr uint32_t kTmemCols = kAColBase + kASlots * kACols;     // 512
-constexpr int kNumBars = 2 * kStages + kASlots + kTGroups + 3;
+constexpr int kNumBars = 2 * kStages + kASlots + kTGroups + kMmaIssuers + 1;
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kSlotBytes + kNumBars * 8 + 16;
 static_assert(kTmemCols == 512, "the TMEM allocation must be a power of two <= 512");
 static_assert(kStages % 2 == 0 && kASlots % 2 == 0 && kTGroups % 2 == 0, "rings must keep stage parity");
@@ -132,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *done = full_r + kStages;
     uint64_t *full_a = done + kStages;     // fp16 A tile written to TMEM (per A slot)
     uint64_t *empty_t = full_a + kASlots;  // accumulator group drained by the epilogue
-    uint64_t *mma_done = empty_t + kTGroups;  // [2]
-    uint64_t *never = mma_done + 2;           // signalled by nobody: the fault-injection hook waits on it
+    uint64_t *mma_done = empty_t + kTGroups;  // [kMmaIssuers]
+    uint64_t *never = mma_done + kMmaIssuers;  // signalled by nobody: the fault-injection hook waits on it
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
     int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -147,8 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kASlots; ++s) mbar_init(&full_a[s], 4);
         for (int g = 0; g < kTGroups; ++g) mbar_init(&empty_t[g], 4);
-        mbar_init(&mma_done[0], 1);
-        mbar_init(&mma_done[1], 1);
+        for (int i = 0; i < kMmaIssuers; ++i) mbar_init(&mma_done[i], 1);
         mbar_init(never, 1);
         fence_mbar_init();
     }
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     unsigned char *slot = ring + size_t(st) * kSlotBytes;
                     const int k0 = (ug.ks0 + j) * kKS;
                     mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
-                    tma_load_2d(slot, &tmQ, k0, ug.n0, &full_r[st], pol_q);
+                    tma_load_3d(slot, &tmQ, 0, ug.n0, k0 / 128, &full_r[st], pol_q);
                     tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
                 }
             }
@@ -188,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = J > kStages ? J - kStages : 0; i < J; ++i)
                 mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.timeout_ns);
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ---- MMA issuers: warp 13 the even stages, warp 14 the odd ones ----
+    } else if (warp >= kMmaWarp) {
+        // ---- MMA issuers: warp kMmaWarp + i the stages J = i mod kMmaIssuers ----
         if (lane == 0) {
             const int par = warp - kMmaWarp;
             constexpr uint32_t idesc = idesc_f16(false, kRows, kNPad);
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
                 const int nst = unit_geometry(a, u).nst;
                 for (int j = 0; j < nst; ++j, ++J) {
-                    if ((J & 1) != par) continue;
+                    if (J % kMmaIssuers != par) continue;
                     const int st = J % kStages, g = J % kASlots;
                     const uint32_t ph = static_cast<uint32_t>((J / kASlots) & 1);
                     // the converters arrive on full_a only after the stage's TMA copies (X included)
@@ -314,29 +316,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok && lane == 0) atomicOr(a.status, kWsStatusTimeout);
                     tc_fence_after();
-                    uint32_t v[kBlocksPerStage][16];
-                    if (ok) {
-                        const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
-                                            static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+                    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
+                                        static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+                    // two blocks' sums at a time (fewer live registers); the group is handed back
+                    // once all four are read
 #pragma unroll
-                        for (int q = 0; q < kBlocksPerStage; ++q) tmem_ld_16_async(ta + q * kNPad, v[q]);
-                        tmem_wait_ld();
-                    } else {
+                    for (int hq = 0; hq < kBlocksPerStage; hq += 2) {
+                        uint32_t v[2][16];
+                        if (ok) {
+                            tmem_ld_16_async(ta + hq * kNPad, v[0]);
+                            tmem_ld_16_async(ta + (hq + 1) * kNPad, v[1]);
+                            tmem_wait_ld();
+                        } else {
 #pragma unroll
-                        for (int q = 0; q < kBlocksPerStage; ++q)
+                            for (int m = 0; m < kNPad; ++m) v[0][m] = v[1][m] = 0u;
+                        }
+                        if (hq + 2 == kBlocksPerStage) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
+                        }
 #pragma unroll
-                            for (int m = 0; m < kNPad; ++m) v[q][m] = 0u;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
+                        for (int q = 0; q < 2; ++q) {
+                            const int b = h * kBlocksPerStage + hq + q;  // Q8_0 block within the superblock
+                            const float dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(
+                                (b & 1) ? (dw[b >> 1] >> 16) : (dw[b >> 1] & 0xffffu))));
 #pragma unroll
-                    for (int q = 0; q < kBlocksPerStage; ++q) {
-                        const int b = h * kBlocksPerStage + q;  // Q8_0 block within the superblock
-                        const float dsc = __half2float(__ushort_as_half(
-                            static_cast<unsigned short>((b & 1) ? (dw[b >> 1] >> 16) : (dw[b >> 1] & 0xffffu))));
-#pragma unroll
-                        for (int m = 0; m < kNPad; ++m) acc[m] = fmaf(dsc, __uint_as_float(v[q][m]), acc[m]);
+                            for (int m = 0; m < kNPad; ++m) acc[m] = fmaf(dsc, __uint_as_float(v[q][m]), acc[m]);
+                        }
                     }
                 }
             }
@@ -516,7 +523,7 @@ dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X
         return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
 
     CUtensorMap tmQ, tmX;
-    dspark_status st = make_tmap_2d_u8_sw128(&tmQ, Wq, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRows, kKS);
+    dspark_status st = make_tmap_kblocks_u8(&tmQ, Wq, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRows, 1);
     if (st != DSPARK_OK) return st;
     st = make_tmap_kblocks(&tmX, X, false, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, 2);
     if (st != DSPARK_OK) return st;
