@@ -274,9 +274,12 @@ Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
     p.nkb = (K + kKB - 1) / kKB;
-    // about kUnitsPerSm units per SM, each with at least 4 k-blocks to amortize the pipeline fill
+    // about kUnitsPerSm units per SM, each with at least 16 k-blocks (256 KB of weights): a
+    // unit's setup, first copies and split-K epilogue take a few microseconds, so shorter units
+    // spend longer on them than on their stream (measured on the grouped Qwen3-8B projections:
+    // 4 -> 16 k-blocks, 48.8 -> 46.0 us, the four shapes alone unchanged)
     int S = (kUnitsPerSm * sms) / p.nrb;
-    const int smax = p.nkb / 4 > 0 ? p.nkb / 4 : 1;
+    const int smax = p.nkb / 16 > 0 ? p.nkb / 16 : 1;
     if (S > smax) S = smax;
     if (S < 1) S = 1;
     p.S = S;
