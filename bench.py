@@ -309,6 +309,9 @@ def run_gpu(args, rank, world):
     # the order they become ready, so the inputs are ordered small and urgent first: the
     # draft's 15 MB, then the projections' 0.2 MB, then the probes' 61 MB, each lane's
     # kernels overlapping the later copies.  Every lane starts after the step's start event.
+    # (Splitting the probe batch into pieces on two alternating streams, so that each piece's
+    # probes overlap the next piece's copy, was measured slower: 424 / 535 / 625 us for 1 / 4 /
+    # 8 pieces.)
     e2e = None
     if not args.no_e2e:
         base_h = torch.from_numpy(mk["base"]).pin_memory()
@@ -349,18 +352,21 @@ def run_gpu(args, rank, world):
             flush_l2(2)
             e2e_step()
         torch.cuda.synchronize()
-        e2e_ms = []
+        e2e_ms, enqueue_s = [], []
         for s in range(args.steps):
             flush_l2(s)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
+            h0 = time.perf_counter()
             e2e_step()
+            enqueue_s.append(time.perf_counter() - h0)
             b.record(stream)
             b.synchronize()
             e2e_ms.append(a.elapsed_time(b))
         e2e = {"value": statistics.mean(e2e_ms) * 1000.0, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "host_enqueue_us": statistics.median(enqueue_s) * 1e6,
                "api": "dspark_markov_draft_host, dspark_ws_matvec_grouped_host and "
                       "dspark_conf_probe_host on three streams, pinned host buffers, input copies "
                       "ordered by the calls' inputs_copied events"}
