@@ -18,7 +18,7 @@
 // order.  Every output is summed in one fixed order (blocks, then split-K units in order), so
 // results are deterministic and row m's does not depend on M.
 //
-// GB300 design (persistent: one CTA per SM, 16 warps)
+// GB300 design (persistent: one CTA per SM, 15 warps)
 //  * Work unit = (128 weight rows, a range of 256-k superblocks); K is split so that there is
 //    about one unit per SM.  Each CTA takes every gridDim.x-th unit and streams the stages of
 //    its units back to back, so one unit's epilogue overlaps the next unit's loads.
@@ -30,14 +30,18 @@
 //    subtraction of 1152 leaves q exactly) and writes them with tcgen05.st straight into tensor
 //    memory, where the MMA takes its A operand: the fp16 copy never touches shared memory.
 //  * Warp 13 allocates all 512 TMEM columns (16 accumulator slots of 128 x 16 fp32 and a 4-slot
-//    ring of fp16 A tiles).  Warps 13-15 issue the MMAs, warp 13 + i those of the stages
-//    J = i mod 3: per Q8_0 block two tcgen05.mma kind::f16 (M=128, N=16, K=16; A from TMEM,
-//    B = X from shared memory) into a fresh accumulator slot, and one tcgen05.commit per stage,
-//    which hands the stage's 4 slots to the epilogue and frees its A tile and its
-//    shared-memory slot.  A single issuing thread spends far longer per MMA than the tensor
-//    pipe does (the barrier waits and the commit of each stage, slowed further while the
-//    converters stream tcgen05.st), and issuers in separate warps proceed in parallel.  A
-//    fourth issuer would need a 17th warp, which lowers every thread's register budget to 96.
+//    ring of fp16 A tiles).  Warps 13 and 14 issue the MMAs of the even and odd stages: per
+//    Q8_0 block two tcgen05.mma kind::f16 (M=128, N=16, K=16; A from TMEM, B = X from shared
+//    memory) into a fresh accumulator slot, and one tcgen05.commit per stage, which hands the
+//    stage's 4 slots to the epilogue and frees its A tile and its shared-memory slot.  A
+//    single issuing thread spends far longer per MMA than the tensor pipe does (the barrier
+//    waits and the commit of each stage, slowed further while the converters stream
+//    tcgen05.st), and issuers in separate warps proceed in parallel.  The issuer count must
+//    divide the 4 A slots / accumulator groups: each issuer then also handled the previous
+//    use of every slot it waits on (stage J - 4), so the slot's barriers are never more than
+//    one phase from the one it waits for and the parity wait is exact.  With three issuers
+//    stage J - 4 belongs to another issuer, a lagging converter leaves the barrier a whole
+//    phase behind, the parity test passes early and the MMAs read a half-written A tile.
 //  * Warps 0-3 (one TMEM lane = one weight row per thread) read a stage's 4 x 16 sums with
 //    tcgen05.ld and fold them in with the row's scales (loaded 8 at a time from global memory,
 //    four loads ahead).
@@ -53,8 +57,8 @@ namespace {
 constexpr int kConvWarps = 8;          // two groups of 4, alternate stages
 constexpr int kTmaWarp = 4 + kConvWarps;
 constexpr int kMmaWarp = kTmaWarp + 1;  // first of kMmaIssuers warps
-constexpr int kMmaIssuers = 3;         // issuer i takes the stages J = i mod 3
-constexpr int kThreads = 32 * (kMmaWarp + kMmaIssuers);  // 512: warps 0-3 epilogue, 4-11 convert, 12 TMA, 13-15 MMA
+constexpr int kMmaIssuers = 2;         // issuer i takes the stages J = i mod 2
+constexpr int kThreads = 32 * (kMmaWarp + kMmaIssuers);  // 480: warps 0-3 epilogue, 4-11 convert, 12 TMA, 13-14 MMA
 constexpr int kRows = 128;             // weight rows per unit: MMA M, TMEM lanes
 constexpr int kNPad = 16;              // MMA N: X rows padded to 16
 constexpr int kKS = 128;               // k per stage: 128 B of int8 per row (the 128-byte swizzle span)
@@ -75,6 +79,9 @@ constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kSlotBytes + kNumBars * 8
 static_assert(kTmemCols == 512, "the TMEM allocation must be a power of two <= 512");
 static_assert(kStages % 2 == 0 && kASlots % 2 == 0 && kTGroups % 2 == 0, "rings must keep stage parity");
 static_assert(kASlots == kTGroups && kASlots < kStages, "stage j uses A slot and accumulator group j % 4");
+static_assert(kASlots % kMmaIssuers == 0 && kASlots % 2 == 0,
+              "the issuer (and the converter group) of stage j must also own stage j - kASlots, "
+              "so that its parity waits on the slot's barriers are exact");
 
 struct Q8Args {
     const uint16_t *d;  // [N, K/32] fp16 scales
