@@ -187,3 +187,131 @@ def test_an_issuer_count_that_does_not_divide_the_slots_is_caught(issuers):
     c = kernel_constants()
     err = check(c["stages"], c["aslots"], issuers, c["conv_groups"], trials=2000)
     assert err is not None and "(A written)" in err
+
+
+# ---------------------------------------------------------------- Markov draft kernel ---
+MARKOV_SRC = os.path.join(os.path.dirname(SRC), "markov_tc.cu")
+
+
+def markov_slots(rank):
+    """Tile slots of the Markov kernel's ring at this rank (the ring holds kRingBytes of
+    [128 x rank] bf16 tiles, one 16 KB box per 64 columns)."""
+    m = re.search(r"constexpr int kRingBytes = (\d+) \* kBoxBytes;", open(MARKOV_SRC).read())
+    assert m
+    return int(m.group(1)) // (rank // 64)
+
+
+def run_markov(nslots, k, ntiles, rng):
+    """One random interleaving of the Markov kernel's roles for one CTA: the TMA producer
+    (one copy per tile, running ahead across positions), the MMA issuer (per position: wait
+    for H; per tile: wait for its accumulator to be drained, then for the tile), the epilogue
+    (per tile: wait for the commit that frees the slot and hands over the accumulator; after
+    the last tile of a position: the next position's H).  Returns an error string or None."""
+    full = [Barrier() for _ in range(nslots)]
+    empty = [Barrier() for _ in range(nslots)]  # one commit per tile: slot free + accumulator ready
+    acc_empty = [Barrier() for _ in range(2)]
+    h_full = [Barrier() for _ in range(2)]
+    h_full[0].completed = 1  # the epilogue builds position 0's H before the loop
+    total = k * ntiles
+    error = None
+
+    def wait(bar, kk, who):
+        nonlocal error
+        if (bar.completed & 1) == (kk & 1):
+            return False
+        if bar.completed != kk + 1 and error is None:
+            error = f"{who}: passed with {bar.completed} completed phases, wanted {kk + 1}"
+        return True
+
+    st = dict(prod=0, mma=0, mma_w=0, epi=0)
+    pending_land, pending_mma = [], []
+
+    def producer():
+        q = st["prod"]
+        if q >= total:
+            return False
+        if q >= nslots and not wait(empty[q % nslots], q // nslots - 1, f"producer tile {q}"):
+            return False
+        pending_land.append(q)
+        st["prod"] += 1
+        return True
+
+    def issuer():
+        q = st["mma"]
+        if q >= total:
+            return False
+        i, t = divmod(q, ntiles)
+        w = st["mma_w"]
+        if w == 0:  # the position's H (first tile of each position only)
+            if t == 0 and not wait(h_full[i & 1], i >> 1, f"issuer position {i} (H)"):
+                return False
+            st["mma_w"] = 1
+            return True
+        if w == 1:  # accumulator q & 1 drained (tile q - 2)
+            if q >= 2 and not wait(acc_empty[q & 1], (q >> 1) - 1, f"issuer tile {q} (accumulator)"):
+                return False
+            st["mma_w"] = 2
+            return True
+        if not wait(full[q % nslots], q // nslots, f"issuer tile {q} (tile landed)"):
+            return False
+        pending_mma.append(q)
+        st["mma"] += 1
+        st["mma_w"] = 0
+        return True
+
+    def epilogue():
+        q = st["epi"]
+        if q >= total:
+            return False
+        if not wait(empty[q % nslots], q // nslots, f"epilogue tile {q}"):
+            return False
+        acc_empty[q & 1].completed += 1
+        i, t = divmod(q, ntiles)
+        if t == ntiles - 1 and i + 1 < k:
+            h_full[(i + 1) & 1].completed += 1
+        st["epi"] += 1
+        return True
+
+    def land(x):
+        q = pending_land.pop(x)
+        full[q % nslots].completed += 1
+        return True
+
+    def mma_complete(x):
+        if x != 0:  # one issuer: its commits complete in issue order
+            return False
+        q = pending_mma.pop(0)
+        empty[q % nslots].completed += 1
+        return True
+
+    while error is None:
+        actions = [producer, issuer, epilogue]
+        actions += [lambda x=x: land(x) for x in range(len(pending_land))]
+        actions += [lambda x=x: mma_complete(x) for x in range(len(pending_mma))]
+        rng.shuffle(actions)
+        if not any(a() for a in actions):
+            break
+    if error:
+        return error
+    if st["epi"] < total:
+        return f"deadlock: epilogue at tile {st['epi']} of {total}"
+    return None
+
+
+@pytest.mark.parametrize("rank", [64, 128, 256])
+def test_markov_protocol_is_exact_under_random_interleavings(rank):
+    nslots = markov_slots(rank)
+    rng = random.Random(rank)
+    for _ in range(150):
+        k = rng.randint(1, 6)
+        ntiles = rng.randint(1, 14)
+        err = run_markov(nslots, k, ntiles, rng)
+        assert err is None, (rank, nslots, k, ntiles, err)
+
+
+def test_markov_model_catches_a_one_slot_ring():
+    # with one slot the producer's and the epilogue's waits on the same barrier can be two
+    # phases apart: the model must see it (and the kernel never runs with fewer than 3)
+    rng = random.Random(7)
+    assert any(run_markov(1, 4, 6, rng) for _ in range(300))
+    assert min(markov_slots(r) for r in (64, 128, 256)) >= 2
