@@ -131,17 +131,21 @@ def markov_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(B):
-    """DRAM bytes per Markov launch from the committed ncu summary, if it was taken on the
-    current kernel source and this num_reqs; else None."""
-    p = os.path.join(REPO, "profiles", "markov_draft_full_vocab_27b.md")
+MARKOV_PROFILE = os.path.join("profiles", "markov_draft_full_vocab_27b.md")
+
+
+def recorded_traffic(B, what="traffic_bytes_per_launch"):
+    """Bytes per Markov launch from the committed ncu summary (DRAM read + write for
+    `traffic_bytes_per_launch`, L2-to-SM reads for `l2_to_sm_bytes_per_launch`), if it was
+    taken on the current kernel source and this num_reqs; else None."""
+    p = os.path.join(REPO, MARKOV_PROFILE)
     if not os.path.exists(p):
         return None
     text = open(p).read()
     src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     if not src or src.group(1) != markov_source_hash():
         return None
-    m = re.search(rf"traffic_bytes_per_launch\[num_reqs={B}\]:\s*([0-9.eE+]+)", text)
+    m = re.search(rf"{what}\[num_reqs={B}\]:\s*([0-9.eE+]+)", text)
     return float(m.group(1)) if m else None
 
 
@@ -197,6 +201,88 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- ceilings ---------------
+def load_bench_library():
+    """libdspark_bench.so: the measurement kernels (read bandwidth, empty launch)."""
+    import ctypes
+
+    from dspark_draft_sampling_gb300 import build
+
+    lib = ctypes.CDLL(build.bench_lib_file())
+    lib.dspark_bench_read.restype = ctypes.c_int
+    lib.dspark_bench_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.dspark_bench_empty.restype = ctypes.c_int
+    lib.dspark_bench_empty.argtypes = [ctypes.c_void_p]
+    return lib
+
+
+def measure_ceilings(dev, reps: int = 10):
+    """Ceilings measured on this GPU in this run, with the same CUDA-event method as the
+    kernels: the L2-to-SM read bandwidth (a 64 MiB buffer, well inside L2, read 20 times in
+    one launch after a warming pass; best of `reps`), the DRAM read bandwidth (a 2 GiB buffer
+    read once; best of `reps`) and the event floor (two events around one empty launch after
+    an L2 flush; median of 50)."""
+    import ctypes
+
+    import torch
+
+    lib = load_bench_library()
+    stream = torch.cuda.current_stream(dev)
+    s = ctypes.c_void_p(stream.cuda_stream)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = {}
+
+    def best_read(buf, passes, warm):
+        nbytes = buf.numel()
+        best = None
+        for _ in range(reps):
+            if warm:
+                rc = lib.dspark_bench_read(ctypes.c_void_p(buf.data_ptr()), nbytes, 1,
+                                           ctypes.c_void_p(sink.data_ptr()), sms * 4, 512, s)
+                assert rc == 0, rc
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = lib.dspark_bench_read(ctypes.c_void_p(buf.data_ptr()), nbytes, passes,
+                                       ctypes.c_void_p(sink.data_ptr()), sms * 4, 512, s)
+            b.record(stream)
+            b.synchronize()
+            assert rc == 0, rc
+            gbs = nbytes * passes / (a.elapsed_time(b) * 1e-3) / 1e9
+            best = gbs if best is None else max(best, gbs)
+        return best
+
+    l2buf = torch.ones(64 << 20, dtype=torch.uint8, device=dev)
+    out["l2_read_gbs"] = best_read(l2buf, 20, True)
+    del l2buf
+    big = torch.ones(2 << 30, dtype=torch.uint8, device=dev)
+    out["dram_read_gbs"] = best_read(big, 1, False)
+    del big
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sinkf = torch.empty((), dtype=torch.int32, device=dev)
+    ts = []
+    for r in range(53):
+        flush.fill_(r & 0xFF)
+        torch.amax(flush.view(torch.int32), dim=0, out=sinkf)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        assert lib.dspark_bench_empty(s) == 0
+        b.record(stream)
+        b.synchronize()
+        if r >= 3:
+            ts.append(a.elapsed_time(b) * 1000.0)
+    out["event_floor_us"] = {"median": statistics.median(ts), "mean": statistics.mean(ts),
+                             "min": min(ts), "max": max(ts)}
+    out["method"] = ("libdspark_bench read kernel (16-byte ld.global.cg, grid = 4 x SMs x 512 "
+                     "threads): 64 MiB read 20 times per launch after a warming pass (L2) and "
+                     "2 GiB read once (DRAM), best of 10; empty launch between two events "
+                     "after an L2 flush, 50 samples")
+    return out
 
 
 # ---------------------------------------------------------------- GPU arm ----------------
@@ -372,7 +458,8 @@ def run_gpu(args, rank, world):
                       "ordered by the calls' inputs_copied events"}
     plan.close()
 
-    res = dict(ms_step=ms_step, wall=wall, markov_ms=statistics.mean(markov_ms),
+    ceilings = None if args.no_ceilings else measure_ceilings(dev)
+    res = dict(ms_step=ms_step, wall=wall, markov_ms=statistics.mean(markov_ms), ceilings=ceilings,
                probe_ms=statistics.mean(probe_ms), ws_ms=statistics.mean(ws_ms),
                clocks=clk, e2e=e2e, kernels=kernels_per_step * args.steps,
                markov_ms_min=min(markov_ms))
@@ -488,9 +575,11 @@ def run_configs(dev, mk27, reps: int = 30):
     peak, _ = read_peak()
 
     def stats(ts):
+        # CUDA event timestamps on this GPU step in about 2 us, so a median of short launches
+        # sits on that grid; the mean of many samples averages the step out
         ts = sorted(ts)
         q = lambda f: ts[min(len(ts) - 1, int(round(f * (len(ts) - 1))))]
-        return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9)}
+        return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "mean": statistics.mean(ts)}
 
     def timed(fn, cold):
         for _ in range(3):
@@ -517,7 +606,8 @@ def run_configs(dev, mk27, reps: int = 30):
         cold, warm = timed(fn, True), timed(fn, False)
         return {"us_cold": cold, "us_warm": warm, "algorithmic_bytes": nbytes,
                 "GBps_cold": nbytes / (cold["median"] * 1e-6) / 1e9,
-                "frac_of_hbm_cold": nbytes / (cold["median"] * 1e-6) / 1e9 / peak}
+                "frac_of_hbm_cold": nbytes / (cold["median"] * 1e-6) / 1e9 / peak,
+                "frac_of_hbm_cold_mean": nbytes / (cold["mean"] * 1e-6) / 1e9 / peak}
 
     out = {}
     w1_27 = torch.from_numpy(mk27["w1"].view(np.int16)).to(dev)
@@ -572,6 +662,10 @@ def run_configs(dev, mk27, reps: int = 30):
         wsp = api.new_ws_workspace(7, N, K, dev)
         out[f"ws_matvec_m7_{K}x{N}"] = entry(lambda: api.ws_matvec(W, X, out=Y, workspace=wsp, stream=stream),
                                              ws_bytes(7, N, K))
+        # the prior-art library path beside it (cuBLAS through torch.matmul, fp16, M = 7):
+        # context only, not part of the draft step
+        Wt = W.t()
+        out[f"cublas_matmul_m7_{K}x{N}"] = entry(lambda: torch.matmul(X, Wt, out=Y), ws_bytes(7, N, K))
     return out
 
 
@@ -625,6 +719,48 @@ def cpu_baseline(B):
             "host_cpus": os.cpu_count()}
 
 
+def markov_roofline(B, mb, t_s, peak, peak_kind, ceil):
+    """Roofline of the Markov kernel.  `achieved` / `frac` follow the pages' accounting
+    (markov_w2 re-read whole at every position) against the measured HBM copy bandwidth;
+    because each position starts on rows the previous one left in L2, that accounting can
+    exceed 1.  So the line also states the two ceilings the kernel actually streams against:
+    its DRAM bytes (ncu, committed summary) over the HBM peak, and its L2-to-SM bytes over
+    the L2 read bandwidth measured in this run, and names the one that binds (or neither)."""
+    traffic = recorded_traffic(B)
+    l2b = recorded_traffic(B, "l2_to_sm_bytes_per_launch")
+    l2_src = "ncu l1tex__m_xbar2l1tex_read_bytes (committed summary)"
+    if l2b is None:
+        l2b, l2_src = float(mb), "algorithmic bytes (every byte reaches the SMs from L2 once)"
+    achieved = mb / t_s / 1e9
+    r = {"kernel": "markov_tc_kernel (k=15 positions, one launch)",
+         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+         "frac": achieved / peak, "peak_source": peak_kind,
+         "algorithmic_bytes_per_launch": mb, "traffic": traffic,
+         "traffic_source": (f"dram__bytes_read.sum + dram__bytes_write.sum from {MARKOV_PROFILE}, "
+                            "used only while the kernel sources hash to the value recorded there"),
+         "l2_to_sm_bytes_per_launch": l2b, "l2_to_sm_source": l2_src}
+    l2_peak = ceil.get("l2_read_gbs") if ceil else None
+    fr = {}
+    if traffic:
+        fr["dram"] = traffic / t_s / 1e9 / peak
+        r["frac_dram"] = fr["dram"]
+    if l2_peak:
+        fr["l2"] = l2b / t_s / 1e9 / l2_peak
+        r["frac_l2"] = fr["l2"]
+        r["l2_peak"] = l2_peak
+    if fr:
+        name = max(fr, key=fr.get)
+        t_min = max((traffic / (peak * 1e9)) if traffic else 0.0,
+                    (l2b / (l2_peak * 1e9)) if l2_peak else 0.0)
+        r["frac_ceiling"] = t_min / t_s
+        if fr[name] >= 0.75:
+            r["binding"] = name
+        else:
+            r["binding"] = ("neither DRAM nor L2 bandwidth: the chain of k grid-wide argmax "
+                            "barriers and the bytes each SM keeps in flight bound the kernel")
+    return r
+
+
 # ---------------------------------------------------------------- main -------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -634,8 +770,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--reference-budget-s", type=float, default=90.0,
                     help="--impl reference: seconds of oracle time the timed steps may take")
-    ap.add_argument("--num-reqs", type=int, default=1)
+    ap.add_argument("--num-reqs", type=int, default=8,
+                    help="requests of the Markov draft (the 27B lane's largest configuration is 8)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ceilings", action="store_true",
+                    help="skip the in-run L2 / DRAM read bandwidth and event-floor measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the separately timed rows beyond the headline step")
@@ -714,7 +853,7 @@ def main():
     wb = sum(ws_bytes(7, N, K) for (K, N) in synth.WS_SHAPES)
     peak, peak_kind = read_peak()
     achieved = mb / (markov_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(B)
+    roof = markov_roofline(B, mb, markov_ms * 1e-3, peak, peak_kind, res["ceilings"])
     line = {
         "metric": METRIC,
         "value": job_value_us(ms_step, world),
@@ -729,11 +868,8 @@ def main():
         "dtype": "f32",
         "data": "synthetic (seeded numpy PCG64; shapes and distributions of the pages' lanes)",
         "config": config_dict(B),
-        "roofline": {"kernel": "markov_tc_kernel (k=15 positions, one launch)",
-                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": mb,
-                     "traffic": traffic},
+        "roofline": roof,
+        "ceilings": res["ceilings"],
         "parts": {
             "markov_draft_us": markov_ms * 1000.0,
             "markov_us_per_position": markov_ms * 1000.0 / k,

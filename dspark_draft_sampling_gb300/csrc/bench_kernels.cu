@@ -1,0 +1,60 @@
+// Measurement kernels (libdspark_bench): a strided 16-byte read of a buffer, repeated, for
+// the L2 and DRAM read bandwidth of this GPU, and an empty launch for the event-timing floor.
+// They are not part of the draft step.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dspark_bench.h"
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_cg_v4(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) read_kernel(const uint4 *__restrict__ p, size_t n16, int passes,
+                                                    unsigned long long *sink) {
+    uint32_t acc = 0;
+    const size_t stride = size_t(gridDim.x) * blockDim.x;
+    const size_t first = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int r = 0; r < passes; ++r) {
+        size_t i = first;
+        // eight independent loads in flight per thread
+        for (; i + 7 * stride < n16; i += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = ld_cg_v4(p + i + u * stride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+        }
+        for (; i < n16; i += stride) {
+            const uint4 v = ld_cg_v4(p + i);
+            acc ^= v.x ^ v.y ^ v.z ^ v.w;
+        }
+    }
+    if (acc == 0x9e3779b9u) atomicAdd(sink, 1ull);
+}
+
+__global__ void empty_kernel() {}
+
+}  // namespace
+
+extern "C" int dspark_bench_read(const void *buf, size_t bytes, int passes, unsigned long long *sink, int grid,
+                                 int block, void *stream) {
+    if (!buf || !sink || (bytes % 16) != 0 || (reinterpret_cast<uintptr_t>(buf) & 15u) != 0 || passes < 1 ||
+        grid < 1 || block < 1 || block > 1024)
+        return static_cast<int>(cudaErrorInvalidValue);
+    read_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4 *>(buf), bytes / 16,
+                                                                         passes, sink);
+    return static_cast<int>(cudaGetLastError());
+}
+
+extern "C" int dspark_bench_empty(void *stream) {
+    empty_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    return static_cast<int>(cudaGetLastError());
+}

@@ -6,6 +6,9 @@
 // gather markov_w1[prev], bias GEMV over the whole bf16 markov_w2 [vocab, rank], add the
 // position's base-logit row, greedy argmax with lowest-index tie-break, d2t map, and
 // carry prev on the device; only the final [num_reqs, k] ids leave the GPU.
+#include <cuda.h>
+
+#include <mutex>
 #include <new>
 
 #include "markov.cuh"
@@ -20,7 +23,7 @@ size_t workspace_bytes(int k) {
 dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16_t *w2, const int32_t *d2t,
                              int64_t *prev, int B, int k, int V, int R, int64_t *out_ids, float *dbg_logits,
                              float *dbg_bias, void *workspace, size_t ws_bytes, unsigned bar_extra,
-                             unsigned long long timeout_ns, cudaStream_t stream) {
+                             unsigned long long timeout_ns, cudaStream_t stream, bool clear_out_ids) {
     clear_error();
     if (B < 0 || k < 0 || V < 1 || R < 1) return fail(DSPARK_ERR_INVALID, "markov: bad sizes B=%d k=%d V=%d R=%d", B, k, V, R);
     if (R != 64 && R != 128 && R != 256)
@@ -42,7 +45,12 @@ dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
 
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    cudaError_t e = cudaMemsetAsync(ws, 0, workspace_bytes(k), stream);
+    cudaError_t e;
+    if (clear_out_ids) {  // every id -1 until the kernel writes it
+        e = cudaMemsetAsync(out_ids, 0xFF, size_t(B) * size_t(k) * sizeof(int64_t), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(out_ids)");
+    }
+    e = cudaMemsetAsync(ws, 0, workspace_bytes(k), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(markov workspace)");
     MarkovArgs args;
     args.base = base;
@@ -120,19 +128,61 @@ static __device__ __align__(256) unsigned char g_markov_noalloc_scratch[dspark::
 
 namespace dspark {
 namespace {
-// Device address of the scratch array, looked up once per device with that device current.
+using PFN_ctx_get_current = CUresult (*)(CUcontext *);
+using PFN_ctx_get_id = CUresult (*)(CUcontext, unsigned long long *);
+
+// Process-unique id of the calling thread's current CUDA context (0 if none is current
+// or the driver does not provide the query).  Ids are never reused, unlike context handles.
+unsigned long long current_context_id() {
+    static PFN_ctx_get_current get_current = nullptr;
+    static PFN_ctx_get_id get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_ctx_get_current>(f1);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_ctx_get_id>(f2);
+        looked_up = true;
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context.  It is looked up with
+// cudaGetSymbolAddress the first time a context uses the entry point (once per device in the
+// usual one-context-per-device process) and cached with that context's id; a different
+// context on the same device (a context the caller created, or the primary context again
+// after cudaDeviceReset) has its own copy of the array and gets its own lookup.
 dspark_status noalloc_scratch(void **out) {
-    static void *addr[64] = {nullptr};
+    struct Entry {
+        unsigned long long ctx_id;
+        void *addr;
+    };
+    static Entry cache[64] = {};
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(DSPARK_ERR_UNSUPPORTED, "markov_noalloc: device ordinal %d >= 64", dev);
-    void *p = __atomic_load_n(&addr[dev], __ATOMIC_ACQUIRE);
-    if (!p) {
-        e = cudaGetSymbolAddress(&p, g_markov_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(markov scratch)");
-        __atomic_store_n(&addr[dev], p, __ATOMIC_RELEASE);
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (id != 0 && cache[dev].ctx_id == id && cache[dev].addr) {
+        *out = cache[dev].addr;
+        return DSPARK_OK;
     }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_markov_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(markov scratch)");
+    // the lookup makes the runtime's context current if none was: key the cache on it
+    cache[dev].ctx_id = id != 0 ? id : current_context_id();
+    cache[dev].addr = p;
     *out = p;
     return DSPARK_OK;
 }
@@ -152,9 +202,12 @@ extern "C" dspark_status dspark_markov_draft_noalloc(const float *base_logits, c
     void *scratch = nullptr;
     dspark_status st = dspark::noalloc_scratch(&scratch);
     if (st != DSPARK_OK) return st;
+    // out_ids is set to -1 first: the status word in the static scratch cannot be read by the
+    // caller, so a position the kernel could not finish (a device-side wait that gave up)
+    // shows as -1 instead of a stale id
     return dspark::markov_enqueue(base_logits, markov_w1, markov_w2, d2t, prev, num_reqs, k, vocab, rank, out_ids,
                                   nullptr, nullptr, scratch, dspark::kNoAllocScratchBytes, 0u,
-                                  dspark::kDefaultTimeoutNs, reinterpret_cast<cudaStream_t>(stream));
+                                  dspark::kDefaultTimeoutNs, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" dspark_status dspark_markov_status(const void *workspace, dspark_stream_t stream) {

@@ -29,11 +29,12 @@ struct MarkovArgs {
 dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream);
 
 // Workspace bytes for k positions, and the checked enqueue behind every Markov entry point
-// (markov.cu): memset of the workspace header + the cooperative kernel, on `stream`.
+// (markov.cu): memset of the workspace header + the cooperative kernel, on `stream`; with
+// clear_out_ids, out_ids is first set to -1.
 size_t workspace_bytes(int k);
 dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16_t *w2, const int32_t *d2t,
                              int64_t *prev, int B, int k, int V, int R, int64_t *out_ids, float *dbg_logits,
                              float *dbg_bias, void *workspace, size_t ws_bytes, unsigned bar_extra,
-                             unsigned long long timeout_ns, cudaStream_t stream);
+                             unsigned long long timeout_ns, cudaStream_t stream, bool clear_out_ids = false);
 
 }  // namespace dspark

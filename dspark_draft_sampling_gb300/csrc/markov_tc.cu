@@ -302,7 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
                 }
                 named_bar_sync(1, kEpiThreads);
-                if (et < a.B && s_best[et] != 0ull && i + 1 < a.k) {
+                // A wait of this CTA gave up during the position: its keys miss tiles, so it
+                // neither contributes them nor arrives.  The other CTAs' barrier waits then run
+                // out too, and no id of this or a later position is written.
+                const bool self_broken = *reinterpret_cast<volatile int *>(s_abort) != 0;
+                if (!self_broken && et < a.B && s_best[et] != 0ull && i + 1 < a.k) {
                     // this CTA's candidate may be the winner: pull its markov_w1 row into L2 so
                     // the gather after the barrier is an L2 hit
                     const uint32_t cand = argmax_key_index(s_best[et]);
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int off = 0; off < R * 2; off += 128)
                         asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<const char *>(row) + off));
                 }
-                if (et == 0) {
+                if (et == 0 && !self_broken) {
                     for (int r = 0; r < a.B; ++r) {
                         const unsigned long long k_cta = s_best[r];
                         if (k_cta != 0ull) atomicMax(&a.best[size_t(i) * kMaxReqs + r], k_cta);

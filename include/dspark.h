@@ -136,11 +136,18 @@ void dspark_markov_plan_destroy(dspark_markov_plan *plan);
  *   loads the library holds its own copy until the process exits.  Each call clears it
  *   (a memset on `stream`) before the kernel.  All calls on one device share that copy:
  *   calls that overlap on the GPU (for example on two streams with no ordering between
- *   them) race and give undefined results, so serialize them.  The device status word
- *   lives in the same array and is not readable by the caller.
- *   Set-up: the first call on each device (with that device current) looks up the
- *   array's device address with cudaGetSymbolAddress and caches it; make that first call
- *   before any stream capture. */
+ *   them) race and give undefined results, so serialize them.
+ *   Errors seen only on the device: the status word lives in the same array and cannot be
+ *   read by the caller.  Instead, out_ids is set to -1 (a memset on `stream`) before the
+ *   kernel, so a position the kernel did not finish -- a device-side wait that gave up, or
+ *   an out-of-range prev / d2t entry -- reads -1; prev is only written when every position
+ *   finished.  Treat a draft with any -1 id as failed.
+ *   Set-up: the array's device address is looked up with cudaGetSymbolAddress the first
+ *   time a CUDA context (normally: once per device, with that device current) uses this
+ *   entry point, and cached with that context's id; a later context on the same device
+ *   (one the caller created, or the primary context after cudaDeviceReset) gets its own
+ *   lookup.  The first lookup may load the library's device code: make the first call in
+ *   each context before any stream capture. */
 dspark_status dspark_markov_draft_noalloc(const float *base_logits, const uint16_t *markov_w1,
                                           const uint16_t *markov_w2, const int32_t *d2t,
                                           int64_t *prev, int num_reqs, int k, int vocab, int rank,

@@ -282,3 +282,26 @@ def test_ws_grouped_host_validation(dspark_lib):
     assert g(p, 1, NULL, 1 << 20, NULL, NULL) == INVALID
     assert g(p, 1, FAKE_ODD, 1 << 20, NULL, NULL) == INVALID
     assert g(p, 0, NULL, 0, NULL, NULL) == 0
+
+
+def test_bench_library_exports_its_header():
+    """libdspark_bench.so (measurement kernels used by bench.py) exports what its header
+    declares."""
+    from dspark_draft_sampling_gb300 import build
+
+    build.build()
+    hdr = os.path.join(os.path.dirname(HEADER), "dspark_bench.h")
+    text = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(dspark_bench_[a-z0-9_]+)\s*\(", text)))
+    assert names == ["dspark_bench_empty", "dspark_bench_read"]
+    out = subprocess.run(["nm", "-D", "--defined-only", build.bench_lib_file()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (dspark_\w+)", out))
+    assert set(names) <= exported
+    lib = ctypes.CDLL(build.bench_lib_file())
+    # argument checks reject before launching anything (cudaErrorInvalidValue = 1)
+    lib.dspark_bench_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    assert lib.dspark_bench_read(FAKE, 24, 1, FAKE, 1, 32, NULL) == 1
+    assert lib.dspark_bench_read(FAKE_ODD, 32, 1, FAKE, 1, 32, NULL) == 1
+    assert lib.dspark_bench_read(FAKE, 32, 0, FAKE, 1, 32, NULL) == 1

@@ -46,6 +46,18 @@ def test_full_vocab_27b_lane(B):
     assert rep["n_exempt"] <= 1
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("B", [4, 8])
+def test_full_vocab_27b_lane_production_kernel(B):
+    """The kernel instantiation the benchmark times (no debug outputs) on the full 27B lane:
+    ids and the final prev against the oracle, with the near-tie exemption reported."""
+    inp = synth.markov_config("full_vocab_27b", num_reqs=B)
+    g = parity.gpu_markov(inp, dbg=False)
+    rep = parity.check_markov(inp, g, values=False)
+    print(f"num_reqs={B}: n_exempt={rep['n_exempt']} {rep['exempt']}")
+    assert rep["n_exempt"] <= 1
+
+
 @pytest.mark.parametrize("B,k,V,R,d2t", [
     (3, 5, 1000, 64, "identity"),
     (5, 3, 777, 128, "injective"),

@@ -47,6 +47,8 @@ def test_noalloc_matches_workspace_entry_two_calls(dspark_lib, lane, num_reqs):
         out_b = api.markov_draft(b["base"], b["w1"], b["w2"], b["d2t"], b["prev"], workspace=ws)
         torch.cuda.synchronize()
         assert api.markov_status(ws) == 0
+        # every position finished: the entry point sets out_ids to -1 before its kernel
+        assert (out_a >= 0).all()
         np.testing.assert_array_equal(out_a.cpu().numpy(), out_b.cpu().numpy())
         np.testing.assert_array_equal(a["prev"].cpu().numpy(), b["prev"].cpu().numpy())
         if call == 0:
@@ -65,9 +67,30 @@ def test_noalloc_at_its_limits(dspark_lib):
     out = torch.full((B, k), -7, dtype=torch.int64, device="cuda")
     _noalloc(lib, a, B, k, V, 128, out)
     torch.cuda.synchronize()
+    assert (out >= 0).all()
     rep = parity.check_markov(inp, dict(out_ids=out.cpu().numpy(), prev=a["prev"].cpu().numpy(), logits=None,
                                         bias=None, status=0), values=False)
     assert rep["n_exempt"] <= 2
+
+
+def test_noalloc_allocates_no_device_memory(dspark_lib):
+    """After a first call (which may load the library's device code), further calls leave the
+    device's free memory unchanged: the entry point itself allocates nothing."""
+    lib = dspark_lib
+    inp = synth.markov_config("tiny", seed=3)
+    B, k, V = inp["base"].shape
+    R = inp["w2"].shape[1]
+    t = parity.markov_to_device(inp)
+    out = torch.empty((B, k), dtype=torch.int64, device="cuda")
+    _noalloc(lib, t, B, k, V, R, out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        _noalloc(lib, t, B, k, V, R, out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert (out >= 0).all()
 
 
 def test_noalloc_rejects_too_many_positions(dspark_lib):
