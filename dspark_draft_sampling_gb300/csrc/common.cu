@@ -90,6 +90,14 @@ dspark_status make_tmap_kblocks(CUtensorMap *map, const void *base, bool bf16, u
                         CU_TENSOR_MAP_SWIZZLE_128B, base, 3, dims, strides, box);
 }
 
+dspark_status make_tmap_rows_f32(CUtensorMap *map, const float *base, uint64_t planes, uint64_t rows, uint64_t cols,
+                                 uint32_t box_planes, uint32_t box_cols) {
+    const cuuint64_t dims[3] = {cols, rows, planes};
+    const cuuint64_t strides[2] = {cols * 4, rows * cols * 4};
+    const cuuint32_t box[3] = {box_cols, 1, box_planes};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, base, 3, dims, strides, box);
+}
+
 dspark_status make_tmap_kblocks_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                                   uint32_t box_katoms) {
     const cuuint64_t dims[3] = {128, rows, cols / 128};

@@ -69,7 +69,7 @@ dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16
     args.V = V;
     args.bar_extra = bar_extra;
     args.timeout_ns = timeout_ns;
-    return launch_markov_tc(args, R, sms, stream);
+    return launch_markov_tc(args, R, markov_grid(V, sms), stream);
 }
 
 }  // namespace dspark

@@ -25,8 +25,11 @@ struct MarkovArgs {
     unsigned long long timeout_ns;
 };
 
-// tcgen05 form (markov_tc.cu): one CTA per SM, cooperative launch.
+// tcgen05 form (markov_tc.cu): at most one CTA per SM, cooperative launch.
 dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream);
+// Grid of the Markov kernel for a vocabulary of V rows on `sms` SMs: the fewest CTAs whose
+// largest share of 128-row tiles equals that of an even split over all SMs.
+int markov_grid(int V, int sms);
 
 // Workspace bytes for k positions, and the checked enqueue behind every Markov entry point
 // (markov.cu): memset of the workspace header + the cooperative kernel, on `stream`; with

@@ -10,26 +10,29 @@
 // Here it runs on the 5th-generation tensor cores; the SMs only stream markov_w2 and do the
 // argmax epilogue, so the cost no longer grows with the number of requests.
 //
-// GB300 design (one persistent CTA per SM, cooperative launch for the step barrier)
+// GB300 design (one persistent cooperative launch, one CTA per SM at most)
 //  * CTA c owns a contiguous range of 128-row tiles of markov_w2 for every position; odd
-//    positions walk it backwards so each position starts on rows still in L2.
-//  * Warp 4 (one thread): one 3-D TMA tensor copy per tile, the whole [128 rows x rank] bf16
-//    tile (64 KB at rank 256: rank/64 blocks of [128 x 64] in the 128-byte swizzle) into a
-//    192 KB ring of tile slots.  markov_w2 does not depend on prev, so it runs ahead across
-//    position boundaries.
+//    positions walk it backwards so each position starts on rows still in L2.  The grid is
+//    the fewest CTAs that give no CTA more tiles than an even split over all SMs would.
+//  * Warp 4 (one thread): per tile, one 3-D TMA tensor copy of the whole [128 rows x rank]
+//    bf16 tile (64 KB at rank 256: rank/64 blocks of [128 x 64] in the 128-byte swizzle) and
+//    one of the tile's base-logit rows for every request ([num_reqs x 128] fp32) into the same
+//    ring slot.  Neither depends on prev, so the producer runs ahead across positions.
 //  * Warp 5: allocates 32 TMEM columns (two 128 x 16 fp32 accumulators); one thread issues,
 //    per tile, rank/16 tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows,
 //    N = 16 request slots, K = 16) against H, which the epilogue warps write into shared
 //    memory in the same swizzled layout (rows >= num_reqs stay zero), then one
-//    tcgen05.commit that both frees the tile slot and hands the accumulator to the epilogue.
-//    One barrier round trip per 64 KB keeps the single issuing thread ahead of the stream.
-//  * Warps 0-3 (thread = TMEM lane = vocab row of the tile): tcgen05.ld the accumulator,
-//    add the base logits, keep the best (value, lowest index) key per request; at the end
-//    of a position reduce keys (warp shuffles, shared atomicMax, one global atomicMax per
-//    request), pass the grid barrier, read the winners, write out_ids / prev and build the
-//    next position's H from markov_w1.
+//    tcgen05.commit for the slot and one for the accumulator.
+//  * Warps 0-3 (thread = TMEM lane = vocab row of the tile): read the tile's base logits
+//    from the slot as soon as it lands (the slot is free again once both they and the MMAs
+//    are done with it), tcgen05.ld the accumulator, keep the best (value, row) per request;
+//    at the end of a position turn them into 64-bit keys and reduce (warp, shared atomicMax,
+//    one global atomicMax per request), pass the grid barrier, read the winners, write
+//    out_ids / prev and build the next position's H from markov_w1.
 // Products of bf16 values are exact in fp32; the tensor core accumulates in fp32.  Every
 // row's sum is computed the same way regardless of the grid and of num_reqs.
+#include <cmath>
+
 #include "markov.cuh"
 #include "tc.cuh"
 
@@ -38,16 +41,25 @@ namespace {
 
 constexpr int kThreads = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
 constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kTileRows = 128;
-constexpr int kKB = 64;                            // k per box (128 B of bf16)
-constexpr int kBoxBytes = kTileRows * kKB * 2;     // 16 KB: one 64-k block of a tile
-constexpr int kRingBytes = 12 * kBoxBytes;         // 192 KB of tile slots
-constexpr int kMaxSlots = kRingBytes / kBoxBytes;  // rank 64: 12 slots; rank 256: 3
-constexpr int kNPad = 16;                          // MMA N: request slots
-constexpr int kHBlockBytes = kNPad * kKB * 2;      // 2 KB per k-block of H
-constexpr int kHMaxBytes = 4 * kHBlockBytes;       // rank <= 256
+constexpr int kKB = 64;                          // k per box (128 B of bf16)
+constexpr int kBoxBytes = kTileRows * kKB * 2;   // 16 KB: one 64-k block of a tile
+constexpr int kRingBudget = 204 * 1024;          // tile slots: markov_w2 tile + its base rows
+constexpr int kMaxSlots = 12;
+constexpr int kNPad = 16;                        // MMA N: request slots
+constexpr int kHBlockBytes = kNPad * kKB * 2;    // 2 KB per k-block of H
+constexpr int kHMaxBytes = 4 * kHBlockBytes;     // rank <= 256
 constexpr uint32_t kTmemCols = 32;
-constexpr size_t kSmemBytes = 1024 + size_t(kRingBytes) + 2 * kHMaxBytes + 512;
+constexpr size_t kSmemBytes = 1024 + size_t(kRingBudget) + 2 * kHMaxBytes + 512;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+// Bytes reserved in a slot for the base rows of NB requests (a multiple of 1024, so the next
+// slot's markov_w2 blocks stay aligned for the 128-byte swizzle).
+template <int NB>
+constexpr int base_area_bytes() {
+    return (NB * kTileRows * 4 + 1023) / 1024 * 1024;
+}
 
 // Warp-wide max of 64-bit keys with two 32-bit redux.sync reductions: the max high word,
 // then the max low word among the lanes holding it.
@@ -60,18 +72,22 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 
 template <int NB, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
-    markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, MarkovArgs a, int R) {
+    markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmBase,
+                     MarkovArgs a, int R, int base_tma) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     unsigned char *ring = smem;
-    unsigned char *hbuf = smem + size_t(kRingBytes);  // 2 buffers
-    // full[s]: tile slot s landed.  empty[s]: the MMAs of the tile in slot s are done (one
-    // tcgen05.commit): the slot may be refilled and the tile's accumulator read.
+    unsigned char *hbuf = smem + size_t(kRingBudget);  // 2 buffers
+    // full[s]: slot s landed (tile and base rows).  empty[s]: the MMAs of the tile in slot s
+    // are done (one tcgen05.commit) and the four epilogue warps have read its base rows: the
+    // slot may be refilled.  acc_full[b]: accumulator b holds a finished tile (a commit).
+    // acc_empty[b]: the epilogue has read accumulator b.
     uint64_t *full = reinterpret_cast<uint64_t *>(hbuf + 2 * kHMaxBytes);
     uint64_t *empty = full + kMaxSlots;
-    uint64_t *acc_empty = empty + kMaxSlots;  // [2] accumulator drained by the epilogue
-    uint64_t *h_full = acc_empty + 2;      // [2]
+    uint64_t *acc_full = empty + kMaxSlots;  // [2]
+    uint64_t *acc_empty = acc_full + 2;      // [2]
+    uint64_t *h_full = acc_empty + 2;        // [2]
     unsigned long long *s_best = reinterpret_cast<unsigned long long *>(h_full + 2);  // [kMaxReqs]
     int *s_cur = reinterpret_cast<int *>(s_best + kMaxReqs);                          // [kMaxReqs]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_cur + kMaxReqs);
@@ -82,8 +98,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nctas = gridDim.x;
     const int cta = blockIdx.x;
     const int nkb = R / kKB;
-    const int slot_bytes = nkb * kBoxBytes;
-    const int nslots = kRingBytes / slot_bytes;
+    const int w2_bytes = nkb * kBoxBytes;
+    const int slot_bytes = w2_bytes + base_area_bytes<NB>();
+    const int nslots = min(kMaxSlots, kRingBudget / slot_bytes);
     const int T = (a.V + kTileRows - 1) / kTileRows;
     const int t0 = static_cast<int>(static_cast<long long>(cta) * T / nctas);
     const int t1 = static_cast<int>(static_cast<long long>(cta + 1) * T / nctas);
@@ -100,10 +117,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxSlots; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 1 + kEpiWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_empty[b], kEpiThreads / 32);
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiWarps);
             mbar_init(&h_full[b], kEpiThreads);
         }
         for (int r = 0; r < kMaxReqs; ++r) {
@@ -134,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint64_t pol;
             asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+            const uint64_t pol_base = l2_policy_evict_first();
+            const uint32_t tx = static_cast<uint32_t>(w2_bytes + (base_tma ? a.B * kTileRows * 4 : 0));
             int st = 0;
             uint32_t ph = 0;
             for (int i = 0; i < a.k; ++i)
@@ -143,8 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         atomicOr(a.status, kStatusTimeout);
                         goto producer_done;
                     }
-                    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(slot_bytes));
-                    tma_load_3d(ring + size_t(st) * slot_bytes, &tmW2, 0, y, 0, &full[st], pol);  // whole tile
+                    unsigned char *slot = ring + size_t(st) * slot_bytes;
+                    mbar_arrive_expect_tx(&full[st], tx);
+                    tma_load_3d(slot, &tmW2, 0, y, 0, &full[st], pol);  // whole tile
+                    if (base_tma) tma_load_3d(slot + w2_bytes, &tmBase, y, i, 0, &full[st], pol_base);
                     if (++st == nslots) {
                         st = 0;
                         ph ^= 1u;
@@ -190,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_f16(d, dA + 4, dB + 4, idesc, 1u);
                         tc_mma_f16(d, dA + 6, dB + 6, idesc, 1u);
                     }
-                    tc_commit(&empty[st]);  // frees the slot and hands the accumulator over
+                    tc_commit(&empty[st]);    // the MMAs no longer read the slot
+                    tc_commit(&acc_full[ab]);  // the accumulator holds the tile
                     if (++st == nslots) {
                         st = 0;
                         ph ^= 1u;
@@ -223,68 +246,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         build_h(0);
         mbar_arrive(&h_full[0]);
 
+        const unsigned live = (a.B >= 32 ? 0xffffffffu : ((1u << a.B) - 1u)) & ~bad_mask;
         bool aborted = false;  // CTA-uniform: no more computing or grid barriers, keep draining
-        bool broken = false;   // this thread's wait on an accumulator timed out
-        // Base logits do not depend on prev: they are loaded kBaseAhead tiles ahead of use
-        // (across position boundaries), so a tile's epilogue never waits on a DRAM round trip.
-        constexpr int kBaseAhead = 4;
-        float bq[kBaseAhead][NB];
-        int ip = 0, tp = 0;  // the next tile to prefetch, as (position, tile)
-        auto load_base = [&](float (&dst)[NB]) {
-            const int rowp = tile_at(ip, tp) * kTileRows + et;
-            const bool in = ntiles > 0 && ip < a.k && rowp < a.V;
-#pragma unroll
-            for (int r = 0; r < NB; ++r)
-                dst[r] = (in && r < a.B) ? __ldg(a.base + (size_t(r) * a.k + ip) * a.V + rowp) : 0.f;
-            if (++tp >= ntiles) {
-                tp = 0;
-                ++ip;
-            }
+        bool broken = false;   // one of this thread's waits timed out
+        auto give_up = [&]() {
+            broken = true;
+            atomicOr(a.status, kStatusTimeout);
+            *reinterpret_cast<volatile int *>(s_abort) = 1;
         };
-#pragma unroll
-        for (int q = 0; q < kBaseAhead; ++q) load_base(bq[q]);
         int tc = 0;
-        int es = 0;  // slot of tile tc, and the phase of its empty barrier
+        int es = 0;  // slot of tile tc, and the phase of its barriers
         uint32_t eph = 0;
         for (int i = 0; i < a.k; ++i) {
-            unsigned long long best[NB];
+            // best (value, row) per request over this thread's rows; rows are visited in
+            // increasing order on even positions and decreasing order on odd ones, so the
+            // lowest row among equal values is kept by > and >= respectively
+            float bval[NB];
+            int bidx[NB];
 #pragma unroll
-            for (int r = 0; r < NB; ++r) best[r] = 0ull;
+            for (int r = 0; r < NB; ++r) {
+                bval[r] = -INFINITY;
+                bidx[r] = -1;
+            }
+            const bool odd = (i & 1) != 0;
             for (int t = 0; t < ntiles; ++t, ++tc) {
                 const int ab = tc & 1;
+                const uint32_t abph = static_cast<uint32_t>(tc >> 1) & 1u;
                 const int row = tile_at(i, t) * kTileRows + et;
                 const bool valid = row < a.V && !aborted;
+                // the slot's base rows, read as soon as it lands
+                if (!broken && !mbar_wait(&full[es], eph, a.timeout_ns)) give_up();
                 float bv[NB];
+                if (base_tma) {
+                    const float *sb = reinterpret_cast<const float *>(ring + size_t(es) * slot_bytes + w2_bytes);
 #pragma unroll
-                for (int r = 0; r < NB; ++r) bv[r] = bq[0][r];
+                    for (int r = 0; r < NB; ++r) bv[r] = r < a.B ? sb[r * kTileRows + et] : 0.f;
+                } else {
 #pragma unroll
-                for (int q = 0; q + 1 < kBaseAhead; ++q)
-#pragma unroll
-                    for (int r = 0; r < NB; ++r) bq[q][r] = bq[q + 1][r];
-                load_base(bq[kBaseAhead - 1]);
-                if (!broken && !mbar_wait(&empty[es], eph, a.timeout_ns)) {
-                    broken = true;
-                    atomicOr(a.status, kStatusTimeout);
-                    *reinterpret_cast<volatile int *>(s_abort) = 1;
+                    for (int r = 0; r < NB; ++r)
+                        bv[r] = (r < a.B && row < a.V) ? __ldg(a.base + (size_t(r) * a.k + i) * a.V + row) : 0.f;
                 }
-                tc_fence_after();
-                uint32_t v[16];
-                tmem_ld_16(tmem + ab * kNPad + (static_cast<uint32_t>(warp * 32) << 16), v);
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                if (lane == 0) mbar_arrive(&empty[es]);
                 if (++es == nslots) {
                     es = 0;
                     eph ^= 1u;
                 }
+                if (!broken && !mbar_wait(&acc_full[ab], abph, a.timeout_ns)) give_up();
+                tc_fence_after();
+                uint32_t v[8];
+                tmem_ld_8(tmem + ab * kNPad + (static_cast<uint32_t>(warp * 32) << 16), v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 if (valid && !broken) {
 #pragma unroll
                     for (int r = 0; r < NB; ++r) {
-                        if (r < a.B && !((bad_mask >> r) & 1u)) {
+                        if ((live >> r) & 1u) {
                             const float bias = __uint_as_float(v[r]);
                             const float logit = bv[r] + bias;
-                            const unsigned long long key = argmax_key(logit, static_cast<uint32_t>(row));
-                            best[r] = key > best[r] ? key : best[r];
+                            const bool take = bidx[r] < 0 || (odd ? logit >= bval[r] : logit > bval[r]);
+                            bval[r] = take ? logit : bval[r];
+                            bidx[r] = take ? row : bidx[r];
                             if constexpr (DBG) {
                                 const size_t o = (size_t(r) * a.k + i) * a.V + row;
                                 if (a.dbg_logits) a.dbg_logits[o] = logit;
@@ -298,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- end of position: CTA max, global max, grid barrier, winner ----
 #pragma unroll
                 for (int r = 0; r < NB; ++r) {
-                    const unsigned long long k_w = warp_max_u64(best[r]);
+                    const unsigned long long key =
+                        bidx[r] >= 0 ? argmax_key(bval[r], static_cast<uint32_t>(bidx[r])) : 0ull;
+                    const unsigned long long k_w = warp_max_u64(key);
                     if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
                 }
                 named_bar_sync(1, kEpiThreads);
@@ -378,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NB, bool DBG>
-dspark_status launch_nb(const CUtensorMap &tm, const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
+dspark_status launch_nb(const CUtensorMap &tm, const CUtensorMap &tb, const MarkovArgs &args, int R, int base_tma,
+                        int nctas, cudaStream_t stream) {
     auto kern = markov_tc_kernel<NB, DBG>;
     static int configured_dev = -1;
     int dev = 0;
@@ -403,29 +429,46 @@ dspark_status launch_nb(const CUtensorMap &tm, const MarkovArgs &args, int R, in
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm, args, R);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm, tb, args, R, base_tma);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(markov_tc)");
     return DSPARK_OK;
 }
 
 template <bool DBG>
-dspark_status launch_dbg(const CUtensorMap &tm, const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
-    if (args.B <= 1) return launch_nb<1, DBG>(tm, args, R, nctas, stream);
-    if (args.B <= 2) return launch_nb<2, DBG>(tm, args, R, nctas, stream);
-    if (args.B <= 4) return launch_nb<4, DBG>(tm, args, R, nctas, stream);
-    return launch_nb<8, DBG>(tm, args, R, nctas, stream);
+dspark_status launch_dbg(const CUtensorMap &tm, const CUtensorMap &tb, const MarkovArgs &args, int R, int base_tma,
+                         int nctas, cudaStream_t stream) {
+    if (args.B <= 1) return launch_nb<1, DBG>(tm, tb, args, R, base_tma, nctas, stream);
+    if (args.B <= 2) return launch_nb<2, DBG>(tm, tb, args, R, base_tma, nctas, stream);
+    if (args.B <= 4) return launch_nb<4, DBG>(tm, tb, args, R, base_tma, nctas, stream);
+    return launch_nb<8, DBG>(tm, tb, args, R, base_tma, nctas, stream);
 }
 
 }  // namespace
 
+int markov_grid(int V, int sms) {
+    const int T = (V + kTileRows - 1) / kTileRows;
+    const int per = (T + sms - 1) / sms;  // most tiles any CTA gets with all SMs in use
+    return (T + per - 1) / per;           // the fewest CTAs that keep that maximum
+}
+
 dspark_status launch_markov_tc(const MarkovArgs &args, int R, int nctas, cudaStream_t stream) {
     if (R % kKB != 0 || R > 256) return fail(DSPARK_ERR_UNSUPPORTED, "markov_tc: rank %d", R);
-    CUtensorMap tm;
+    CUtensorMap tm, tb;
     dspark_status st = make_tmap_kblocks(&tm, args.w2, true, static_cast<uint64_t>(args.V), static_cast<uint64_t>(R),
                                          kTileRows, static_cast<uint32_t>(R / kKB));
     if (st != DSPARK_OK) return st;
-    if (args.dbg_logits || args.dbg_bias) return launch_dbg<true>(tm, args, R, nctas, stream);
-    return launch_dbg<false>(tm, args, R, nctas, stream);
+    // base rows by TMA when the tensor map can describe them (row stride a multiple of 16
+    // bytes, 16-byte aligned base); otherwise the epilogue loads them itself
+    const int base_tma = (args.V % 4 == 0 && aligned(args.base, 16)) ? 1 : 0;
+    if (base_tma) {
+        st = make_tmap_rows_f32(&tb, args.base, static_cast<uint64_t>(args.B), static_cast<uint64_t>(args.k),
+                                static_cast<uint64_t>(args.V), static_cast<uint32_t>(args.B), kTileRows);
+        if (st != DSPARK_OK) return st;
+    } else {
+        tb = tm;  // unused
+    }
+    if (args.dbg_logits || args.dbg_bias) return launch_dbg<true>(tm, tb, args, R, base_tma, nctas, stream);
+    return launch_dbg<false>(tm, tb, args, R, base_tma, nctas, stream);
 }
 
 }  // namespace dspark

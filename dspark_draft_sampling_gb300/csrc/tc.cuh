@@ -27,6 +27,12 @@ dspark_status make_tmap_kblocks_u8(CUtensorMap *map, const void *base, uint64_t 
 dspark_status make_tmap_kblocks(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
                                 uint32_t box_rows, uint32_t box_kblocks);
 
+// 3-D view of a row-major fp32 array [planes, rows, cols] (cols a multiple of 4, base 16-byte
+// aligned): one box = box_cols consecutive columns of one row in each of box_planes planes,
+// stored plane after plane without swizzle.  Out-of-range elements read as zero.
+dspark_status make_tmap_rows_f32(CUtensorMap *map, const float *base, uint64_t planes, uint64_t rows, uint64_t cols,
+                                 uint32_t box_planes, uint32_t box_cols);
+
 // ---- device ----------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads, TMA).
@@ -104,6 +110,15 @@ __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t (&v)[16]) {
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr)
         : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 8 consecutive 32-bit columns, waited for.
+__device__ __forceinline__ void tmem_ld_8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 

@@ -178,6 +178,19 @@ def ws_inputs(M: int, N: int, K: int, *, seed: int = 0, w_sd: float = 0.02,
     return dict(W=W, X=X, M=M, N=N, K=K)
 
 
+def ws_exact_inputs(M: int, N: int, K: int, *, seed: int = 0) -> dict:
+    """Weight-stationary matvec inputs whose products and partial sums are all exact in fp32:
+    X integers in [-3, 3], W = k / 1024 with integer k in [-127, 127] (both exact in fp16).
+    Every partial sum is a multiple of 2^-10 below K * 381 * 2^-10 in magnitude, exact in fp32
+    while K * 381 < 2^24 (K <= 44034)."""
+    if K * 381 >= (1 << 24):
+        raise ValueError("K too large for exact fp32 partial sums")
+    x = _rng(seed, _S_WSX).integers(-3, 4, size=(M, K)).astype(np.float32)
+    w = (_rng(seed, _S_WSW).integers(-127, 128, size=(N, K), dtype=np.int16).astype(np.float32)
+         * np.float32(1.0 / 1024.0))
+    return dict(W=f32_to_f16_bits(w), X=f32_to_f16_bits(x), M=M, N=N, K=K)
+
+
 def ws_q8_inputs(M: int, N: int, K: int, *, seed: int = 0, d_sd: float = 2e-4,
                  power_of_two_scales: bool = False) -> dict:
     """Inputs of a quantized weight-stationary matvec: W as Q8_0 blocks (row-major by weight

@@ -35,6 +35,23 @@ def test_qwen3_8b_projection_shapes(K, N):
     parity.check_ws(inp, y32=y32, y16=y16)
 
 
+@pytest.mark.parametrize("K,N", synth.WS_SHAPES)
+def test_exact_inputs_fp16_is_the_oracles_rne(K, N):
+    """Inputs whose every partial sum is exact in fp32: any correct accumulation order gives
+    Y itself, so the fp32 output must equal the oracle's Y and the fp16 output the oracle's
+    RNE(Y), bit for bit -- including values exactly halfway between two fp16 numbers."""
+    inp = synth.ws_exact_inputs(7, N, K, seed=K + N)
+    y32, y16 = _run(inp)
+    rep = parity.check_ws(inp, y32=y32, y16=y16, exact=True)
+    Y, Y16 = parity.oracle.ws_matvec(inp["W"], inp["X"])
+    h = Y16.view(np.float16).astype(np.float64)
+    up = np.nextafter(Y16.view(np.float16), np.float16(np.inf)).astype(np.float64)
+    n_rounded = int((h != Y).sum())
+    n_ties = int((np.abs(Y - h) == (up - h) / 2).sum())
+    print(f"{K}x{N}: {rep['fp16_total']} outputs, {n_rounded} rounded, {n_ties} exact ties")
+    assert n_rounded > rep["fp16_total"] // 4 and n_ties > 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 8), (2, 100, 64), (3, 1000, 2056), (5, 153, 4104),
                                    (8, 4096, 512), (9, 300, 1024), (16, 777, 4096), (7, 1, 12288),
                                    (4, 5000, 8)])

@@ -193,24 +193,48 @@ def test_an_issuer_count_that_does_not_divide_the_slots_is_caught(issuers):
 MARKOV_SRC = os.path.join(os.path.dirname(SRC), "markov_tc.cu")
 
 
-def markov_slots(rank):
-    """Tile slots of the Markov kernel's ring at this rank (the ring holds kRingBytes of
-    [128 x rank] bf16 tiles, one 16 KB box per 64 columns)."""
-    m = re.search(r"constexpr int kRingBytes = (\d+) \* kBoxBytes;", open(MARKOV_SRC).read())
-    assert m
-    return int(m.group(1)) // (rank // 64)
+def markov_slots(rank, nb=8):
+    """Tile slots of the Markov kernel's ring at this rank and request count: kRingBudget
+    bytes of slots, each one [128 x rank] bf16 tile (one 16 KB box per 64 columns) plus the
+    tile's base rows (nb x 128 fp32, rounded up to 1 KB), at most kMaxSlots."""
+    text = open(MARKOV_SRC).read()
+    budget = re.search(r"constexpr int kRingBudget = (\d+) \* 1024;", text)
+    cap = re.search(r"constexpr int kMaxSlots = (\d+);", text)
+    assert budget and cap
+    slot = (rank // 64) * 16384 + (nb * 128 * 4 + 1023) // 1024 * 1024
+    return min(int(cap.group(1)), int(budget.group(1)) * 1024 // slot)
 
 
-def run_markov(nslots, k, ntiles, rng):
+class Barrier2(Barrier):
+    """An mbarrier whose phase completes after `count` arrivals."""
+
+    def __init__(self, count):
+        super().__init__()
+        self.count = count
+        self.arrived = 0
+
+    def arrive(self):
+        self.arrived += 1
+        if self.arrived == self.count:
+            self.arrived = 0
+            self.completed += 1
+
+
+def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
     """One random interleaving of the Markov kernel's roles for one CTA: the TMA producer
-    (one copy per tile, running ahead across positions), the MMA issuer (per position: wait
-    for H; per tile: wait for its accumulator to be drained, then for the tile), the epilogue
-    (per tile: wait for the commit that frees the slot and hands over the accumulator; after
-    the last tile of a position: the next position's H).  Returns an error string or None."""
+    (one copy of tile + base rows per slot, running ahead across positions), the MMA issuer
+    (per position: wait for H; per tile: wait for its accumulator to be drained, then for the
+    slot; its completion commits to the slot and to the accumulator), and each epilogue warp
+    (per tile: wait for the slot to land, read the base rows and arrive on the slot's empty
+    barrier, wait for the accumulator, read it and arrive on its empty barrier; after the last
+    tile of a position: the next position's H).  The slot's empty barrier completes after the
+    commit and every epilogue warp (with epilogue_holds_slot=False, after the commit alone).
+    Returns an error string or None."""
     full = [Barrier() for _ in range(nslots)]
-    empty = [Barrier() for _ in range(nslots)]  # one commit per tile: slot free + accumulator ready
-    acc_empty = [Barrier() for _ in range(2)]
-    h_full = [Barrier() for _ in range(2)]
+    empty = [Barrier2(1 + (epi_warps if epilogue_holds_slot else 0)) for _ in range(nslots)]
+    acc_full = [Barrier() for _ in range(2)]
+    acc_empty = [Barrier2(epi_warps) for _ in range(2)]
+    h_full = [Barrier2(epi_warps) for _ in range(2)]
     h_full[0].completed = 1  # the epilogue builds position 0's H before the loop
     total = k * ntiles
     error = None
@@ -223,7 +247,8 @@ def run_markov(nslots, k, ntiles, rng):
             error = f"{who}: passed with {bar.completed} completed phases, wanted {kk + 1}"
         return True
 
-    st = dict(prod=0, mma=0, mma_w=0, epi=0)
+    st = dict(prod=0, mma=0, mma_w=0)
+    epi = [dict(q=0, step=0) for _ in range(epi_warps)]
     pending_land, pending_mma = [], []
 
     def producer():
@@ -259,17 +284,26 @@ def run_markov(nslots, k, ntiles, rng):
         st["mma_w"] = 0
         return True
 
-    def epilogue():
-        q = st["epi"]
+    def epilogue(w):
+        e = epi[w]
+        q = e["q"]
         if q >= total:
             return False
-        if not wait(empty[q % nslots], q // nslots, f"epilogue tile {q}"):
+        if e["step"] == 0:  # slot landed: read the base rows, release the slot
+            if not wait(full[q % nslots], q // nslots, f"epilogue warp {w} tile {q} (base rows)"):
+                return False
+            if epilogue_holds_slot:
+                empty[q % nslots].arrive()
+            e["step"] = 1
+            return True
+        if not wait(acc_full[q & 1], q >> 1, f"epilogue warp {w} tile {q} (accumulator)"):
             return False
-        acc_empty[q & 1].completed += 1
+        acc_empty[q & 1].arrive()
         i, t = divmod(q, ntiles)
         if t == ntiles - 1 and i + 1 < k:
-            h_full[(i + 1) & 1].completed += 1
-        st["epi"] += 1
+            h_full[(i + 1) & 1].arrive()
+        e["q"] += 1
+        e["step"] = 0
         return True
 
     def land(x):
@@ -281,11 +315,12 @@ def run_markov(nslots, k, ntiles, rng):
         if x != 0:  # one issuer: its commits complete in issue order
             return False
         q = pending_mma.pop(0)
-        empty[q % nslots].completed += 1
+        empty[q % nslots].arrive()
+        acc_full[q & 1].completed += 1
         return True
 
     while error is None:
-        actions = [producer, issuer, epilogue]
+        actions = [producer, issuer] + [lambda w=w: epilogue(w) for w in range(epi_warps)]
         actions += [lambda x=x: land(x) for x in range(len(pending_land))]
         actions += [lambda x=x: mma_complete(x) for x in range(len(pending_mma))]
         rng.shuffle(actions)
@@ -293,14 +328,15 @@ def run_markov(nslots, k, ntiles, rng):
             break
     if error:
         return error
-    if st["epi"] < total:
-        return f"deadlock: epilogue at tile {st['epi']} of {total}"
+    if any(e["q"] < total for e in epi):
+        return f"deadlock: epilogue at tiles {[e['q'] for e in epi]} of {total}"
     return None
 
 
 @pytest.mark.parametrize("rank", [64, 128, 256])
 def test_markov_protocol_is_exact_under_random_interleavings(rank):
     nslots = markov_slots(rank)
+    assert nslots == {64: 10, 128: 5, 256: 3}[rank]
     rng = random.Random(rank)
     for _ in range(150):
         k = rng.randint(1, 6)
@@ -309,9 +345,10 @@ def test_markov_protocol_is_exact_under_random_interleavings(rank):
         assert err is None, (rank, nslots, k, ntiles, err)
 
 
-def test_markov_model_catches_a_one_slot_ring():
-    # with one slot the producer's and the epilogue's waits on the same barrier can be two
-    # phases apart: the model must see it (and the kernel never runs with fewer than 3)
+def test_markov_model_catches_a_slot_freed_by_the_mma_alone():
+    # if the MMAs' commit alone freed a slot, the producer could refill it before a slow
+    # epilogue warp has read the tile's base rows; the model must see that wait pass a phase
+    # late, and the kernel's ring must keep at least three slots
     rng = random.Random(7)
-    assert any(run_markov(1, 4, 6, rng) for _ in range(300))
-    assert min(markov_slots(r) for r in (64, 128, 256)) >= 2
+    assert any(run_markov(3, 4, 6, rng, epilogue_holds_slot=False) for _ in range(300))
+    assert min(markov_slots(r, nb) for r in (64, 128, 256) for nb in (1, 2, 4, 8)) >= 3
