@@ -509,17 +509,29 @@ def run_next_rows(dev, reps: int = 20):
         return (torch.randn(shape, generator=gen, device=dev) * sd).half()
 
     out = {}
-    # Q8_0 projections, M = 7
-    q8_us, q8_bytes = 0.0, 0
+    # Q8_0 projections, M = 7: each shape alone, and the four back to back in one timed region
+    # (a layer's projections: programmatic dependent launch overlaps each launch's prologue
+    # with the previous one's tail)
+    q8_us, q8_bytes, q8_calls = 0.0, 0, []
     for (K, N) in synth.WS_SHAPES:
         q, d = q8_weights(N, K)
         X = f16((7, K), 1.0)
         Y = torch.empty((7, N), dtype=torch.float16, device=dev)
         wsq = api.new_ws_q8_workspace(7, N, K, dev)
-        q8_us += timed(lambda: api.ws_matvec_q8(q, d, X, out=Y, workspace=wsq, stream=stream))
-        q8_bytes += N * K + N * (K // 32) * 2 + 7 * K * 2 + 7 * N * 2
+        call = (lambda q=q, d=d, X=X, Y=Y, wsq=wsq: api.ws_matvec_q8(q, d, X, out=Y, workspace=wsq, stream=stream))
+        us = timed(call)
+        nb = N * K + N * (K // 32) * 2 + 7 * K * 2 + 7 * N * 2
+        out[f"ws_q8_m7_{K}x{N}_us"] = us
+        out[f"ws_q8_m7_{K}x{N}_frac_of_hbm"] = nb / (us * 1e-6) / 1e9 / peak
+        q8_us += us
+        q8_bytes += nb
+        q8_calls.append(call)
     out["ws_q8_qwen3_8b_4_shapes_us"] = q8_us
     out["ws_q8_qwen3_8b_GBps"] = q8_bytes / (q8_us * 1e-6) / 1e9
+    seq = timed(lambda: [c() for c in q8_calls])
+    out["ws_q8_qwen3_8b_4_shapes_back_to_back_us"] = seq
+    out["ws_q8_qwen3_8b_back_to_back_frac_of_hbm"] = q8_bytes / (seq * 1e-6) / 1e9 / peak
+    del q8_calls
     K, N = 4096, 151936
     q, d = q8_weights(N, K)
     X = f16((7, K), 1.0)
@@ -653,7 +665,47 @@ def run_configs(dev, mk27, reps: int = 30):
         stream.synchronize()
         if r >= 3:
             lat.append((time.perf_counter() - t0) * 1e6)
-    out["probe_latency_1_with_4B_readback"] = {"us_host_clock": stats(lat)}
+    out["probe_latency_1_with_4B_readback"] = {"us_host_clock": stats(lat),
+                                                "how": "launch, 4-byte cudaMemcpyAsync to pinned memory, stream sync"}
+    # the same probe with the gate stored by the kernel straight into pinned host memory and
+    # the host polling that word: no copy and no stream synchronization on the host path
+    g_map = torch.empty(1, dtype=torch.int32).pin_memory()
+    g_np = g_map.numpy()
+    lat = []
+    for r in range(reps + 3):
+        g_np[0] = -1
+        t0 = time.perf_counter()
+        api.conf_probe(wq, h1, pr["bias"], pr["threshold"], gate_out=g_map, stream=stream)
+        while g_np[0] == -1:
+            pass
+        if r >= 3:
+            lat.append((time.perf_counter() - t0) * 1e6)
+    stream.synchronize()
+    out["probe_latency_1_mapped_gate"] = {"us_host_clock": stats(lat),
+                                          "how": "api.conf_probe (Python wrapper), the kernel stores the gate "
+                                                 "into pinned host memory, the host polls the 4-byte word"}
+    # the same through the C ABI with the arguments marshalled once (what a C caller pays)
+    import ctypes
+
+    lib = api.load_library()
+    cargs = (ctypes.c_void_p(wq.data_ptr()), ctypes.c_void_p(h1.data_ptr()), ctypes.c_float(pr["bias"]),
+             ctypes.c_float(pr["threshold"]), synth.PROBE_K, 1, None, ctypes.c_void_p(g_map.data_ptr()),
+             ctypes.c_void_p(stream.cuda_stream))
+    fn = lib.dspark_conf_probe
+    lat = []
+    for r in range(reps + 3):
+        g_np[0] = -1
+        t0 = time.perf_counter()
+        rc = fn(*cargs)
+        while g_np[0] == -1:
+            pass
+        if r >= 3:
+            lat.append((time.perf_counter() - t0) * 1e6)
+        assert rc == 0
+    stream.synchronize()
+    out["probe_latency_1_mapped_gate_c_abi"] = {"us_host_clock": stats(lat),
+                                                "how": "dspark_conf_probe through ctypes with prepared arguments, "
+                                                       "gate stored into pinned host memory, host polls"}
     for (K, N) in synth.WS_SHAPES:
         w = synth.ws_inputs(7, N, K)
         W = torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16)

@@ -113,13 +113,14 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _ptr(t, name: str, *, dtypes=None, itemsize=None, allow_none=False):
+def _ptr(t, name: str, *, dtypes=None, itemsize=None, allow_none=False, allow_pinned=False):
     if t is None:
         if allow_none:
             return None
         raise ValueError(f"{name} is required")
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    pinned_ok = allow_pinned and isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned()
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or pinned_ok):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if allow_pinned else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtypes is not None and t.dtype not in dtypes:
@@ -330,6 +331,8 @@ class GatedDraftPlan:
 def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gate_out=None,
                stream=None):
     """Q8_0 confidence probes.  wq uint8 [K/32*34], hidden fp32 [n, K] (or [K]).
+    gate_out may be a pinned host tensor: the kernel then stores each 4-byte decision
+    straight into host memory (the device reaches pinned memory by the same address).
     Returns (logit_out [n] fp32, gate_out [n] int32)."""
     lib = load_library()
     if hidden.dim() == 1:
@@ -339,13 +342,13 @@ def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gat
         raise ValueError("wq must hold K/32 Q8_0 blocks of 34 bytes")
     if gate_out is None:
         gate_out = torch.empty(n, dtype=torch.int32, device=hidden.device)
-    if logit_out is None:
+    if logit_out is None and gate_out.is_cuda:
         logit_out = torch.empty(n, dtype=torch.float32, device=hidden.device)
     st = lib.dspark_conf_probe(_ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)),
                                _ptr(hidden, "hidden", dtypes=(torch.float32,)),
                                float(bias), float(threshold), K, n,
-                               _ptr(logit_out, "logit_out", dtypes=(torch.float32,)),
-                               _ptr(gate_out, "gate_out", dtypes=(torch.int32,)),
+                               _ptr(logit_out, "logit_out", dtypes=(torch.float32,), allow_none=True),
+                               _ptr(gate_out, "gate_out", dtypes=(torch.int32,), allow_pinned=True),
                                _stream(stream))
     _check(lib, st)
     return logit_out, gate_out

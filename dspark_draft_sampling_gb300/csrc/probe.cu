@@ -4,10 +4,13 @@
 // "Root cause"): a 7424-wide matvec of the hidden vector against Q8_0 weights, run on
 // the GPU so that only a 4-byte gate decision crosses to the host.
 //
-// One CTA per probe.  Threads stride over 16-byte chunks of the hidden vector (one
-// vector load each), dequantize the matching four int8 weights with their block's fp16
-// scale exactly in fp32, and accumulate; a fixed warp butterfly plus an in-order sum of
-// the eight warp totals gives z, so the result does not depend on scheduling.  The gate
+// One CTA of 256 threads per probe.  Thread t walks the 16-byte chunks t, t + 256, ... of the
+// hidden vector (one vector load each), dequantizes the matching four int8 weights with their
+// block's fp16 scale exactly in fp32, and accumulates in chunk order; a fixed warp butterfly
+// plus an in-order sum of the eight warp totals gives z.  Two load schedules, the same
+// arithmetic in the same order (so the same bits): for a large batch a loop unrolled four
+// times (many CTAs resident, few registers each), for a small batch or a single probe every
+// chunk load of a thread issued before any is used (one memory latency per probe).  The gate
 // compares z with logit(threshold) (computed on the host), which is the same decision as
 // sigmoid(z) >= threshold without evaluating an exponential on the device.
 #include <cuda_fp16.h>
@@ -21,16 +24,35 @@ namespace {
 
 constexpr int kProbeThreads = 256;
 constexpr int kProbeWarps = kProbeThreads / 32;
+constexpr int kAhead = 8;  // small batches: chunk loads per thread in flight together
 
 __device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
     const uint4 u = ldg_nc_v4(p);
     return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
 }
 
+// acc += d * (q0 x0 + q1 x1 + q2 x2 + q3 x3) for chunk c, the weights read from its Q8_0 block
+__device__ __forceinline__ float probe_chunk(const uint8_t *__restrict__ wq, int c, float4 xv, float acc) {
+    const uint8_t *blk = wq + size_t(c >> 3) * 34;
+    const int off = 2 + 4 * (c & 7);
+    const unsigned short dbits = static_cast<unsigned short>(__ldg(blk) | (__ldg(blk + 1) << 8));
+    const float d = __half2float(__ushort_as_half(dbits));
+    const float q0 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 0)));
+    const float q1 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 1)));
+    const float q2 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 2)));
+    const float q3 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 3)));
+    float s = q0 * xv.x;
+    s = fmaf(q1, xv.y, s);
+    s = fmaf(q2, xv.z, s);
+    s = fmaf(q3, xv.w, s);
+    return fmaf(d, s, acc);
+}
+
 // The probe's input vector may come in two pieces (the hidden state and the Markov
 // state): chunk c < nchunks_a reads piece a, the rest read piece b.  With one piece
 // (nchunks_b == 0) this is the plain contiguous probe; the chunk order, and so every
 // rounding, is the same either way.
+template <bool kAllAhead>
 __global__ void __launch_bounds__(kProbeThreads)
     conf_probe_kernel(const uint8_t *__restrict__ wq, const float *__restrict__ xa, long long lda, int nchunks_a,
                       const float *__restrict__ xb, long long ldb, int nchunks_b, float bias, float t_logit,
@@ -41,23 +63,25 @@ __global__ void __launch_bounds__(kProbeThreads)
     const float *pa = xa + size_t(blockIdx.x) * lda;
     const float *pb = xb ? xb + size_t(blockIdx.x) * ldb : nullptr;
     const int nchunks = nchunks_a + nchunks_b;  // 4 floats per chunk; a Q8_0 block spans 8 chunks
+    auto chunk_ptr = [&](int c) { return c < nchunks_a ? pa + 4 * c : pb + 4 * (c - nchunks_a); };
     float acc = 0.f;
+    if constexpr (kAllAhead) {
+        for (int c0 = threadIdx.x; c0 < nchunks; c0 += kAhead * kProbeThreads) {
+            float4 xv[kAhead];
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u) {
+                const int c = c0 + u * kProbeThreads;
+                xv[u] = c < nchunks ? ldg_stream_f4(chunk_ptr(c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u) {
+                const int c = c0 + u * kProbeThreads;
+                if (c < nchunks) acc = probe_chunk(wq, c, xv[u], acc);
+            }
+        }
+    } else {
 #pragma unroll 4
-    for (int c = threadIdx.x; c < nchunks; c += kProbeThreads) {
-        const float4 xv = ldg_stream_f4(c < nchunks_a ? pa + 4 * c : pb + 4 * (c - nchunks_a));
-        const uint8_t *blk = wq + size_t(c >> 3) * 34;
-        const int off = 2 + 4 * (c & 7);
-        const unsigned short dbits = static_cast<unsigned short>(__ldg(blk) | (__ldg(blk + 1) << 8));
-        const float d = __half2float(__ushort_as_half(dbits));
-        const float q0 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 0)));
-        const float q1 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 1)));
-        const float q2 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 2)));
-        const float q3 = static_cast<float>(static_cast<int8_t>(__ldg(blk + off + 3)));
-        float s = q0 * xv.x;
-        s = fmaf(q1, xv.y, s);
-        s = fmaf(q2, xv.z, s);
-        s = fmaf(q3, xv.w, s);
-        acc = fmaf(d, s, acc);
+        for (int c = threadIdx.x; c < nchunks; c += kProbeThreads) acc = probe_chunk(wq, c, ldg_stream_f4(chunk_ptr(c)), acc);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -103,14 +127,20 @@ dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long lo
     const float t_logit = static_cast<float>(std::log(t / (1.0 - t)));
     const uint8_t *wb = static_cast<const uint8_t *>(w_q8_0);
     const float *xbp = Kb > 0 ? xb : nullptr;
+    // all loads of a thread in flight together while the batch fits in one wave of CTAs
+    int sms = 0;
+    int rc = current_sm_count(&sms);
+    if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
+    const bool ahead = n_probes <= 8 * sms;
+    auto kern = ahead ? conf_probe_kernel<true> : conf_probe_kernel<false>;
     cudaError_t e;
     if (set_cond) {  // inside a conditional graph: plain launch
-        conf_probe_kernel<<<n_probes, kProbeThreads, 0, stream>>>(wb, xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit,
-                                                                  logit_out, gate_out, cond, set_cond);
+        kern<<<n_probes, kProbeThreads, 0, stream>>>(wb, xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit, logit_out,
+                                                     gate_out, cond, set_cond);
         e = cudaGetLastError();
     } else {
-        e = launch_pdl(conf_probe_kernel, dim3(static_cast<unsigned>(n_probes)), dim3(kProbeThreads), 0, stream, wb,
-                       xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit, logit_out, gate_out, cond, set_cond);
+        e = launch_pdl(kern, dim3(static_cast<unsigned>(n_probes)), dim3(kProbeThreads), 0, stream, wb, xa, lda,
+                       Ka / 4, xbp, ldb, Kb / 4, bias, t_logit, logit_out, gate_out, cond, set_cond);
     }
     if (e != cudaSuccess) return cuda_fail(e, "conf_probe launch");
     return DSPARK_OK;

@@ -8,21 +8,28 @@
 // tensor cores, which leaves the SMs free to keep the stream going.
 //
 // GB300 design
-//  * Work unit = (128 weight rows, a contiguous range of 64-wide k-blocks).  K is split so
-//    that there is about one unit per SM.
+//  * Work unit = (128 weight rows, a contiguous range of 64-wide k-blocks).  The split of K
+//    per row block (S units) and the CTAs per SM (1 with a 10-stage ring, 2 with 5 stages)
+//    are chosen per shape so that one wave of CTAs covers every unit with the smallest
+//    largest load on any SM.
 //  * Warp 4 (one thread) streams, per k-block, the W tile [128 rows x 64 k] (16 KB) and
 //    the X tile [16 rows x 64 k] (2 KB; rows >= M read as zero) with 2-D TMA tensor copies
-//    in the 128-byte-swizzled layout, through an mbarrier ring: 10 stages (180 KB, one CTA
-//    per SM) when the launch has at most one unit per SM, else 5 (two CTAs per SM).
+//    in the 128-byte-swizzled layout, through an mbarrier ring.  It initializes the barriers
+//    and issues the first ring's worth of copies before the CTA-wide set-up (TMEM allocation,
+//    the CTA barrier), so the first tile's DRAM latency overlaps that set-up.
 //  * Warp 5 allocates 32 TMEM columns and one thread issues, per k-block, four
 //    tcgen05.mma kind::f16 (M=128, N=16, K=16; fp16 in, fp32 accumulate) into TMEM.
 //    tcgen05.commit frees each stage once its MMAs are done, and signals the epilogue
 //    after the last one.
 //  * Warps 0-3 (128 threads, one TMEM lane = one weight row each) load the 128 x 16
-//    accumulator tile with tcgen05.ld.  With one unit per row block they write Y directly;
-//    otherwise they store the fp32 partial tile, and the last unit of the row block (a
-//    ticket counter) sums the partials in unit order, so the result is deterministic and
-//    does not depend on M.
+//    accumulator tile with tcgen05.ld.  With one unit per row block they write Y directly.
+//    Otherwise the S units of a row block reduce their fp32 partials in a fixed order,
+//    0 + p_0 + p_1 + ... + p_{S-1}, so the result is deterministic and does not depend on M:
+//    in a single-problem launch the S units form a thread-block cluster and units 1..S-1
+//    store their partial rows into unit 0's shared memory (distributed shared memory), one
+//    cluster barrier, then unit 0 sums and writes Y; in a grouped launch (several problems,
+//    CTAs of different problems in one grid) the partials go through the caller's workspace
+//    and the last unit of the row block (a ticket counter) sums them.  Both give the same bits.
 #include <cuda_fp16.h>
 
 #include "tc.cuh"
@@ -31,16 +38,13 @@ namespace dspark {
 namespace {
 
 constexpr int kThreads = 192;      // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
-// Ring depth, chosen per launch.  With at most one unit per SM, 10 x 18 KB stages and one CTA
-// per SM (measured best on GB300 among {5, 8, 10, 12} stages x {1, 2, 4} units per SM for the
-// four Qwen3-8B projection shapes).  With more units than SMs (a grouped launch, a large N)
-// each SM runs several CTAs in turn, and each CTA spends microseconds on its setup, its first
-// copies and its epilogue with the stream idle; 5 stages let two CTAs share an SM, so one
-// streams while the other starts or finishes (measured on the grouped projections: 53.0 ->
-// 48.7 us; on a 151936 x 4096 matrix 187 -> 182 us).
+// Ring depth per launch: 10 x 18 KB stages with one CTA per SM, 5 stages with two (each SM
+// then overlaps one CTA's fixed costs with the other's stream; measured on the grouped
+// projections 53.0 -> 48.7 us, on a 151936 x 4096 matrix 187 -> 182 us), fewer when a
+// cluster's receive area needs the room.
 constexpr int kStagesSolo = 10;
 constexpr int kStagesShared = 5;
-constexpr int kUnitsPerSm = 1;
+constexpr int kMaxSplit = 8;       // units per row block (the portable cluster size)
 constexpr int kRowsPerUnit = 128;  // MMA M
 constexpr int kNPad = 16;          // MMA N: X rows padded to 16
 constexpr int kKB = 64;            // k per block (128 bytes of fp16 = the swizzle span)
@@ -48,13 +52,16 @@ constexpr int kABytes = kRowsPerUnit * kKB * 2;  // 16 KB
 constexpr int kBBytes = kNPad * kKB * 2;         // 2 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 18 KB (multiple of 1024)
 constexpr uint32_t kTmemCols = 32;
-constexpr size_t smem_bytes_for(int nst) { return 1024 + size_t(nst) * kStageBytes + 256; }
+constexpr size_t kSmemSolo = 227 * 1024;         // per-CTA shared memory with one CTA per SM
+constexpr size_t kSmemShared = 113 * 1024;       // ... with two
+// dynamic shared memory: alignment slack, ring, cluster receive area, barriers and flags
+constexpr size_t smem_bytes_for(int nst, size_t recv) { return 1024 + size_t(nst) * kStageBytes + recv + 256; }
 
 constexpr int kMaxProblems = 8;
 
 struct WsProblem {
     void *Y;
-    float *partial;     // [units][128][16] fp32 (split-K only)
+    float *partial;     // [units][128][16] fp32 (split-K through the workspace only)
     unsigned *tickets;  // [row blocks]
     int y_fp32;
     int M, N, K;
@@ -65,30 +72,59 @@ struct WsProblem {
 
 // Kernel parameters: up to kMaxProblems independent problems share one launch, CTA b taking
 // unit b - unit0 of the problem whose range holds it.  The tensor maps stay in parameter
-// space (__grid_constant__), where TMA reads them.
+// space (__grid_constant__), where TMA reads them.  The scalars and problem descriptors come
+// first: a CTA's first reads of the (cold) parameter block then fall on its first lines.
 struct WsGroup {
-    CUtensorMap tmW[kMaxProblems];
-    CUtensorMap tmX[kMaxProblems];
-    WsProblem prob[kMaxProblems];
     int nprob;
-    int nst;            // ring stages (kStagesSolo or kStagesShared)
+    int nst;            // ring stages
+    int cluster;        // 1: one problem whose S units per row block form a cluster (DSMEM sum)
+    int mcols;          // cluster mode: partial columns sent per row (8 or 16)
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
                                   // this long on a barrier that nothing signals
+    WsProblem prob[kMaxProblems];
+    CUtensorMap tmW[kMaxProblems];
+    CUtensorMap tmX[kMaxProblems];
 };
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr_cta, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr_cta), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Every thread of every CTA of the cluster; the warp must be converged (aligned form).
+__device__ __forceinline__ void cluster_sync_all() {
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void store_y(const WsProblem &a, int row, const float (&y)[kNPad]) {
+#pragma unroll
+    for (int m = 0; m < kNPad; ++m) {
+        if (m < a.M) {
+            const size_t o = size_t(m) * a.N + row;
+            if (a.y_fp32)
+                static_cast<float *>(a.Y)[o] = y[m];
+            else
+                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_constant__ WsGroup g) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-aligned tiles
     const int nst = g.nst;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(nst) * kStageBytes);
-    uint64_t *empty = full + nst;
-    uint64_t *done = empty + nst;
-    uint64_t *never = done + 1;  // signalled by nobody: the fault-injection hook waits on it
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
-    int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -104,8 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     const int kb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nkb / a.S);
     const int nk = kb1 - kb0;
     const int n0 = rb * kRowsPerUnit;
+    // cluster mode: unit 0 of the row block receives the other units' partial rows here,
+    // [S - 1][128 rows][mcols] fp32
+    const size_t recv_bytes = g.cluster ? size_t(a.S - 1) * kRowsPerUnit * g.mcols * 4 : 0;
+    float *recv = reinterpret_cast<float *>(smem + size_t(nst) * kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(nst) * kStageBytes + recv_bytes);
+    uint64_t *empty = full + nst;
+    uint64_t *done = empty + nst;
+    uint64_t *never = done + 1;  // signalled by nobody: the fault-injection hook waits on it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
+    int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
-    if (threadIdx.x == 0) {
+    if (warp == 4 && lane == 0) {
+        // The producer sets up the barriers and starts the first ring's worth of copies before
+        // the CTA-wide set-up, so the DRAM latency of the first tiles overlaps it.
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -113,6 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
         mbar_init(done, 1);
         mbar_init(never, 1);
         fence_mbar_init();
+        pdl_wait();  // no global-memory access before this point
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_x = l2_policy_evict_last();
+        for (int j = 0; j < nk && j < nst; ++j) {
+            unsigned char *sa = smem + size_t(j) * kStageBytes;
+            mbar_arrive_expect_tx(&full[j], kStageBytes);
+            tma_load_2d(sa, tmW, (kb0 + j) * kKB, n0, &full[j], pol_w);
+            tma_load_2d(sa + kABytes, tmX, (kb0 + j) * kKB, 0, &full[j], pol_x);
+        }
     }
     if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -123,13 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     pdl_wait();  // no global-memory access before this point
 
     if (warp == 4) {
-        // ---- TMA producer ----
+        // ---- TMA producer: the copies after the first ring's worth ----
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             int st = 0;
-            uint32_t ph = 0;
-            for (int j = 0; j < nk; ++j) {
+            uint32_t ph = 1;  // the first use of every slot was issued above
+            for (int j = nst; j < nk; ++j) {
                 if (!mbar_wait(&empty[st], ph ^ 1u, g.timeout_ns)) {
                     atomicOr(g.status, kWsStatusTimeout);
                     break;
@@ -182,20 +239,24 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
         tmem_ld_16(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
         const int lrow = warp * 32 + lane;
         const int row = n0 + lrow;
-        const int M = a.M;
         if (a.S == 1) {
             if (ok && row < a.N) {
+                float y[kNPad];
 #pragma unroll
-                for (int m = 0; m < kNPad; ++m) {
-                    if (m < M) {
-                        const float y = __uint_as_float(v[m]);
-                        const size_t o = size_t(m) * a.N + row;
-                        if (a.y_fp32)
-                            static_cast<float *>(a.Y)[o] = y;
-                        else
-                            static_cast<__half *>(a.Y)[o] = __float2half_rn(y);
-                    }
-                }
+                for (int m = 0; m < kNPad; ++m) y[m] = __uint_as_float(v[m]);
+                store_y(a, row, y);
+            }
+        } else if (g.cluster) {
+            // units 1..S-1: this row's partial goes into unit 0's receive area (the cluster
+            // barrier below orders it before unit 0 reads it)
+            if (sk != 0) {
+                const uint32_t dst = map_to_rank(
+                    smem_addr(recv + (size_t(sk - 1) * kRowsPerUnit + lrow) * g.mcols), 0u);
+#pragma unroll
+                for (int q = 0; q < kNPad / 4; ++q)
+                    if (4 * q < g.mcols)
+                        st_cluster_v4(dst + 16u * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             }
         } else {
             float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(unit) * kRowsPerUnit + lrow) * kNPad);
@@ -210,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
             if (*s_last) {
                 __threadfence();
                 if (ok && row < a.N) {
-                    // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads are issued
+                    // y[m] = 0 + partial[0][row][m] + partial[1][row][m] + ...; loads are issued
                     // four units at a time so their latencies overlap, the sum order is fixed
                     const float4 *base =
                         reinterpret_cast<const float4 *>(a.partial + (size_t(rb) * a.S * kRowsPerUnit + lrow) * kNPad);
@@ -245,21 +306,36 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
                             y[4 * q + 3] += t.w;
                         }
                     }
-#pragma unroll
-                    for (int m = 0; m < kNPad; ++m) {
-                        if (m < M) {
-                            const size_t o = size_t(m) * a.N + row;
-                            if (a.y_fp32)
-                                static_cast<float *>(a.Y)[o] = y[m];
-                            else
-                                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
-                        }
-                    }
+                    store_y(a, row, y);
                 }
                 if (threadIdx.x == 0) a.tickets[rb] = 0u;  // zero again for the next call
             }
         }
+        if (g.cluster && a.S > 1) {
+            cluster_sync_all();
+            if (sk == 0 && ok && row < a.N) {
+                // y[m] = 0 + p_0[m] + p_1[m] + ... + p_{S-1}[m]: the order of the workspace path
+                float y[kNPad];
+#pragma unroll
+                for (int m = 0; m < kNPad; ++m) y[m] = 0.f + __uint_as_float(v[m]);
+                for (int s = 1; s < a.S; ++s) {
+                    const float4 *src = reinterpret_cast<const float4 *>(recv + (size_t(s - 1) * kRowsPerUnit + lrow) * g.mcols);
+#pragma unroll
+                    for (int q = 0; q < kNPad / 4; ++q) {
+                        if (4 * q < g.mcols) {
+                            const float4 t = src[q];
+                            y[4 * q] += t.x;
+                            y[4 * q + 1] += t.y;
+                            y[4 * q + 2] += t.z;
+                            y[4 * q + 3] += t.w;
+                        }
+                    }
+                }
+                store_y(a, row, y);
+            }
+        }
     }
+    if (g.cluster && a.S > 1 && warp >= 4) cluster_sync_all();  // every thread of the cluster arrives
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -268,41 +344,121 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
 
 struct Plan {
     int nrb, nkb, S;
+    int cps;  // CTAs per SM the split was sized for (1 or 2)
 };
 
+// Receive area of a cluster launch: (S - 1) partial tiles of 128 rows x mcols fp32.
+size_t recv_bytes_for(int S, int M) { return size_t(S - 1) * kRowsPerUnit * (M <= 8 ? 8 : 16) * 4; }
+
+// Ring stages that fit with `cps` CTAs per SM next to a receive area of `recv` bytes.
+int stages_for(int cps, size_t recv) {
+    const size_t budget = cps == 1 ? kSmemSolo : kSmemShared;
+    const int cap = cps == 1 ? kStagesSolo : kStagesShared;
+    const long long fit = (static_cast<long long>(budget) - static_cast<long long>(smem_bytes_for(0, recv))) / kStageBytes;
+    return static_cast<int>(fit < cap ? fit : cap);
+}
+
+// Whether one wave of a cluster launch holds `units` CTAs in clusters of S (cached per device
+// and shape of the question).
+bool clusters_fit(int S, int cps, int M, int units);
+
+// The split of K: for S = 1 .. kMaxSplit units per row block with one CTA per SM, the
+// largest number of k-blocks any SM streams when every unit is resident in one wave; the
+// smallest wins, then the smaller S.  A shape with more row blocks than SMs runs unsplit with
+// two CTAs per SM.  (Splits sized for two CTAs per SM were measured about 1 us faster alone on
+// the 12288-row and 12288-wide projections, but their extra short units slowed the grouped
+// launch of the four projections, so they are not used.)  Whether the clusters fit is asked
+// for the largest receive area (M = 16), so the split depends on N and K only and a problem is
+// split the same way in a single and in a grouped launch.
 Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
     p.nkb = (K + kKB - 1) / kKB;
-    // about kUnitsPerSm units per SM, each with at least 16 k-blocks (256 KB of weights): a
-    // unit's setup, first copies and split-K epilogue take a few microseconds, so shorter units
-    // spend longer on them than on their stream (measured on the grouped Qwen3-8B projections:
-    // 4 -> 16 k-blocks, 48.8 -> 46.0 us, the four shapes alone unchanged)
-    int S = (kUnitsPerSm * sms) / p.nrb;
-    const int smax = p.nkb / 16 > 0 ? p.nkb / 16 : 1;
-    if (S > smax) S = smax;
-    if (S < 1) S = 1;
-    p.S = S;
+    p.S = 1;
+    p.cps = 2;
+    long long best = -1;
+    for (int cps = 1; cps <= 1; ++cps) {
+        for (int S = 1; S <= kMaxSplit && S <= p.nkb; ++S) {
+            const long long units = static_cast<long long>(p.nrb) * S;
+            if (units > static_cast<long long>(cps) * sms) break;
+            if (stages_for(cps, recv_bytes_for(S, 16)) < 3) break;
+            if (S > 1 && !clusters_fit(S, cps, 16, static_cast<int>(units))) continue;
+            const long long per_sm = (units + sms - 1) / sms;            // CTAs on the busiest SM
+            const long long load = per_sm * ((p.nkb + S - 1) / S);     // its k-blocks
+            if (best < 0 || load < best) {
+                best = load;
+                p.S = S;
+                p.cps = cps;
+            }
+        }
+    }
     return p;
 }
 
-// Workspace: a fixed ticket area first (so tickets stay at the same place and stay zero
-// whatever shapes share the workspace), then the partial tiles.
-size_t workspace_bytes_for(const Plan &p) {
-    const size_t fixed = kWsHeaderBytes + kWsTicketBytes;
-    if (p.S == 1) return fixed;
-    return fixed + size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
+// ---- cluster occupancy, queried once per device and (S, cps, receive size) ----------------
+dspark_status configure_kernel(int dev) {
+    static int configured_dev = -1;
+    if (configured_dev == dev) return DSPARK_OK;
+    cudaError_t e = cudaFuncSetAttribute(ws_matvec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemSolo));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_matvec_tc_kernel, kThreads,
+                                                      smem_bytes_for(kStagesSolo, 0));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
+    if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
+    configured_dev = dev;
+    return DSPARK_OK;
+}
+
+bool clusters_fit(int S, int cps, int M, int units) {
+    struct Entry {
+        int dev, S, cps, mc, clusters;
+    };
+    static Entry cache[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const int mc = M <= 8 ? 8 : 16;
+    int clusters = -1;
+    for (int i = 0; i < n; ++i)
+        if (cache[i].dev == dev && cache[i].S == S && cache[i].cps == cps && cache[i].mc == mc) clusters = cache[i].clusters;
+    if (clusters < 0) {
+        if (configure_kernel(dev) != DSPARK_OK) return false;
+        const size_t recv = recv_bytes_for(S, M);
+        const int nst = stages_for(cps, recv);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(S));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem_bytes_for(nst, recv);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, ws_matvec_tc_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            c = 0;
+        }
+        clusters = c;
+        if (n < 64) cache[n++] = Entry{dev, S, cps, mc, clusters};
+    }
+    return static_cast<long long>(clusters) * S >= units;
 }
 
 }  // namespace
 }  // namespace dspark
 
 extern "C" size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K) {
+    // a single problem reduces its split-K partials in distributed shared memory: the
+    // workspace holds only the status word and the (unused) ticket area
     (void)M;
-    int sms = 0;
-    if (N <= 0 || K <= 0) return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
-    if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
-    return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
+    (void)N;
+    (void)K;
+    return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
 }
 
 namespace {
@@ -324,11 +480,20 @@ dspark_status check_problem(const dspark_ws_problem &q, bool *skip) {
     return DSPARK_OK;
 }
 
+int live_problems(const dspark_ws_problem *probs, int n) {
+    int live = 0;
+    for (int i = 0; i < n; ++i)
+        if (probs[i].N > 0 && probs[i].K > 0 && probs[i].M > 0) ++live;
+    return live;
+}
+
 // Workspace of a group: header, one ticket area (the problems' row blocks one after the
-// other), then each split problem's partial tiles.  0 when the sizes are invalid.
+// other), then each split problem's partial tiles -- unless the launch holds one problem,
+// which reduces in distributed shared memory.  0 when the sizes are invalid.
 size_t group_workspace_bytes(const dspark_ws_problem *probs, int n, int sms) {
     using namespace dspark;
     size_t bytes = dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
+    if (live_problems(probs, n) <= 1) return bytes;
     for (int i = 0; i < n; ++i) {
         if (probs[i].N <= 0 || probs[i].K <= 0 || probs[i].M <= 0) continue;
         const Plan p = plan_for(probs[i].N, probs[i].K, sms);
@@ -359,9 +524,16 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
     const size_t need = group_workspace_bytes(probs, n, sms);
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec: workspace of %zu bytes < required %zu", workspace_bytes, need);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    dspark_status st = configure_kernel(dev);
+    if (st != DSPARK_OK) return st;
 
     WsGroup g;
     g.nprob = 0;
+    g.cluster = live == 1 ? 1 : 0;
+    g.mcols = 16;
     g.status = static_cast<unsigned *>(workspace);
     g.timeout_ns = kDefaultTimeoutNs;
     g.stall_ns = stall_ns;
@@ -386,14 +558,16 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
             order[b] = order[b - 1];
             order[b - 1] = t;
         }
+    Plan solo = {};
     for (int oi = 0; oi < norder; ++oi) {
         const dspark_ws_problem &q = probs[order[oi]];
         const Plan p = plan_for(q.N, q.K, sms);
+        solo = p;
         if ((ticket_off + p.nrb) * sizeof(unsigned) > kWsTicketBytes)
             return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: more than %zu rows in one call", kWsTicketBytes / 4 * kRowsPerUnit);
         const int j = g.nprob++;
-        dspark_status st = make_tmap_2d(&g.tmW[j], q.W, false, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K),
-                                        kRowsPerUnit, kKB);
+        st = make_tmap_2d(&g.tmW[j], q.W, false, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K), kRowsPerUnit,
+                          kKB);
         if (st != DSPARK_OK) return st;
         st = make_tmap_2d(&g.tmX[j], q.X, false, static_cast<uint64_t>(q.M), static_cast<uint64_t>(q.K), kNPad, kKB);
         if (st != DSPARK_OK) return st;
@@ -408,7 +582,7 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
         a.unit0 = static_cast<int>(units);
         a.tickets = nullptr;
         a.partial = nullptr;
-        if (p.S > 1) {
+        if (p.S > 1 && !g.cluster) {
             a.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes) + ticket_off;
             a.partial = reinterpret_cast<float *>(ws + partial_off);
             ticket_off += p.nrb;
@@ -417,24 +591,36 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
         units += static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
     }
 
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ws_matvec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_bytes_for(kStagesSolo)));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_matvec_tc_kernel, kThreads,
-                                                          smem_bytes_for(kStagesSolo));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
-        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
-        configured_dev = dev;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    size_t recv = 0;
+    if (g.cluster) {
+        // one problem: the ring sized for the CTAs per SM its split assumed, and for S > 1 the
+        // S units of a row block as one cluster with unit 0's receive area
+        const int M = g.prob[0].M;
+        g.mcols = M <= 8 ? 8 : 16;
+        recv = solo.S > 1 ? recv_bytes_for(solo.S, M) : 0;
+        g.nst = stages_for(solo.cps, recv);
+        if (solo.S > 1) {
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = static_cast<unsigned>(solo.S);
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        }
+    } else {
+        // more units than SMs: two CTAs per SM with the shallower ring
+        g.nst = units > static_cast<unsigned>(sms) ? kStagesShared : kStagesSolo;
     }
-    // more units than SMs: two CTAs per SM with the shallower ring
-    g.nst = units > static_cast<unsigned>(sms) ? kStagesShared : kStagesSolo;
-    cudaError_t e = launch_pdl(ws_matvec_tc_kernel, dim3(units), dim3(kThreads), smem_bytes_for(g.nst),
-                               reinterpret_cast<cudaStream_t>(stream), g);
+    cfg.gridDim = dim3(units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes_for(g.nst, recv);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaLaunchKernelEx(&cfg, ws_matvec_tc_kernel, g);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;
 }

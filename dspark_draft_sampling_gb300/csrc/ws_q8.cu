@@ -18,10 +18,13 @@
 // order.  Every output is summed in one fixed order (blocks, then split-K units in order), so
 // results are deterministic and row m's does not depend on M.
 //
-// GB300 design (persistent: one CTA per SM, 15 warps)
-//  * Work unit = (128 weight rows, a range of 256-k superblocks); K is split so that there is
-//    about one unit per SM.  Each CTA takes every gridDim.x-th unit and streams the stages of
-//    its units back to back, so one unit's epilogue overlaps the next unit's loads.
+// GB300 design (one CTA per SM, 15 warps)
+//  * Work unit = (128 weight rows, a range of 256-k superblocks).  With at most as many row
+//    blocks as SMs, K is split into S <= 8 units per row block, one unit per CTA, S chosen for
+//    the fewest superblocks per CTA in one wave, and the S CTAs of a row block form a
+//    thread-block cluster.  With more row blocks than SMs the CTAs are persistent: each takes
+//    every gridDim.x-th unit and streams the stages of its units back to back, so one unit's
+//    epilogue overlaps the next unit's loads.
 //  * Warp 12 (one thread) streams, per 128-k stage, the int8 tile [128 rows x 128 k] (16 KB,
 //    128-byte swizzle, one 3-D copy of a single 128-byte column atom) and the X tile [16 rows x 128 k] (two 2 KB fp16 atoms in one 3-D copy;
 //    rows >= M read as zero) with TMA tensor copies through a 10-stage ring (200 KB).
@@ -45,8 +48,10 @@
 //  * Warps 0-3 (one TMEM lane = one weight row per thread) read a stage's 4 x 16 sums with
 //    tcgen05.ld and fold them in with the row's scales (loaded 8 at a time from global memory,
 //    four loads ahead).
-//    With one unit per row block they write Y directly; otherwise they store fp32 partials and
-//    the last unit of the row block (a ticket counter) sums them in unit order.
+//    With one unit per row block they write Y directly.  Otherwise, after a cluster barrier
+//    (every unit of the row block has finished streaming, so unit 0's ring is idle), units
+//    1..S-1 store their partial rows into unit 0's ring through distributed shared memory and,
+//    after a second barrier, unit 0 sums 0 + p_0 + p_1 + ... + p_{S-1} and writes Y.
 #include <cuda_fp16.h>
 
 #include "tc.cuh"
@@ -65,6 +70,7 @@ constexpr int kKS = 128;               // k per stage: 128 B of int8 per row (th
 constexpr int kBlocksPerStage = kKS / 32;   // 4 Q8_0 blocks
 constexpr int kSuper = 2;              // stages per 256-k superblock (8 scales of a row)
 constexpr int kStages = 10;            // shared-memory ring (even, so each stage parity keeps its slots)
+constexpr int kMaxSplit = 8;           // units per row block (the portable cluster size)
 constexpr int kQBytes = kRows * kKS;                // 16 KB int8 tile
 constexpr int kXAtomBytes = kNPad * 64 * 2;         // 2 KB: 16 rows x 64 fp16
 constexpr int kSlotBytes = kQBytes + 2 * kXAtomBytes;  // 20 KB (multiple of 1024)
@@ -86,13 +92,13 @@ static_assert(kASlots % kMmaIssuers == 0 && kASlots % 2 == 0,
 struct Q8Args {
     const uint16_t *d;  // [N, K/32] fp16 scales
     void *Y;
-    float *partial;     // [units][128][16] fp32 (split-K only)
-    unsigned *tickets;  // [row blocks]
     int y_fp32;
     int M, N, K;
     int nsb;    // 256-k superblocks
     int S;      // units per row block
     int units;  // row blocks x S; CTA c takes units c, c + gridDim.x, ...
+    int cluster;  // 1: one unit per CTA and the S units of a row block form a cluster
+    int mcols;    // cluster mode: partial columns sent per row (8 or 16)
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
@@ -127,6 +133,38 @@ __device__ __forceinline__ uint32_t q8_pair_to_f16x2(uint32_t u, uint32_t sel) {
 
 __device__ __forceinline__ uint4 ldg_u4(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr_cta, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr_cta), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Every thread of every CTA of the cluster; the warp must be converged (aligned form).
+__device__ __forceinline__ void cluster_sync_all() {
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void store_y(const Q8Args &a, int row, const float (&y)[kNPad]) {
+#pragma unroll
+    for (int m = 0; m < kNPad; ++m) {
+        if (m < a.M) {
+            const size_t o = size_t(m) * a.N + row;
+            if (a.y_fp32)
+                static_cast<float *>(a.Y)[o] = y[m];
+            else
+                static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+        }
+    }
+}
+
 // Stage J is the CTA's J-th 128-k stage over all its units, in order.  Ring positions:
 // shared-memory slot J % kStages, TMEM A slot and accumulator group J % kASlots, and the
 // phase of each ring's barrier is (J / ring size) & 1.
@@ -145,7 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *mma_done = empty_t + kTGroups;  // [kMmaIssuers]
     uint64_t *never = mma_done + kMmaIssuers;  // signalled by nobody: the fault-injection hook waits on it
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
-    int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -354,82 +391,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            const int M = a.M;
             if (a.S == 1) {
-                if (ok && rowok) {
+                if (ok && rowok) store_y(a, row, acc);
+            } else if (a.cluster) {
+                // Every CTA has one unit.  First barrier: every CTA of the cluster has finished
+                // its stream, so the ring of unit 0 is idle; units 1..S-1 then store this row's
+                // partial into it, and after the second barrier unit 0 sums
+                // y = 0 + p_0 + p_1 + ... + p_{S-1}, the order of the workspace path.
+                const int sk = u % a.S;
+                cluster_sync_all();
+                float *recv = reinterpret_cast<float *>(ring);
+                if (sk != 0) {
+                    const uint32_t dst = map_to_rank(smem_addr(recv + (size_t(sk - 1) * kRows + lrow) * a.mcols), 0u);
 #pragma unroll
-                    for (int m = 0; m < kNPad; ++m) {
-                        if (m < M) {
-                            const size_t o = size_t(m) * a.N + row;
-                            if (a.y_fp32)
-                                static_cast<float *>(a.Y)[o] = acc[m];
-                            else
-                                static_cast<__half *>(a.Y)[o] = __float2half_rn(acc[m]);
-                        }
-                    }
+                    for (int q = 0; q < kNPad / 4; ++q)
+                        if (4 * q < a.mcols)
+                            st_cluster_v4(dst + 16u * q, acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                 }
-            } else {
-                float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(u) * kRows + lrow) * kNPad);
+                cluster_sync_all();
+                if (sk == 0 && ok && rowok) {
+                    float y[kNPad];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    p[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-                __threadfence();
-                named_bar_sync(1, 128);
-                if (threadIdx.x == 0) *s_last = (atomicAdd(&a.tickets[ug.rb], 1u) == static_cast<unsigned>(a.S - 1));
-                named_bar_sync(1, 128);
-                if (*s_last) {
-                    __threadfence();
-                    if (ok && rowok) {
-                        // y[m] = sum over units s = 0, 1, ... of partial[s][row][m]; loads issued
-                        // four units at a time so their latencies overlap, the sum order is fixed
-                        const float4 *base =
-                            reinterpret_cast<const float4 *>(a.partial + (size_t(ug.rb) * a.S * kRows + lrow) * kNPad);
-                        constexpr size_t kUnitF4 = size_t(kRows) * kNPad / 4;
-                        float y[kNPad];
+                    for (int m = 0; m < kNPad; ++m) y[m] = 0.f + acc[m];
+                    for (int s2 = 1; s2 < a.S; ++s2) {
+                        const float4 *src = reinterpret_cast<const float4 *>(recv + (size_t(s2 - 1) * kRows + lrow) * a.mcols);
 #pragma unroll
-                        for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
-                        int s = 0;
-                        for (; s + 4 <= a.S; s += 4) {
-                            float4 tq[4][4];
-#pragma unroll
-                            for (int q2 = 0; q2 < 4; ++q2)
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) tq[q2][q] = __ldcg(base + size_t(s + q2) * kUnitF4 + q);
-#pragma unroll
-                            for (int q2 = 0; q2 < 4; ++q2)
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    y[4 * q] += tq[q2][q].x;
-                                    y[4 * q + 1] += tq[q2][q].y;
-                                    y[4 * q + 2] += tq[q2][q].z;
-                                    y[4 * q + 3] += tq[q2][q].w;
-                                }
-                        }
-                        for (; s < a.S; ++s) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float4 tq = __ldcg(base + size_t(s) * kUnitF4 + q);
-                                y[4 * q] += tq.x;
-                                y[4 * q + 1] += tq.y;
-                                y[4 * q + 2] += tq.z;
-                                y[4 * q + 3] += tq.w;
-                            }
-                        }
-#pragma unroll
-                        for (int m = 0; m < kNPad; ++m) {
-                            if (m < M) {
-                                const size_t o = size_t(m) * a.N + row;
-                                if (a.y_fp32)
-                                    static_cast<float *>(a.Y)[o] = y[m];
-                                else
-                                    static_cast<__half *>(a.Y)[o] = __float2half_rn(y[m]);
+                        for (int q = 0; q < kNPad / 4; ++q) {
+                            if (4 * q < a.mcols) {
+                                const float4 t = src[q];
+                                y[4 * q] += t.x;
+                                y[4 * q + 1] += t.y;
+                                y[4 * q + 2] += t.z;
+                                y[4 * q + 3] += t.w;
                             }
                         }
                     }
-                    if (threadIdx.x == 0) a.tickets[ug.rb] = 0u;  // zero again for the next call
+                    store_y(a, row, y);
                 }
             }
         }
+    }
+    // cluster mode: the two barriers of the epilogue, for every other thread of the CTA
+    if (a.cluster && a.S > 1 && warp >= 4) {
+        cluster_sync_all();
+        cluster_sync_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -439,24 +444,80 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct Plan {
     int nrb, nsb, S;
+    bool cluster;  // one unit per CTA, the S units of a row block as one cluster
 };
 
+dspark_status configure_kernel(int dev) {
+    static int configured_dev = -1;
+    if (configured_dev == dev) return DSPARK_OK;
+    cudaError_t e = cudaFuncSetAttribute(ws_q8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec_q8)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_q8_tc_kernel, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec_q8)");
+    if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
+    configured_dev = dev;
+    return DSPARK_OK;
+}
+
+// How many CTAs one wave of clusters of S holds (cached per device and S).
+int cluster_capacity(int S) {
+    static int cache[64][kMaxSplit + 1];
+    static bool init = false;
+    if (!init) {
+        for (auto &row : cache)
+            for (int &c : row) c = -1;
+        init = true;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev][S] >= 0) return cache[dev][S];
+    if (configure_kernel(dev) != DSPARK_OK) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, ws_q8_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        c = 0;
+    }
+    cache[dev][S] = c * S;
+    return cache[dev][S];
+}
+
+// The split of K: with at most as many row blocks as SMs, the S (1 .. kMaxSplit) that gives
+// the fewest superblocks to any CTA with every unit in one wave of clusters (then the
+// smaller S); each CTA takes one unit and the S units of a row block reduce in distributed
+// shared memory.  More row blocks than SMs: unsplit, persistent CTAs walking the units.
 Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRows - 1) / kRows;
     p.nsb = K / (kKS * kSuper);
-    // about one unit per SM, each with at least one superblock
-    int S = sms / p.nrb;
-    if (S > p.nsb) S = p.nsb;
-    if (S < 1) S = 1;
-    p.S = S;
+    p.S = 1;
+    p.cluster = false;
+    if (p.nrb > sms) return p;
+    int best = -1;
+    for (int S = 1; S <= kMaxSplit && S <= p.nsb; ++S) {
+        const long long units = static_cast<long long>(p.nrb) * S;
+        if (units > sms) break;
+        if (S > 1 && units > cluster_capacity(S)) continue;
+        const int load = (p.nsb + S - 1) / S;
+        if (best < 0 || load < best) {
+            best = load;
+            p.S = S;
+        }
+    }
+    p.cluster = p.S > 1;
     return p;
-}
-
-size_t workspace_bytes_for(const Plan &p) {
-    const size_t fixed = kWsHeaderBytes + kWsTicketBytes;
-    if (p.S == 1) return fixed;
-    return fixed + size_t(p.nrb) * p.S * kRows * kNPad * sizeof(float);
 }
 
 __global__ void q8_0_repack_kernel(const uint8_t *__restrict__ aos, int8_t *__restrict__ q, uint16_t *__restrict__ d,
@@ -496,11 +557,12 @@ extern "C" dspark_status dspark_q8_0_repack(const void *w_q8_0, int8_t *q, uint1
 }
 
 extern "C" size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K) {
+    // split rows reduce in distributed shared memory: the workspace holds only the status
+    // word and the (unused) ticket area
     (void)M;
-    int sms = 0;
-    if (N <= 0 || K < 256) return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
-    if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
-    return dspark::workspace_bytes_for(dspark::plan_for(N, K, sms));
+    (void)N;
+    (void)K;
+    return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
 }
 
 namespace {
@@ -522,10 +584,15 @@ dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "cudaGetDevice");
+    dspark_status st0 = configure_kernel(dev);
+    if (st0 != DSPARK_OK) return st0;
     const Plan p = plan_for(N, K, sms);
     if (size_t(p.nrb) * sizeof(unsigned) > kWsTicketBytes)
         return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: N=%d exceeds %zu rows", N, kWsTicketBytes / 4 * kRows);
-    const size_t need = workspace_bytes_for(p);
+    const size_t need = kWsHeaderBytes + kWsTicketBytes;
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
 
@@ -546,32 +613,30 @@ dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X
     args.S = p.S;
     args.units = p.nrb * p.S;
     args.timeout_ns = kDefaultTimeoutNs;
-    args.partial = nullptr;
-    args.tickets = nullptr;
+    args.cluster = p.cluster ? 1 : 0;
+    args.mcols = M <= 8 ? 8 : 16;
     args.status = static_cast<unsigned *>(workspace);
     args.stall_ns = stall_ns;
-    if (p.S > 1) {
-        unsigned char *ws = static_cast<unsigned char *>(workspace);
-        args.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes);
-        args.partial = reinterpret_cast<float *>(ws + kWsHeaderBytes + kWsTicketBytes);
-    }
 
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ws_q8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec_q8)");
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_q8_tc_kernel, kThreads, kSmemBytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec_q8)");
-        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
-        configured_dev = dev;
-    }
     const int grid = args.units < sms ? args.units : sms;  // persistent: one CTA per SM
-    cudaError_t e = launch_pdl(ws_q8_tc_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
-                               reinterpret_cast<cudaStream_t>(stream), tmQ, tmX, args);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.cluster) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(p.S);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel, tmQ, tmX, args);
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
 }

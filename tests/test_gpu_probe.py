@@ -106,3 +106,17 @@ def test_odd_aligned_weight_row():
     assert torch.equal(z1.view(torch.int32), z2.view(torch.int32))
     assert torch.equal(g1, g2)
     parity.check_probe(inp, z2.cpu().numpy(), g2.cpu().numpy())
+
+
+def test_gate_into_pinned_host_memory():
+    """gate_out in pinned host memory: the kernel's own 4-byte store is the readback."""
+    inp = synth.probe_inputs(3, 7424, seed=9)
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    hid = torch.from_numpy(inp["hidden"]).cuda()
+    _, g_dev = api.conf_probe(wq, hid, inp["bias"], 0.5)
+    g_host = torch.full((3,), -1, dtype=torch.int32).pin_memory()
+    api.conf_probe(wq, hid, inp["bias"], 0.5, gate_out=g_host)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(g_host.numpy(), g_dev.cpu().numpy())
+    _, go = parity.oracle.conf_probe(inp["wq"], inp["hidden"], inp["bias"], 0.5)
+    np.testing.assert_array_equal(g_host.numpy(), go)
