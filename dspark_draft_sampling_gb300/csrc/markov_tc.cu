@@ -18,11 +18,13 @@
 //    bf16 tile (64 KB at rank 256: rank/64 blocks of [128 x 64] in the 128-byte swizzle) and
 //    one of the tile's base-logit rows for every request ([num_reqs x 128] fp32) into the same
 //    ring slot.  Neither depends on prev, so the producer runs ahead across positions.
-//  * Warp 5: allocates 32 TMEM columns (two 128 x 16 fp32 accumulators); one thread issues,
-//    per tile, rank/16 tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows,
-//    N = 16 request slots, K = 16) against H, which the epilogue warps write into shared
-//    memory in the same swizzled layout (rows >= num_reqs stay zero), then one
-//    tcgen05.commit for the slot and one for the accumulator.
+//  * Warp 5 allocates 32 TMEM columns (two 128 x 16 fp32 accumulators).  Warps 5 and 6 each
+//    have one thread issuing the MMAs of every other tile into its own accumulator: per tile
+//    rank/16 tcgen05.mma kind::f16 (bf16 in, fp32 accumulate; M = 128 rows, N = 16 request
+//    slots, K = 16) against H, which the epilogue warps write into shared memory in the same
+//    swizzled layout (rows >= num_reqs stay zero), then one tcgen05.commit for the slot and
+//    one for the accumulator.  Issuing a tile's MMAs takes a good part of a slot's cycle, so
+//    two issuers keep tiles that land together from queueing behind one thread.
 //  * Warps 0-3 (thread = TMEM lane = vocab row of the tile): read the tile's base logits
 //    from the slot as soon as it lands (the slot is free again once both they and the MMAs
 //    are done with it), tcgen05.ld the accumulator, keep the best (value, row) per request;
@@ -39,7 +41,8 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
+constexpr int kMmaIssuers = 2;  // issuer p takes the tiles with counter tc % 2 == p (accumulator p)
+constexpr int kThreads = 32 * (5 + kMmaIssuers);  // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM, 6 MMA
 constexpr int kEpiThreads = 128;
 constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kTileRows = 128;
@@ -51,7 +54,7 @@ constexpr int kNPad = 16;                        // MMA N: request slots
 constexpr int kHBlockBytes = kNPad * kKB * 2;    // 2 KB per k-block of H
 constexpr int kHMaxBytes = 4 * kHBlockBytes;     // rank <= 256
 constexpr uint32_t kTmemCols = 32;
-constexpr size_t kSmemBytes = 1024 + size_t(kRingBudget) + 2 * kHMaxBytes + 512;
+constexpr size_t kSmemBytes = 1024 + size_t(kRingBudget) + 2 * kHMaxBytes + 768;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // Bytes reserved in a slot for the base rows of NB requests (a multiple of 1024, so the next
@@ -89,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *acc_empty = acc_full + 2;      // [2]
     uint64_t *h_full = acc_empty + 2;        // [2]
     unsigned long long *s_best = reinterpret_cast<unsigned long long *>(h_full + 2);  // [kMaxReqs]
-    int *s_cur = reinterpret_cast<int *>(s_best + kMaxReqs);                          // [kMaxReqs]
+    unsigned long long *s_wbest = s_best + kMaxReqs;  // [kEpiWarps][kMaxReqs] each warp's best keys
+    int *s_cur = reinterpret_cast<int *>(s_wbest + kEpiWarps * kMaxReqs);            // [kMaxReqs]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_cur + kMaxReqs);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -102,8 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int slot_bytes = w2_bytes + base_area_bytes<NB>();
     const int nslots = min(kMaxSlots, kRingBudget / slot_bytes);
     const int T = (a.V + kTileRows - 1) / kTileRows;
-    const int t0 = static_cast<int>(static_cast<long long>(cta) * T / nctas);
-    const int t1 = static_cast<int>(static_cast<long long>(cta + 1) * T / nctas);
+    // 32-bit unsigned: cta <= 152 and T < 2^24, so cta * T < 2^32
+    const int t0 = static_cast<int>(static_cast<unsigned>(cta) * static_cast<unsigned>(T) / static_cast<unsigned>(nctas));
+    const int t1 =
+        static_cast<int>(static_cast<unsigned>(cta + 1) * static_cast<unsigned>(T) / static_cast<unsigned>(nctas));
     const int ntiles = t1 - t0;
     auto tile_at = [t0, ntiles](int i, int t) { return t0 + ((i & 1) ? ntiles - 1 - t : t); };
 
@@ -174,26 +180,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
         producer_done:;
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp >= 5) {
+        // ---------------- MMA issuers: issuer p takes the tiles tc with tc % 2 == p ----------------
         if (lane == 0) {
+            const int p = warp - 5;
             constexpr uint32_t idesc = idesc_f16(true, kTileRows, kNPad);
             // Descriptors are built once and advanced by adding byte offsets >> 4 to their
             // address field (all of shared memory is below 256 KB, so it never carries).
             const uint64_t dA0 = smem_desc_sw128(smem_addr(ring));
             const uint64_t dH0 = smem_desc_sw128(smem_addr(hbuf));
-            int st = 0, ab = 0;
-            uint32_t ph = 0, aph = 0;
+            const uint32_t d = tmem + static_cast<uint32_t>(p * kNPad);  // accumulator p
+            int tc = 0;
             bool broken = false;
             for (int i = 0; i < a.k && !broken; ++i) {
+                // every issuer waits for every position's H, so its parity waits stay exact
                 if (!mbar_wait(&h_full[i & 1], (i >> 1) & 1, a.timeout_ns)) {
                     broken = true;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t dH = dH0 + static_cast<uint64_t>((i & 1) * (kHMaxBytes >> 4));
-                for (int t = 0; t < ntiles && !broken; ++t) {
-                    if (!mbar_wait(&acc_empty[ab], aph ^ 1u, a.timeout_ns)) {
+                for (int t = 0; t < ntiles && !broken; ++t, ++tc) {
+                    if ((tc & 1) != p) continue;
+                    const int st = tc % nslots;
+                    const uint32_t ph = static_cast<uint32_t>((tc / nslots) & 1);
+                    const uint32_t aph = static_cast<uint32_t>((tc >> 1) & 1);  // use tc / 2 of accumulator p
+                    if (!mbar_wait(&acc_empty[p], aph ^ 1u, a.timeout_ns)) {
                         broken = true;
                         break;
                     }
@@ -202,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + ab * kNPad;
                     const uint64_t dT = dA0 + static_cast<uint64_t>(st * (slot_bytes >> 4));
                     for (int kb = 0; kb < nkb; ++kb) {
                         const uint64_t dA = dT + static_cast<uint64_t>(kb * (kBoxBytes >> 4));
@@ -213,15 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_f16(d, dA + 6, dB + 6, idesc, 1u);
                     }
                     tc_commit(&empty[st]);    // the MMAs no longer read the slot
-                    tc_commit(&acc_full[ab]);  // the accumulator holds the tile
-                    if (++st == nslots) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
-                    if (++ab == 2) {
-                        ab = 0;
-                        aph ^= 1u;
-                    }
+                    tc_commit(&acc_full[p]);  // the accumulator holds the tile
                 }
             }
             if (broken) atomicOr(a.status, kStatusTimeout);
@@ -324,7 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const unsigned long long key =
                         bidx[r] >= 0 ? argmax_key(bval[r], static_cast<uint32_t>(bidx[r])) : 0ull;
                     const unsigned long long k_w = warp_max_u64(key);
-                    if (lane == 0 && r < a.B && k_w != 0ull) atomicMax(&s_best[r], k_w);
+                    if (lane == 0) s_wbest[warp * kMaxReqs + r] = k_w;
+                }
+                named_bar_sync(1, kEpiThreads);
+                if (et < a.B) {  // the CTA's best key of request et: the max over the four warps
+                    unsigned long long k_c = s_wbest[et];
+#pragma unroll
+                    for (int w = 1; w < kEpiWarps; ++w) {
+                        const unsigned long long k_w = s_wbest[w * kMaxReqs + et];
+                        k_c = k_w > k_c ? k_w : k_c;
+                    }
+                    s_best[et] = k_c;
                 }
                 named_bar_sync(1, kEpiThreads);
                 // A wait of this CTA gave up during the position: its keys miss tiles, so it

@@ -136,8 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     const int unit = static_cast<int>(blockIdx.x) - a.unit0;
     const int rb = unit / a.S;
     const int sk = unit % a.S;
-    const int kb0 = static_cast<int>(static_cast<long long>(sk) * a.nkb / a.S);
-    const int kb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nkb / a.S);
+    // 32-bit: sk <= 8 and nkb < 2^25 (a 64-bit division would call a long out-of-line routine)
+    const int kb0 = static_cast<int>(static_cast<unsigned>(sk) * static_cast<unsigned>(a.nkb) / static_cast<unsigned>(a.S));
+    const int kb1 =
+        static_cast<int>(static_cast<unsigned>(sk + 1) * static_cast<unsigned>(a.nkb) / static_cast<unsigned>(a.S));
     const int nk = kb1 - kb0;
     const int n0 = rb * kRowsPerUnit;
     // cluster mode: unit 0 of the row block receives the other units' partial rows here,

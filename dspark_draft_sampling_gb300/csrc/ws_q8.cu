@@ -113,8 +113,10 @@ __device__ __forceinline__ Unit unit_geometry(const Q8Args &a, int u) {
     Unit g;
     g.rb = u / a.S;
     const int sk = u % a.S;
-    g.sb0 = static_cast<int>(static_cast<long long>(sk) * a.nsb / a.S);
-    const int sb1 = static_cast<int>(static_cast<long long>(sk + 1) * a.nsb / a.S);
+    // 32-bit: sk <= 8 and nsb < 2^23
+    g.sb0 = static_cast<int>(static_cast<unsigned>(sk) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
+    const int sb1 =
+        static_cast<int>(static_cast<unsigned>(sk + 1) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
     g.nsup = sb1 - g.sb0;
     g.nst = g.nsup * kSuper;   // 128-k stages
     g.ks0 = g.sb0 * kSuper;    // first 128-k stage index along K

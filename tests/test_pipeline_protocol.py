@@ -220,11 +220,13 @@ class Barrier2(Barrier):
             self.completed += 1
 
 
-def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
+def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True, issuers=2):
     """One random interleaving of the Markov kernel's roles for one CTA: the TMA producer
-    (one copy of tile + base rows per slot, running ahead across positions), the MMA issuer
-    (per position: wait for H; per tile: wait for its accumulator to be drained, then for the
-    slot; its completion commits to the slot and to the accumulator), and each epilogue warp
+    (one copy of tile + base rows per slot, running ahead across positions), the MMA issuers
+    (issuer p takes the tiles tc with tc % issuers == p and accumulator p; per position every
+    issuer waits for H; per own tile: wait for its accumulator to be drained, then for the
+    slot; its completion commits to the slot and to the accumulator; each issuer's commits
+    complete in its issue order, the issuers' in any interleaving), and each epilogue warp
     (per tile: wait for the slot to land, read the base rows and arrive on the slot's empty
     barrier, wait for the accumulator, read it and arrive on its empty barrier; after the last
     tile of a position: the next position's H).  The slot's empty barrier completes after the
@@ -247,9 +249,11 @@ def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
             error = f"{who}: passed with {bar.completed} completed phases, wanted {kk + 1}"
         return True
 
-    st = dict(prod=0, mma=0, mma_w=0)
+    st = dict(prod=0)
+    iss = [dict(q=0, w=0) for _ in range(issuers)]  # q: next tile counter this issuer looks at
     epi = [dict(q=0, step=0) for _ in range(epi_warps)]
-    pending_land, pending_mma = [], []
+    pending_land = []
+    pending_mma = [[] for _ in range(issuers)]
 
     def producer():
         q = st["prod"]
@@ -261,27 +265,32 @@ def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
         st["prod"] += 1
         return True
 
-    def issuer():
-        q = st["mma"]
+    def issuer(p):
+        me = iss[p]
+        q = me["q"]
         if q >= total:
             return False
         i, t = divmod(q, ntiles)
-        w = st["mma_w"]
-        if w == 0:  # the position's H (first tile of each position only)
-            if t == 0 and not wait(h_full[i & 1], i >> 1, f"issuer position {i} (H)"):
+        if me["w"] == 0:  # the position's H (every issuer, first tile of each position)
+            if t == 0 and not wait(h_full[i & 1], i >> 1, f"issuer {p} position {i} (H)"):
                 return False
-            st["mma_w"] = 1
+            me["w"] = 1
             return True
-        if w == 1:  # accumulator q & 1 drained (tile q - 2)
-            if q >= 2 and not wait(acc_empty[q & 1], (q >> 1) - 1, f"issuer tile {q} (accumulator)"):
+        if q % issuers != p:  # another issuer's tile
+            me["q"] += 1
+            me["w"] = 0
+            return True
+        if me["w"] == 1:  # accumulator p drained (its previous use)
+            u = q // issuers
+            if u >= 1 and not wait(acc_empty[p], u - 1, f"issuer {p} tile {q} (accumulator)"):
                 return False
-            st["mma_w"] = 2
+            me["w"] = 2
             return True
-        if not wait(full[q % nslots], q // nslots, f"issuer tile {q} (tile landed)"):
+        if not wait(full[q % nslots], q // nslots, f"issuer {p} tile {q} (tile landed)"):
             return False
-        pending_mma.append(q)
-        st["mma"] += 1
-        st["mma_w"] = 0
+        pending_mma[p].append(q)
+        me["q"] += 1
+        me["w"] = 0
         return True
 
     def epilogue(w):
@@ -296,9 +305,9 @@ def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
                 empty[q % nslots].arrive()
             e["step"] = 1
             return True
-        if not wait(acc_full[q & 1], q >> 1, f"epilogue warp {w} tile {q} (accumulator)"):
+        if not wait(acc_full[q % issuers], q // issuers, f"epilogue warp {w} tile {q} (accumulator)"):
             return False
-        acc_empty[q & 1].arrive()
+        acc_empty[q % issuers].arrive()
         i, t = divmod(q, ntiles)
         if t == ntiles - 1 and i + 1 < k:
             h_full[(i + 1) & 1].arrive()
@@ -311,18 +320,19 @@ def run_markov(nslots, k, ntiles, rng, epi_warps=4, epilogue_holds_slot=True):
         full[q % nslots].completed += 1
         return True
 
-    def mma_complete(x):
-        if x != 0:  # one issuer: its commits complete in issue order
+    def mma_complete(p):
+        if not pending_mma[p]:
             return False
-        q = pending_mma.pop(0)
+        q = pending_mma[p].pop(0)  # one issuer's commits complete in its issue order
         empty[q % nslots].arrive()
-        acc_full[q & 1].completed += 1
+        acc_full[p].completed += 1
         return True
 
     while error is None:
-        actions = [producer, issuer] + [lambda w=w: epilogue(w) for w in range(epi_warps)]
+        actions = [producer] + [lambda p=p: issuer(p) for p in range(issuers)]
+        actions += [lambda w=w: epilogue(w) for w in range(epi_warps)]
         actions += [lambda x=x: land(x) for x in range(len(pending_land))]
-        actions += [lambda x=x: mma_complete(x) for x in range(len(pending_mma))]
+        actions += [lambda p=p: mma_complete(p) for p in range(issuers)]
         rng.shuffle(actions)
         if not any(a() for a in actions):
             break
