@@ -119,10 +119,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // Workspace of the weight-stationary matvecs (fp16 and Q8_0): a status word in a 256-byte
-// header, a fixed ticket area (so it stays at the same place, and zero, whatever shapes share
-// the workspace), then the split-K partial tiles.
+// header (split-K partial sums are reduced in distributed shared memory, not here).
 constexpr size_t kWsHeaderBytes = 256;
-constexpr size_t kWsTicketBytes = 65536;  // up to 16384 row blocks (N <= 2,097,152)
 constexpr unsigned kWsStatusTimeout = 1u;
 
 // Named barrier over `nthreads` threads (a subset of the CTA).

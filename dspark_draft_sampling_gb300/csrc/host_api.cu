@@ -145,8 +145,8 @@ extern "C" dspark_status dspark_ws_matvec_host(const uint16_t *W, const uint16_t
     if (need == 0) return fail(DSPARK_ERR_CUDA, "ws_matvec_host: could not size the scratch");
     if (scratch_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec_host: scratch of %zu bytes < required %zu", scratch_bytes, need);
-    // the matvec workspace comes first, so its zero-filled ticket area stays at offset 0 for
-    // every shape that shares the scratch
+    // the matvec workspace (its status word) comes first, at offset 0 for every shape that
+    // shares the scratch
     const size_t ws = dspark_ws_matvec_workspace_bytes(M, N, K);
     unsigned char *p = static_cast<unsigned char *>(device_scratch);
     unsigned char *x_d = p + up256(ws);
@@ -201,7 +201,7 @@ extern "C" dspark_status dspark_ws_matvec_grouped_host(const dspark_ws_problem *
     if (need == 0) return fail(DSPARK_ERR_CUDA, "ws_matvec_grouped_host: could not size the scratch");
     if (scratch_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec_grouped_host: scratch of %zu bytes < required %zu", scratch_bytes, need);
-    // the grouped workspace first (its zero-filled ticket area at offset 0), then per problem
+    // the grouped workspace first (its status word at offset 0), then per problem
     // the device copies of X and Y
     const size_t ws = dspark_ws_matvec_grouped_workspace_bytes(problems, n_problems);
     unsigned char *p = static_cast<unsigned char *>(device_scratch) + up256(ws);

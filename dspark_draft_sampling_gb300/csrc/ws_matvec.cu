@@ -23,13 +23,15 @@
 //    after the last one.
 //  * Warps 0-3 (128 threads, one TMEM lane = one weight row each) load the 128 x 16
 //    accumulator tile with tcgen05.ld.  With one unit per row block they write Y directly.
-//    Otherwise the S units of a row block reduce their fp32 partials in a fixed order,
-//    0 + p_0 + p_1 + ... + p_{S-1}, so the result is deterministic and does not depend on M:
-//    in a single-problem launch the S units form a thread-block cluster and units 1..S-1
-//    store their partial rows into unit 0's shared memory (distributed shared memory), one
-//    cluster barrier, then unit 0 sums and writes Y; in a grouped launch (several problems,
-//    CTAs of different problems in one grid) the partials go through the caller's workspace
-//    and the last unit of the row block (a ticket counter) sums them.  Both give the same bits.
+//    Otherwise the S units of a row block (S in {2, 4, 8}) are CTAs of one thread-block cluster
+//    and reduce their fp32 partials in a fixed order, 0 + p_0 + p_1 + ... + p_{S-1}, so the
+//    result is deterministic and does not depend on M: units 1..S-1 store their partial rows
+//    into unit 0's shared memory (distributed shared memory), a cluster barrier, then unit 0
+//    sums and writes Y.  A single-problem launch gives unit 0 a receive area of its own; a
+//    grouped launch (several problems in one grid, clusters of the largest S, each problem's
+//    units padded to whole clusters) reuses unit 0's ring once a first cluster barrier shows
+//    every unit of the cluster done with its stream.  Both give the same bits, so a problem
+//    gives the same result alone and in a group.
 #include <cuda_fp16.h>
 
 #include "tc.cuh"
@@ -61,13 +63,12 @@ constexpr int kMaxProblems = 8;
 
 struct WsProblem {
     void *Y;
-    float *partial;     // [units][128][16] fp32 (split-K through the workspace only)
-    unsigned *tickets;  // [row blocks]
     int y_fp32;
     int M, N, K;
+    int nrb;    // row blocks (units beyond nrb * S are padding and stream nothing)
     int nkb;    // k-blocks
     int S;      // units per row block
-    int unit0;  // first CTA of this problem in the grid
+    int unit0;  // first CTA of this problem in the grid (a multiple of the cluster size)
 };
 
 // Kernel parameters: up to kMaxProblems independent problems share one launch, CTA b taking
@@ -77,8 +78,10 @@ struct WsProblem {
 struct WsGroup {
     int nprob;
     int nst;            // ring stages
-    int cluster;        // 1: one problem whose S units per row block form a cluster (DSMEM sum)
-    int mcols;          // cluster mode: partial columns sent per row (8 or 16)
+    int cluster;        // 0: no split problem; 1: one problem, unit 0 has a receive area;
+                        // 2: grouped, unit 0's ring receives after a first cluster barrier
+    int csize;          // cluster size (a multiple of every problem's S)
+    int mcols;          // partial columns sent per row (8 or 16)
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
@@ -140,18 +143,19 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
     const int kb0 = static_cast<int>(static_cast<unsigned>(sk) * static_cast<unsigned>(a.nkb) / static_cast<unsigned>(a.S));
     const int kb1 =
         static_cast<int>(static_cast<unsigned>(sk + 1) * static_cast<unsigned>(a.nkb) / static_cast<unsigned>(a.S));
-    const int nk = kb1 - kb0;
+    const int nk = rb < a.nrb ? kb1 - kb0 : 0;  // padding units stream nothing
     const int n0 = rb * kRowsPerUnit;
-    // cluster mode: unit 0 of the row block receives the other units' partial rows here,
-    // [S - 1][128 rows][mcols] fp32
-    const size_t recv_bytes = g.cluster ? size_t(a.S - 1) * kRowsPerUnit * g.mcols * 4 : 0;
-    float *recv = reinterpret_cast<float *>(smem + size_t(nst) * kStageBytes);
+    // split row blocks: unit 0 of the row block receives the other units' partial rows,
+    // [S - 1][128 rows][mcols] fp32, in its own area (cluster mode 1) or its ring (mode 2)
+    const size_t recv_bytes = g.cluster == 1 ? size_t(a.S - 1) * kRowsPerUnit * g.mcols * 4 : 0;
+    float *recv = reinterpret_cast<float *>(smem + (g.cluster == 1 ? size_t(nst) * kStageBytes : 0));
+    const uint32_t leader =
+        static_cast<uint32_t>(static_cast<int>(blockIdx.x) % g.csize - sk);  // cluster rank of unit 0
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(nst) * kStageBytes + recv_bytes);
     uint64_t *empty = full + nst;
     uint64_t *done = empty + nst;
     uint64_t *never = done + 1;  // signalled by nobody: the fault-injection hook waits on it
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
-    int *s_last = reinterpret_cast<int *>(tmem_slot + 1);
 
     if (warp == 4 && lane == 0) {
         // The producer sets up the barriers and starts the first ring's worth of copies before
@@ -248,75 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
                 for (int m = 0; m < kNPad; ++m) y[m] = __uint_as_float(v[m]);
                 store_y(a, row, y);
             }
-        } else if (g.cluster) {
-            // units 1..S-1: this row's partial goes into unit 0's receive area (the cluster
-            // barrier below orders it before unit 0 reads it)
+        } else {
+            // units 1..S-1: this row's partial goes into unit 0's receive area; in a grouped
+            // launch that is unit 0's ring, idle once every unit of the cluster has passed the
+            // first barrier (every unit's stream is done by then)
+            if (g.cluster == 2) cluster_sync_all();
             if (sk != 0) {
                 const uint32_t dst = map_to_rank(
-                    smem_addr(recv + (size_t(sk - 1) * kRowsPerUnit + lrow) * g.mcols), 0u);
+                    smem_addr(recv + (size_t(sk - 1) * kRowsPerUnit + lrow) * g.mcols), leader);
 #pragma unroll
                 for (int q = 0; q < kNPad / 4; ++q)
                     if (4 * q < g.mcols)
                         st_cluster_v4(dst + 16u * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                       __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             }
-        } else {
-            float4 *p = reinterpret_cast<float4 *>(a.partial + (size_t(unit) * kRowsPerUnit + lrow) * kNPad);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                p[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0) *s_last = (atomicAdd(&a.tickets[rb], 1u) == static_cast<unsigned>(a.S - 1));
-            named_bar_sync(1, 128);
-            if (*s_last) {
-                __threadfence();
-                if (ok && row < a.N) {
-                    // y[m] = 0 + partial[0][row][m] + partial[1][row][m] + ...; loads are issued
-                    // four units at a time so their latencies overlap, the sum order is fixed
-                    const float4 *base =
-                        reinterpret_cast<const float4 *>(a.partial + (size_t(rb) * a.S * kRowsPerUnit + lrow) * kNPad);
-                    constexpr size_t kUnitF4 = size_t(kRowsPerUnit) * kNPad / 4;
-                    float y[kNPad];
-#pragma unroll
-                    for (int m = 0; m < kNPad; ++m) y[m] = 0.f;
-                    int s = 0;
-                    for (; s + 4 <= a.S; s += 4) {
-                        float4 t[4][4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) t[u][q] = __ldcg(base + size_t(s + u) * kUnitF4 + q);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                y[4 * q] += t[u][q].x;
-                                y[4 * q + 1] += t[u][q].y;
-                                y[4 * q + 2] += t[u][q].z;
-                                y[4 * q + 3] += t[u][q].w;
-                            }
-                    }
-                    for (; s < a.S; ++s) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 t = __ldcg(base + size_t(s) * kUnitF4 + q);
-                            y[4 * q] += t.x;
-                            y[4 * q + 1] += t.y;
-                            y[4 * q + 2] += t.z;
-                            y[4 * q + 3] += t.w;
-                        }
-                    }
-                    store_y(a, row, y);
-                }
-                if (threadIdx.x == 0) a.tickets[rb] = 0u;  // zero again for the next call
-            }
-        }
-        if (g.cluster && a.S > 1) {
-            cluster_sync_all();
+            cluster_sync_all();  // orders the stores before unit 0 reads them
             if (sk == 0 && ok && row < a.N) {
-                // y[m] = 0 + p_0[m] + p_1[m] + ... + p_{S-1}[m]: the order of the workspace path
+                // y[m] = 0 + p_0[m] + p_1[m] + ... + p_{S-1}[m]
                 float y[kNPad];
 #pragma unroll
                 for (int m = 0; m < kNPad; ++m) y[m] = 0.f + __uint_as_float(v[m]);
@@ -337,7 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
             }
         }
     }
-    if (g.cluster && a.S > 1 && warp >= 4) cluster_sync_all();  // every thread of the cluster arrives
+    // split row blocks: every other thread of the CTA takes part in the cluster barriers
+    if (a.S > 1 && warp >= 4) {
+        if (g.cluster == 2) cluster_sync_all();
+        cluster_sync_all();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -364,14 +320,15 @@ int stages_for(int cps, size_t recv) {
 // and shape of the question).
 bool clusters_fit(int S, int cps, int M, int units);
 
-// The split of K: for S = 1 .. kMaxSplit units per row block with one CTA per SM, the
-// largest number of k-blocks any SM streams when every unit is resident in one wave; the
-// smallest wins, then the smaller S.  A shape with more row blocks than SMs runs unsplit with
-// two CTAs per SM.  (Splits sized for two CTAs per SM were measured about 1 us faster alone on
-// the 12288-row and 12288-wide projections, but their extra short units slowed the grouped
-// launch of the four projections, so they are not used.)  Whether the clusters fit is asked
-// for the largest receive area (M = 16), so the split depends on N and K only and a problem is
-// split the same way in a single and in a grouped launch.
+// The split of K: for S in {1, 2, 4, 8} units per row block with one CTA per SM, the largest
+// number of k-blocks any SM streams when every unit is resident in one wave; the smallest wins,
+// then the smaller S.  A shape with more row blocks than SMs runs unsplit with two CTAs per SM.
+// (Splits sized for two CTAs per SM were measured about 1 us faster alone on the 12288-row and
+// 12288-wide projections, but their extra short units slowed the grouped launch of the four
+// projections, so they are not used.)  S is a power of two so that one cluster size serves
+// every problem of a grouped launch.  Whether the clusters fit is asked for the largest
+// receive area (M = 16), so the split depends on N and K only and a problem is split the same
+// way in a single and in a grouped launch.
 Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
@@ -379,19 +336,16 @@ Plan plan_for(int N, int K, int sms) {
     p.S = 1;
     p.cps = 2;
     long long best = -1;
-    for (int cps = 1; cps <= 1; ++cps) {
-        for (int S = 1; S <= kMaxSplit && S <= p.nkb; ++S) {
-            const long long units = static_cast<long long>(p.nrb) * S;
-            if (units > static_cast<long long>(cps) * sms) break;
-            if (stages_for(cps, recv_bytes_for(S, 16)) < 3) break;
-            if (S > 1 && !clusters_fit(S, cps, 16, static_cast<int>(units))) continue;
-            const long long per_sm = (units + sms - 1) / sms;            // CTAs on the busiest SM
-            const long long load = per_sm * ((p.nkb + S - 1) / S);     // its k-blocks
-            if (best < 0 || load < best) {
-                best = load;
-                p.S = S;
-                p.cps = cps;
-            }
+    for (int S = 1; S <= kMaxSplit && S <= p.nkb; S *= 2) {
+        const long long units = static_cast<long long>(p.nrb) * S;
+        if (units > sms) break;
+        if (stages_for(1, recv_bytes_for(S, 16)) < 3) break;
+        if (S > 1 && !clusters_fit(S, 1, 16, static_cast<int>(units))) continue;
+        const long long load = (p.nkb + S - 1) / S;  // one CTA per SM: its k-blocks
+        if (best < 0 || load < best) {
+            best = load;
+            p.S = S;
+            p.cps = 1;
         }
     }
     return p;
@@ -455,12 +409,11 @@ bool clusters_fit(int S, int cps, int M, int units) {
 }  // namespace dspark
 
 extern "C" size_t dspark_ws_matvec_workspace_bytes(int M, int N, int K) {
-    // a single problem reduces its split-K partials in distributed shared memory: the
-    // workspace holds only the status word and the (unused) ticket area
+    // split rows reduce in distributed shared memory: the workspace holds the status word
     (void)M;
     (void)N;
     (void)K;
-    return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
+    return dspark::kWsHeaderBytes;
 }
 
 namespace {
@@ -482,26 +435,12 @@ dspark_status check_problem(const dspark_ws_problem &q, bool *skip) {
     return DSPARK_OK;
 }
 
-int live_problems(const dspark_ws_problem *probs, int n) {
-    int live = 0;
-    for (int i = 0; i < n; ++i)
-        if (probs[i].N > 0 && probs[i].K > 0 && probs[i].M > 0) ++live;
-    return live;
-}
-
-// Workspace of a group: header, one ticket area (the problems' row blocks one after the
-// other), then each split problem's partial tiles -- unless the launch holds one problem,
-// which reduces in distributed shared memory.  0 when the sizes are invalid.
+// Workspace of a group: the status word (split rows reduce in distributed shared memory).
 size_t group_workspace_bytes(const dspark_ws_problem *probs, int n, int sms) {
-    using namespace dspark;
-    size_t bytes = dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
-    if (live_problems(probs, n) <= 1) return bytes;
-    for (int i = 0; i < n; ++i) {
-        if (probs[i].N <= 0 || probs[i].K <= 0 || probs[i].M <= 0) continue;
-        const Plan p = plan_for(probs[i].N, probs[i].K, sms);
-        if (p.S > 1) bytes += size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
-    }
-    return bytes;
+    (void)probs;
+    (void)n;
+    (void)sms;
+    return dspark::kWsHeaderBytes;
 }
 
 dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *workspace, size_t workspace_bytes,
@@ -534,39 +473,43 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
 
     WsGroup g;
     g.nprob = 0;
-    g.cluster = live == 1 ? 1 : 0;
-    g.mcols = 16;
     g.status = static_cast<unsigned *>(workspace);
     g.timeout_ns = kDefaultTimeoutNs;
     g.stall_ns = stall_ns;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    size_t ticket_off = 0;  // in row blocks
-    size_t partial_off = kWsHeaderBytes + kWsTicketBytes;
-    unsigned units = 0;
     // The grid takes the problems with the longest units first (longest-processing-time
     // order), so the last wave holds short units and the tail stays short.  The order changes
     // no result: every problem keeps its own split and summation order.
     int order[kMaxProblems];
+    Plan plans[kMaxProblems];
     int norder = 0;
     for (int i = 0; i < n; ++i)
-        if (probs[i].M != 0 && probs[i].N != 0) order[norder++] = i;
-    auto unit_blocks = [&](int i) {
-        const Plan p = plan_for(probs[i].N, probs[i].K, sms);
-        return (p.nkb + p.S - 1) / p.S;
-    };
-    for (int a = 1; a < norder; ++a)  // stable insertion sort, longest units first
-        for (int b = a; b > 0 && unit_blocks(order[b]) > unit_blocks(order[b - 1]); --b) {
-            const int t = order[b];
-            order[b] = order[b - 1];
-            order[b - 1] = t;
+        if (probs[i].M != 0 && probs[i].N != 0) {
+            plans[norder] = plan_for(probs[i].N, probs[i].K, sms);
+            order[norder++] = i;
         }
-    Plan solo = {};
-    for (int oi = 0; oi < norder; ++oi) {
-        const dspark_ws_problem &q = probs[order[oi]];
-        const Plan p = plan_for(q.N, q.K, sms);
-        solo = p;
-        if ((ticket_off + p.nrb) * sizeof(unsigned) > kWsTicketBytes)
-            return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec: more than %zu rows in one call", kWsTicketBytes / 4 * kRowsPerUnit);
+    auto unit_blocks = [&](int j) { return (plans[j].nkb + plans[j].S - 1) / plans[j].S; };
+    int idx[kMaxProblems];
+    for (int j = 0; j < norder; ++j) idx[j] = j;
+    for (int a = 1; a < norder; ++a)  // stable insertion sort, longest units first
+        for (int b = a; b > 0 && unit_blocks(idx[b]) > unit_blocks(idx[b - 1]); --b) {
+            const int t = idx[b];
+            idx[b] = idx[b - 1];
+            idx[b - 1] = t;
+        }
+    // cluster size: the largest split (every split is a power of two, so it divides this one)
+    int csize = 1, mmax = 0;
+    for (int j = 0; j < norder; ++j) {
+        csize = plans[j].S > csize ? plans[j].S : csize;
+        mmax = probs[order[j]].M > mmax ? probs[order[j]].M : mmax;
+    }
+    g.csize = csize;
+    g.mcols = mmax <= 8 ? 8 : 16;
+    g.cluster = csize == 1 ? 0 : (live == 1 ? 1 : 2);
+    unsigned units = 0;
+    for (int oj = 0; oj < norder; ++oj) {
+        const int jj = idx[oj];
+        const dspark_ws_problem &q = probs[order[jj]];
+        const Plan &p = plans[jj];
         const int j = g.nprob++;
         st = make_tmap_2d(&g.tmW[j], q.W, false, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K), kRowsPerUnit,
                           kKB);
@@ -579,18 +522,13 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
         a.M = q.M;
         a.N = q.N;
         a.K = q.K;
+        a.nrb = p.nrb;
         a.nkb = p.nkb;
         a.S = p.S;
         a.unit0 = static_cast<int>(units);
-        a.tickets = nullptr;
-        a.partial = nullptr;
-        if (p.S > 1 && !g.cluster) {
-            a.tickets = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes) + ticket_off;
-            a.partial = reinterpret_cast<float *>(ws + partial_off);
-            ticket_off += p.nrb;
-            partial_off += size_t(p.nrb) * p.S * kRowsPerUnit * kNPad * sizeof(float);
-        }
-        units += static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
+        // whole clusters per problem: the last one may hold padding units
+        const unsigned pu = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
+        units += (pu + static_cast<unsigned>(csize) - 1) / static_cast<unsigned>(csize) * static_cast<unsigned>(csize);
     }
 
     cudaLaunchConfig_t cfg = {};
@@ -600,23 +538,22 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     size_t recv = 0;
-    if (g.cluster) {
-        // one problem: the ring sized for the CTAs per SM its split assumed, and for S > 1 the
-        // S units of a row block as one cluster with unit 0's receive area
-        const int M = g.prob[0].M;
-        g.mcols = M <= 8 ? 8 : 16;
-        recv = solo.S > 1 ? recv_bytes_for(solo.S, M) : 0;
-        g.nst = stages_for(solo.cps, recv);
-        if (solo.S > 1) {
-            attr[1].id = cudaLaunchAttributeClusterDimension;
-            attr[1].val.clusterDim.x = static_cast<unsigned>(solo.S);
-            attr[1].val.clusterDim.y = 1;
-            attr[1].val.clusterDim.z = 1;
-            cfg.numAttrs = 2;
-        }
+    if (live == 1) {
+        // one problem: the ring sized for the CTAs per SM its split assumed, and for S > 1 a
+        // receive area for unit 0
+        recv = csize > 1 ? recv_bytes_for(csize, g.prob[0].M) : 0;
+        g.nst = stages_for(plans[0].cps, recv);
     } else {
-        // more units than SMs: two CTAs per SM with the shallower ring
+        // more units than SMs: two CTAs per SM with the shallower ring (unit 0 receives the
+        // partials in its ring, which holds (S - 1) x 128 x 16 fp32 even at S = 8)
         g.nst = units > static_cast<unsigned>(sms) ? kStagesShared : kStagesSolo;
+    }
+    if (csize > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     cfg.gridDim = dim3(units);
     cfg.blockDim = dim3(kThreads);

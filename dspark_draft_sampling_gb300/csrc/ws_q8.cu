@@ -559,12 +559,11 @@ extern "C" dspark_status dspark_q8_0_repack(const void *w_q8_0, int8_t *q, uint1
 }
 
 extern "C" size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K) {
-    // split rows reduce in distributed shared memory: the workspace holds only the status
-    // word and the (unused) ticket area
+    // split rows reduce in distributed shared memory: the workspace holds the status word
     (void)M;
     (void)N;
     (void)K;
-    return dspark::kWsHeaderBytes + dspark::kWsTicketBytes;
+    return dspark::kWsHeaderBytes;
 }
 
 namespace {
@@ -592,9 +591,7 @@ dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X
     dspark_status st0 = configure_kernel(dev);
     if (st0 != DSPARK_OK) return st0;
     const Plan p = plan_for(N, K, sms);
-    if (size_t(p.nrb) * sizeof(unsigned) > kWsTicketBytes)
-        return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: N=%d exceeds %zu rows", N, kWsTicketBytes / 4 * kRows);
-    const size_t need = kWsHeaderBytes + kWsTicketBytes;
+    const size_t need = kWsHeaderBytes;
     if (workspace_bytes < need)
         return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
 

@@ -206,17 +206,18 @@ dspark_status dspark_conf_probe_split(const void *w_q8_0, const float *hidden, i
  *   Y[m, n] = sum_k X[m, k] * W[n, k]      (fp16 inputs, fp32 accumulation)
  *
  * Runs on the tcgen05 tensor cores (128 weight rows x 16 padded activation rows per MMA).
- * K may be split over several CTAs (about one per SM in total); their fp32 partial sums
- * are added by the last of them in a fixed order.
+ * K may be split over S = 2, 4 or 8 CTAs per 128-row block (chosen from N, K and the SM
+ * count); they form a thread-block cluster and their fp32 partial sums are added in
+ * distributed shared memory in a fixed order, 0 + p_0 + ... + p_{S-1}.
  *
  * Arguments
  *   W          fp16 [N, K] (out x in), 16-byte aligned
  *   X          fp16 [M, K], 16-byte aligned
  *   Y          [M, N]: fp32 if y_is_fp32, else fp16 rounded to nearest even
  *   workspace  device scratch of at least dspark_ws_matvec_workspace_bytes(M, N, K)
- *              bytes (depends on N, K and the current device), 256-byte aligned, and
- *              ZERO-FILLED before its first use; every call leaves it zero-filled again.
- *              Calls sharing a workspace must not overlap on the device.
+ *              bytes (256), 256-byte aligned, ZERO-FILLED before its first use: it holds
+ *              the device status word (see dspark_ws_matvec_status).  Calls sharing a
+ *              workspace must not overlap on the device.
  *   Supported: 1 <= M <= 16, N >= 1, K >= 8 with K % 8 == 0 (M == 0 or N == 0
  *   enqueues nothing).  The result of row m does not depend on M: every output is
  *   summed in one fixed order.
@@ -232,10 +233,8 @@ dspark_status dspark_ws_matvec(const uint16_t *W, const uint16_t *X, void *Y, in
  * the SMs left idle by one problem's tail take the next one's units.  Each problem has the
  * arguments and limits of dspark_ws_matvec; its results are bit-identical to a separate
  * dspark_ws_matvec call.  Problems with M == 0 or N == 0 are skipped.  The workspace
- * (dspark_ws_matvec_grouped_workspace_bytes(problems, n), zero-filled before first use, left
- * zero-filled) is laid out like dspark_ws_matvec's, with the problems' tickets and partial
- * tiles one after the other; at most 16384 row blocks of 128 rows in one call.
- * More than 8 problems: DSPARK_ERR_UNSUPPORTED. */
+ * (dspark_ws_matvec_grouped_workspace_bytes(problems, n), zero-filled before first use) holds
+ * the status word, as for dspark_ws_matvec.  More than 8 problems: DSPARK_ERR_UNSUPPORTED. */
 typedef struct dspark_ws_problem {
     const uint16_t *W;  /* fp16 [N, K] */
     const uint16_t *X;  /* fp16 [M, K] */
@@ -252,8 +251,8 @@ dspark_status dspark_ws_matvec_grouped(const dspark_ws_problem *problems, int n_
 /* Synchronizes `stream`, then reads the status word of a dspark_ws_matvec or
  * dspark_ws_matvec_q8 workspace (its first 4 bytes): DSPARK_OK, or DSPARK_ERR_TIMEOUT if a
  * device-side wait of a call on it gave up since the last check (the kernel then skipped
- * the affected outputs and returned).  A reported timeout is cleared, leaving the workspace
- * zero-filled again. */
+ * the affected outputs and returned).  A reported timeout is cleared, leaving the status
+ * word zero again. */
 dspark_status dspark_ws_matvec_status(void *workspace, dspark_stream_t stream);
 
 /* Fault-injection hook for testing the device-side wait limit: the same launch as
@@ -285,9 +284,12 @@ dspark_status dspark_ws_matvec_debug(const uint16_t *W, const uint16_t *X, void 
  * weight d * q is never rounded to a 16-bit type.
  *   X          fp16 [M, K], 16-byte aligned
  *   Y          [M, N]: fp32 if y_is_fp32, else fp16 rounded to nearest even
- *   workspace  device scratch of at least dspark_ws_matvec_q8_workspace_bytes(M, N, K) bytes,
- *              256-byte aligned and ZERO-FILLED before its first use; every call leaves it
- *              zero-filled again.  Calls sharing a workspace must not overlap on the device.
+ *   workspace  device scratch of at least dspark_ws_matvec_q8_workspace_bytes(M, N, K) bytes
+ *              (256), 256-byte aligned and ZERO-FILLED before its first use: it holds the
+ *              device status word.  Calls sharing a workspace must not overlap on the device.
+ *   K is split over S <= 8 CTAs per 128-row block when there are at most as many row blocks
+ *   as SMs; the S CTAs form a thread-block cluster and add their partial sums in distributed
+ *   shared memory in a fixed order.
  *   Supported: 1 <= M <= 16, N >= 1, K a positive multiple of 256 (M == 0 or N == 0 enqueues
  *   nothing).  Every output is summed in one fixed order, so row m's result does not depend
  *   on M.
@@ -321,7 +323,7 @@ dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, co
  * device_scratch: caller-owned device memory of at least the matching *_scratch_bytes(),
  * 256-byte aligned; it holds the device copies of the inputs and outputs and the operation's
  * workspace.  For dspark_ws_matvec_host the scratch must be ZERO-FILLED before first use
- * (its first part is the matvec workspace; every call leaves it zero-filled again).  Calls
+ * (its first part is the matvec workspace with its status word).  Calls
  * sharing a scratch must not overlap on the device.
  *
  *   dspark_markov_draft_host: base_host float [num_reqs, k, vocab]; prev_host int64

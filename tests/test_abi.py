@@ -51,6 +51,8 @@ def test_workspace_bytes(dspark_lib):
     b = dspark_lib.dspark_markov_workspace_bytes(8, 15, 248320, 256)
     assert a == b and a % 256 == 0 and a >= 256 + 15 * 8 * 8
     assert dspark_lib.dspark_markov_workspace_bytes(1, 0, 10, 64) == 256
+    # the matvecs' workspaces hold only the status word
+    assert dspark_lib.dspark_ws_matvec_workspace_bytes(7, 4096, 4096) == 256
 
 
 def _markov(lib, *, base=FAKE, w1=FAKE, w2=FAKE, d2t=NULL, prev=FAKE, B=1, k=4, V=4096, R=64,
@@ -188,7 +190,7 @@ def test_ws_q8_validation(dspark_lib):
     assert g(ws=FAKE_ODD) == INVALID
     assert g(M=0) == 0
     assert g(N=0) == 0
-    assert lib.dspark_ws_matvec_q8_workspace_bytes(7, 0, 256) == 65536 + 256
+    assert lib.dspark_ws_matvec_q8_workspace_bytes(7, 0, 256) == 256  # the status word
     r = lib.dspark_q8_0_repack
     assert r(FAKE, FAKE, FAKE, 4, 48, NULL) == INVALID
     assert r(FAKE, FAKE, FAKE, -1, 64, NULL) == INVALID

@@ -1,5 +1,5 @@
-"""Parity at the documented size limits: the WS matvecs at the largest N their ticket area
-serves (2,097,152 rows) with M = 16, the first unsupported N, and a probe far wider than the
+"""Parity at large sizes: the WS matvecs with 2,097,152 rows (16384 row blocks, so the grid
+runs in many waves) and M = 16, a ragged row count beyond it, and a probe far wider than the
 7424-wide workload."""
 import ctypes
 
@@ -12,7 +12,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-MAX_N = 16384 * 128  # one 4-byte ticket per 128-row block in a 64 KB area
+MAX_N = 16384 * 128  # 16384 row blocks of 128 rows
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,13 +29,20 @@ def test_fp16_matvec_at_max_rows_and_m():
     parity.check_ws(inp, y32=y.cpu().numpy())
 
 
-def test_fp16_matvec_rejects_one_row_block_more():
-    W = torch.zeros((MAX_N + 1, 8), dtype=torch.float16, device="cuda")
-    X = torch.zeros((1, 8), dtype=torch.float16, device="cuda")
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
-    with pytest.raises(api.DsparkError) as e:
-        api.ws_matvec(W, X, workspace=ws)
-    assert e.value.status == api.DSPARK_ERR_UNSUPPORTED
+def test_fp16_matvec_ragged_rows_beyond_max_sampled():
+    """One row block and one row more (a partial last block): a seeded sample of 4096 weight
+    rows, plus the last 129, against the oracle (each output row depends only on its own
+    weights)."""
+    N, K, M = MAX_N + 129, 64, 16
+    inp = synth.ws_inputs(M, N, K, seed=2, w_sd=0.5)
+    W = torch.from_numpy(inp["W"].view(np.int16)).cuda().view(torch.float16)
+    X = torch.from_numpy(inp["X"].view(np.int16)).cuda().view(torch.float16)
+    y = api.ws_matvec(W, X, out_fp32=True)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.random.default_rng(3).choice(N, 4096, replace=False),
+                                     np.arange(N - 129, N)]))
+    sub = dict(W=np.ascontiguousarray(inp["W"][rows]), X=inp["X"], M=M, N=len(rows), K=K)
+    parity.check_ws(sub, y32=y.cpu().numpy()[:, rows])
 
 
 def test_q8_matvec_at_max_rows_and_m_sampled():

@@ -91,8 +91,8 @@ def test_repeat_bit_identical():
 
 
 def test_workspace_shared_across_shapes():
-    """One zero-filled workspace serves calls of different shapes in any order: the split-K
-    tickets live in a fixed area that every call leaves zero."""
+    """One zero-filled workspace serves calls of different shapes in any order (it holds only
+    the status word; split-K partials are reduced in distributed shared memory)."""
     shapes = [(7, 1024, 4096), (7, 4096, 4096), (3, 12288, 4096), (7, 4096, 12288)]
     size = max(api.ws_matvec_workspace_bytes(*s) for s in shapes)
     ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
@@ -124,7 +124,7 @@ def test_workspace_status_reports_a_wait_that_gave_up():
     y2 = api.ws_matvec(W, X, out_fp32=True, workspace=ws)
     assert api.ws_matvec_status(ws) == 0
     parity.check_ws(inp, y32=y2.cpu().numpy())
-    assert int(ws[:65536 + 256].count_nonzero()) == 0
+    assert int(ws[:256].count_nonzero()) == 0
 
 
 def _problems(shapes, seed, fp32):
@@ -170,4 +170,4 @@ def test_grouped_workspace_reuse_and_empty_problems():
         for (W, X, Y), inp in zip(probs, inps):
             parity.check_ws(inp, y32=Y.cpu().numpy())
     assert api.ws_matvec_status(ws) == 0
-    assert int(ws[:65536 + 256].count_nonzero()) == 0
+    assert int(ws[:256].count_nonzero()) == 0
