@@ -7,10 +7,14 @@
 // One CTA of 256 threads per probe.  Thread t walks the 16-byte chunks t, t + 256, ... of the
 // hidden vector (one vector load each), dequantizes the matching four int8 weights with their
 // block's fp16 scale exactly in fp32, and accumulates in chunk order; a fixed warp butterfly
-// plus an in-order sum of the eight warp totals gives z.  Two load schedules, the same
-// arithmetic in the same order (so the same bits): for a large batch a loop unrolled four
-// times (many CTAs resident, few registers each), for a small batch or a single probe every
-// chunk load of a thread issued before any is used (one memory latency per probe).  The gate
+// plus an in-order sum of the eight warp totals gives z.  Three load schedules, the same
+// arithmetic in the same order (so the same bits): for a small batch or a single probe every
+// chunk load of a thread issued before any is used (one memory latency per probe); for a
+// large batch persistent CTAs (one per SM) that stage the Q8_0 row in shared memory by a bulk
+// copy, decode it once, and stream whole hidden rows through a ring of bulk copies
+// (cp.async.bulk, one thread issuing, several rows in flight per SM) to two groups of 256
+// threads taking alternate probes; or, when the ring does not fit shared memory, a loop
+// unrolled four times with one CTA per probe.  The gate
 // compares z with logit(threshold) (computed on the host), which is the same decision as
 // sigmoid(z) >= threshold without evaluating an exponential on the device.
 #include <cuda_fp16.h>
@@ -100,6 +104,177 @@ __global__ void __launch_bounds__(kProbeThreads)
     }
 }
 
+// ---- large batches: persistent CTAs, hidden rows through a ring of bulk copies ----------
+// Two consumer groups of 256 threads take alternate probes (each group does the arithmetic of
+// conf_probe_kernel for its probe); warp 16 issues the copies.
+constexpr int kRingGroups = 2;
+constexpr int kRingConsumers = kRingGroups * kProbeThreads;
+constexpr int kRingThreads = kRingConsumers + 32;
+constexpr int kRingMaxSlots = 8;
+constexpr size_t kRingSmemBudget = 227 * 1024;
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Block scales padded to 16 bytes, so the ring (bulk-copy destinations) stays 16-byte aligned.
+__host__ __device__ inline size_t ring_scale_bytes(int nchunks) { return (size_t(nchunks / 8) * 4 + 15) / 16 * 16; }
+// The raw Q8_0 row staged for decoding: its bytes plus up to 15 on either side of the
+// 16-byte-aligned interior that the bulk copy moves.
+__host__ __device__ inline size_t ring_raw_bytes(int nchunks) { return (size_t(nchunks / 8) * 34 + 32 + 15) / 16 * 16; }
+
+// Shared memory: the decoded weights (q as 4 floats per chunk, d per block), the ring of
+// nslots hidden rows, the raw Q8_0 row, the barriers and the warp totals.
+size_t ring_smem_bytes(int nchunks, int nslots) {
+    return 128 + size_t(nchunks) * 16 + ring_scale_bytes(nchunks) + size_t(nslots) * nchunks * 16 +
+           ring_raw_bytes(nchunks) + (2 * kRingMaxSlots + 1) * 8 + kRingGroups * 2 * kProbeWarps * 4 + 16;
+}
+
+__global__ void __launch_bounds__(kRingThreads, 1)
+    conf_probe_ring_kernel(const uint8_t *__restrict__ wq, const float *__restrict__ xa, long long lda, int nchunks_a,
+                           const float *__restrict__ xb, long long ldb, int nchunks_b, float bias, float t_logit,
+                           float *logit_out, int32_t *gate_out, int n_probes, int nslots,
+                           unsigned long long timeout_ns) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+    const int nchunks = nchunks_a + nchunks_b;
+    const int nbytes = (nchunks / 8) * 34;                               // the Q8_0 row
+    float4 *wq4 = reinterpret_cast<float4 *>(sm);                        // [nchunks] q as floats
+    float *wd = reinterpret_cast<float *>(wq4 + nchunks);                // [nchunks / 8] block scales
+    float4 *ring = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(wd) +
+                                              ring_scale_bytes(nchunks));  // [nslots][nchunks] hidden rows
+    unsigned char *raw = reinterpret_cast<unsigned char *>(ring + size_t(nslots) * nchunks);
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw + ring_raw_bytes(nchunks));
+    uint64_t *empty = full + kRingMaxSlots;
+    uint64_t *wbar = empty + kRingMaxSlots;                              // the raw row landed
+    float *warp_sum = reinterpret_cast<float *>(wbar + 1);               // [groups][2][kProbeWarps]
+    int *s_abort = reinterpret_cast<int *>(warp_sum + kRingGroups * 2 * kProbeWarps);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // the row's 16-byte-aligned interior [ia, ib) goes by bulk copy, to raw + (ia - row0) where
+    // row0 = wq - lead keeps that destination 16-byte aligned; the ragged ends by byte loads
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(wq);
+    const uintptr_t ia = (w0 + 15) & ~uintptr_t(15);
+    const uintptr_t ib = (w0 + nbytes) & ~uintptr_t(15);
+    const int lead = static_cast<int>(w0 & 15);  // raw[lead + i] holds row byte i
+    const bool interior = ib > ia;
+
+    if (threadIdx.x == kRingConsumers) {
+        for (int q = 0; q < kRingMaxSlots; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], 1);
+        }
+        mbar_init(wbar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    pdl_wait();  // no global-memory access before this point
+
+    if (warp == kRingConsumers / 32) {
+        // ---- copy issuer: the weight row, then the CTA's probes p = blockIdx.x, + gridDim.x, ... ----
+        if (lane == 0) {
+            if (interior) {
+                mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(ib - ia));
+                bulk_copy_g2s(raw + lead + (ia - w0), reinterpret_cast<const void *>(ia), static_cast<uint32_t>(ib - ia),
+                              wbar);
+            }
+            const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
+            int j = 0;
+            for (int p = blockIdx.x; p < n_probes; p += gridDim.x, ++j) {
+                const int q = j % nslots;
+                if (j >= nslots && !mbar_wait(&empty[q], static_cast<uint32_t>((j / nslots) & 1) ^ 1u, timeout_ns)) {
+                    *reinterpret_cast<volatile int *>(s_abort) = 1;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int *>(s_abort)) break;
+                float4 *dst = ring + size_t(q) * nchunks;
+                mbar_arrive_expect_tx(&full[q], bytes);
+                bulk_copy_g2s(dst, xa + size_t(p) * lda, static_cast<uint32_t>(nchunks_a) * 16u, &full[q]);
+                if (nchunks_b)
+                    bulk_copy_g2s(dst + nchunks_a, xb + size_t(p) * ldb, static_cast<uint32_t>(nchunks_b) * 16u,
+                                  &full[q]);
+            }
+            // copies still in flight land before the CTA exits
+            for (int i = j > nslots ? j - nslots : 0; i < j; ++i)
+                mbar_wait(&full[i % nslots], static_cast<uint32_t>((i / nslots) & 1), timeout_ns);
+            if (interior) mbar_wait(wbar, 0, timeout_ns);
+        }
+        return;
+    }
+    // ---- consumers: decode the Q8_0 row once (from shared memory), then one probe per slot ----
+    const int t = threadIdx.x;  // 0 .. kRingConsumers - 1
+    {
+        // ragged ends of the row (at most 15 bytes each) by byte loads
+        const int head = interior ? static_cast<int>(ia - w0) : nbytes;
+        const int tail0 = interior ? static_cast<int>(ib - w0) : nbytes;
+        for (int i = t; i < head; i += kRingConsumers) raw[lead + i] = __ldg(wq + i);
+        for (int i = tail0 + t; i < nbytes; i += kRingConsumers) raw[lead + i] = __ldg(wq + i);
+        bool ok = !interior || mbar_wait(wbar, 0, timeout_ns);
+        if (!ok) *reinterpret_cast<volatile int *>(s_abort) = 1;
+        named_bar_sync(3, kRingConsumers);
+        const unsigned char *rw = raw + lead;
+        for (int c = t; c < nchunks; c += kRingConsumers) {
+            const unsigned char *blk = rw + size_t(c >> 3) * 34;
+            const int off = 2 + 4 * (c & 7);
+            if ((c & 7) == 0) {
+                const unsigned short dbits = static_cast<unsigned short>(blk[0] | (blk[1] << 8));
+                wd[c >> 3] = __half2float(__ushort_as_half(dbits));
+            }
+            wq4[c] = make_float4(static_cast<float>(static_cast<int8_t>(blk[off + 0])),
+                                 static_cast<float>(static_cast<int8_t>(blk[off + 1])),
+                                 static_cast<float>(static_cast<int8_t>(blk[off + 2])),
+                                 static_cast<float>(static_cast<int8_t>(blk[off + 3])));
+        }
+        named_bar_sync(3, kRingConsumers);
+    }
+    const int grp = t / kProbeThreads;
+    const int tid = t - grp * kProbeThreads;  // the thread index of conf_probe_kernel
+    const int gwarp = tid >> 5;
+    int j = grp;
+    for (int p = blockIdx.x + grp * gridDim.x; p < n_probes; p += kRingGroups * gridDim.x, j += kRingGroups) {
+        const int q = j % nslots;
+        bool ok = !*reinterpret_cast<volatile int *>(s_abort) &&
+                  mbar_wait(&full[q], static_cast<uint32_t>((j / nslots) & 1), timeout_ns);
+        float acc = 0.f;
+        if (ok) {
+            const float4 *x = ring + size_t(q) * nchunks;
+#pragma unroll 4
+            for (int c = tid; c < nchunks; c += kProbeThreads) {  // the order of conf_probe_kernel
+                const float4 xv = x[c];
+                const float4 w = wq4[c];
+                float s = w.x * xv.x;
+                s = fmaf(w.y, xv.y, s);
+                s = fmaf(w.z, xv.z, s);
+                s = fmaf(w.w, xv.w, s);
+                acc = fmaf(wd[c >> 3], s, acc);
+            }
+        } else {
+            *reinterpret_cast<volatile int *>(s_abort) = 1;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        float *ws = warp_sum + (grp * 2 + ((j / kRingGroups) & 1)) * kProbeWarps;
+        if (lane == 0) ws[gwarp] = acc;
+        named_bar_sync(1 + grp, kProbeThreads);  // the group is done with slot q and wrote its totals
+        if (tid == 0) {
+            mbar_arrive(&empty[q]);
+            float z = ws[0];
+#pragma unroll
+            for (int w = 1; w < kProbeWarps; ++w) z += ws[w];
+            z += bias;
+            // a wait that gave up (never in normal operation): gate -1, logit NaN
+            const bool good = !*reinterpret_cast<volatile int *>(s_abort);
+            if (logit_out) logit_out[p] = good ? z : __int_as_float(0x7fc00000);
+            gate_out[p] = good ? ((z >= t_logit) ? 1 : 0) : -1;
+        }
+    }
+}
+
 }  // namespace
 
 dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long long lda, const float *xb, int Kb,
@@ -132,6 +307,27 @@ dspark_status probe_enqueue(const void *w_q8_0, const float *xa, int Ka, long lo
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
     const bool ahead = n_probes <= 8 * sms;
+    const int nchunks = K / 4;
+    int nslots = 0;
+    while (nslots < kRingMaxSlots && ring_smem_bytes(nchunks, nslots + 1) <= kRingSmemBudget) ++nslots;
+    if (!ahead && !set_cond && nslots >= 3) {
+        static int configured_dev = -1;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        if (configured_dev != dev) {
+            e = cudaFuncSetAttribute(conf_probe_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kRingSmemBudget));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(conf_probe_ring)");
+            configured_dev = dev;
+        }
+        const unsigned grid = static_cast<unsigned>(n_probes < sms ? n_probes : sms);
+        e = launch_pdl(conf_probe_ring_kernel, dim3(grid), dim3(kRingThreads), ring_smem_bytes(nchunks, nslots), stream,
+                       wb, xa, lda, Ka / 4, xbp, ldb, Kb / 4, bias, t_logit, logit_out, gate_out, n_probes, nslots,
+                       kDefaultTimeoutNs);
+        if (e != cudaSuccess) return cuda_fail(e, "conf_probe launch");
+        return DSPARK_OK;
+    }
     auto kern = ahead ? conf_probe_kernel<true> : conf_probe_kernel<false>;
     cudaError_t e;
     if (set_cond) {  // inside a conditional graph: plain launch

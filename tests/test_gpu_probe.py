@@ -120,3 +120,31 @@ def test_gate_into_pinned_host_memory():
     np.testing.assert_array_equal(g_host.numpy(), g_dev.cpu().numpy())
     _, go = parity.oracle.conf_probe(inp["wq"], inp["hidden"], inp["bias"], 0.5)
     np.testing.assert_array_equal(g_host.numpy(), go)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_large_batch_ring_matches_small_batches_bitwise(split):
+    """A batch large enough for the persistent bulk-copy ring kernel (2048 probes) gives the
+    same bits, probe by probe, as the same probes run 64 at a time (one CTA per probe, every
+    load in flight); with split=True both run over the two-piece input (the ring then copies
+    each row in two pieces), with random block scales and an odd number of probes."""
+    n = 2047
+    inp = synth.probe_inputs(n, 7424, seed=11, random_scales=True, scale=0.01)
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    full = torch.from_numpy(inp["hidden"]).cuda()
+
+    def run(lo, hi):
+        if not split:
+            return api.conf_probe(wq, full[lo:hi], inp["bias"], 0.5)
+        wide = torch.zeros((hi - lo, 7168 + 64), dtype=torch.float32, device="cuda")
+        wide[:, :7168] = full[lo:hi, :7168]
+        return api.conf_probe_split(wq, wide[:, :7168], full[lo:hi, 7168:].contiguous(), inp["bias"], 0.5)
+
+    z_big, g_big = run(0, n)
+    torch.cuda.synchronize()
+    for lo in range(0, n, 64):
+        z, g = run(lo, min(n, lo + 64))
+        torch.cuda.synchronize()
+        assert torch.equal(z.view(torch.int32), z_big[lo:lo + 64].view(torch.int32)), lo
+        assert torch.equal(g, g_big[lo:lo + 64]), lo
+    parity.check_probe(inp, z_big.cpu().numpy(), g_big.cpu().numpy())
