@@ -172,11 +172,15 @@ dspark_status dspark_markov_draft_noalloc(const float *base_logits, const uint16
  *   bias       scalar added to every probe's dot product
  *   threshold  in (0, 1)
  *   K          > 0, multiple of 32
- *   n_probes   >= 0 (0 enqueues nothing); probes are independent (one CTA each)
+ *   n_probes   >= 0 (0 enqueues nothing); probes are independent.  Small batches run one
+ *              CTA per probe; batches larger than 8 x the SM count run on persistent CTAs
+ *              that stream the hidden rows through a ring of bulk copies.  Every probe gives
+ *              the same bits either way.
  *   logit_out  float [n_probes] or NULL
- *   gate_out   int32 [n_probes]: 1 = keep drafting, 0 = stop.  May be device memory or
- *              mapped pinned host memory (then the 4-byte readback is the kernel's
- *              own store).  Must not be NULL.
+ *   gate_out   int32 [n_probes]: 1 = keep drafting, 0 = stop; -1 (with a NaN logit) only if
+ *              a device-side wait of the large-batch form gave up, which does not happen in
+ *              normal operation.  May be device memory or mapped pinned host memory (then
+ *              the 4-byte readback is the kernel's own store).  Must not be NULL.
  * ===================================================================================== */
 dspark_status dspark_conf_probe(const void *w_q8_0, const float *hidden, float bias,
                                 float threshold, int K, int n_probes, float *logit_out,
