@@ -71,11 +71,13 @@ struct WsProblem {
     int unit0;  // first CTA of this problem in the grid (a multiple of the cluster size)
 };
 
-// Kernel parameters: up to kMaxProblems independent problems share one launch, CTA b taking
-// unit b - unit0 of the problem whose range holds it.  The tensor maps stay in parameter
-// space (__grid_constant__), where TMA reads them.  The scalars and problem descriptors come
-// first: a CTA's first reads of the (cold) parameter block then fall on its first lines.
-struct WsGroup {
+// Kernel parameters: up to P independent problems share one launch, CTA b taking unit
+// b - unit0 of the problem whose range holds it.  The tensor maps stay in parameter space
+// (__grid_constant__), where TMA reads them.  The scalars and problem descriptors come first:
+// a CTA's first reads of the (cold) parameter block then fall on its first lines.  A
+// single-problem launch uses P = 1, a parameter block of ~0.3 KB instead of ~2.5 KB.
+template <int P>
+struct WsGroupT {
     int nprob;
     int nst;            // ring stages
     int cluster;        // 0: no split problem; 1: one problem, unit 0 has a receive area;
@@ -86,10 +88,12 @@ struct WsGroup {
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
                                   // this long on a barrier that nothing signals
-    WsProblem prob[kMaxProblems];
-    CUtensorMap tmW[kMaxProblems];
-    CUtensorMap tmX[kMaxProblems];
+    WsProblem prob[P];
+    CUtensorMap tmW[P];
+    CUtensorMap tmX[P];
 };
+using WsGroup = WsGroupT<kMaxProblems>;
+
 
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr_cta, uint32_t rank) {
@@ -123,7 +127,8 @@ __device__ __forceinline__ void store_y(const WsProblem &a, int row, const float
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_constant__ WsGroup g) {
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_constant__ WsGroupT<P> g) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-aligned tiles
@@ -355,14 +360,17 @@ Plan plan_for(int N, int K, int sms) {
 dspark_status configure_kernel(int dev) {
     static int configured_dev = -1;
     if (configured_dev == dev) return DSPARK_OK;
-    cudaError_t e = cudaFuncSetAttribute(ws_matvec_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemSolo));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_matvec_tc_kernel, kThreads,
-                                                      smem_bytes_for(kStagesSolo, 0));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
-    if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
+    const void *kerns[2] = {reinterpret_cast<const void *>(ws_matvec_tc_kernel<1>),
+                            reinterpret_cast<const void *>(ws_matvec_tc_kernel<kMaxProblems>)};
+    for (const void *kern : kerns) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemSolo));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec)");
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes_for(kStagesSolo, 0));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec)");
+        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec kernel cannot be resident on an SM");
+    }
     configured_dev = dev;
     return DSPARK_OK;
 }
@@ -395,7 +403,7 @@ bool clusters_fit(int S, int cps, int M, int units) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, ws_matvec_tc_kernel, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&c, ws_matvec_tc_kernel<1>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             c = 0;
         }
@@ -559,7 +567,23 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes_for(g.nst, recv);
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    e = cudaLaunchKernelEx(&cfg, ws_matvec_tc_kernel, g);
+    if (g.nprob == 1) {  // the small parameter block
+        WsGroupT<1> g1;
+        g1.nprob = 1;
+        g1.nst = g.nst;
+        g1.cluster = g.cluster;
+        g1.csize = g.csize;
+        g1.mcols = g.mcols;
+        g1.status = g.status;
+        g1.timeout_ns = g.timeout_ns;
+        g1.stall_ns = g.stall_ns;
+        g1.prob[0] = g.prob[0];
+        g1.tmW[0] = g.tmW[0];
+        g1.tmX[0] = g.tmX[0];
+        e = cudaLaunchKernelEx(&cfg, ws_matvec_tc_kernel<1>, g1);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, ws_matvec_tc_kernel<kMaxProblems>, g);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec launch");
     return DSPARK_OK;
 }

@@ -189,7 +189,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
+    // TMA producer state (warp kTmaWarp, lane 0): unit u (its geometry computed once), stage j
+    // within it, stage J overall
+    int pu = blockIdx.x, pj = 0, pJ = 0;
+    Unit pug = unit_geometry(a, pu < a.units ? pu : 0);
+    bool pstop = false;
+    uint64_t pol_q = 0, pol_x = 0;
+    // issues the stages up to (not including) stage Jend: int8 tile + two X atoms per stage
+    auto produce = [&](int Jend) {
+        while (!pstop && pu < a.units && pJ < Jend) {
+            if (pj >= pug.nst) {
+                pu += gridDim.x;
+                pj = 0;
+                if (pu < a.units) pug = unit_geometry(a, pu);
+                continue;
+            }
+            const int st = pJ % kStages;
+            // slot st was last used by stage J - kStages
+            if (!mbar_wait(&done[st], static_cast<uint32_t>(((pJ / kStages) & 1) ^ 1), a.timeout_ns)) {
+                atomicOr(a.status, kWsStatusTimeout);
+                pstop = true;
+                break;
+            }
+            unsigned char *slot = ring + size_t(st) * kSlotBytes;
+            const int k0 = (pug.ks0 + pj) * kKS;
+            mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
+            tma_load_3d(slot, &tmQ, 0, pug.n0, k0 / 128, &full_r[st], pol_q);
+            tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
+            ++pj;
+            ++pJ;
+        }
+    };
+    if (warp == kTmaWarp && lane == 0) {
+        // The producer sets up the barriers and issues the first ring's worth of stages before
+        // the CTA-wide set-up (TMEM allocation, the CTA barrier), so their DRAM latency overlaps it.
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_r[s], 1);
             mbar_init(&done[s], 1);
@@ -199,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kMmaIssuers; ++i) mbar_init(&mma_done[i], 1);
         mbar_init(never, 1);
         fence_mbar_init();
+        pdl_wait();  // no global-memory access before this point
+        pol_q = l2_policy_evict_first();
+        pol_x = l2_policy_evict_last();
+        produce(kStages);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -209,31 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // no global-memory access before this point
 
     if (warp == kTmaWarp) {
-        // ---- TMA producer: int8 tile + two X atoms per stage ----
+        // ---- TMA producer: the remaining stages ----
         if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
-            int J = 0;
-            bool stop = false;
-            for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
-                const Unit ug = unit_geometry(a, u);
-                for (int j = 0; j < ug.nst; ++j, ++J) {
-                    const int st = J % kStages;
-                    // slot st was last used by stage J - kStages
-                    if (!mbar_wait(&done[st], static_cast<uint32_t>(((J / kStages) & 1) ^ 1), a.timeout_ns)) {
-                        atomicOr(a.status, kWsStatusTimeout);
-                        stop = true;
-                        break;
-                    }
-                    unsigned char *slot = ring + size_t(st) * kSlotBytes;
-                    const int k0 = (ug.ks0 + j) * kKS;
-                    mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
-                    tma_load_3d(slot, &tmQ, 0, ug.n0, k0 / 128, &full_r[st], pol_q);
-                    tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
-                }
-            }
+            produce(0x7fffffff);
             // copies still in flight (possible only after a consumer gave up) land before exit
-            for (int i = J > kStages ? J - kStages : 0; i < J; ++i)
+            for (int i = pJ > kStages ? pJ - kStages : 0; i < pJ; ++i)
                 mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.timeout_ns);
         }
     } else if (warp >= kMmaWarp) {
