@@ -216,6 +216,8 @@ def load_bench_library():
                                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     lib.dspark_bench_empty.restype = ctypes.c_int
     lib.dspark_bench_empty.argtypes = [ctypes.c_void_p]
+    lib.dspark_bench_empty_smem.restype = ctypes.c_int
+    lib.dspark_bench_empty_smem.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -264,24 +266,29 @@ def measure_ceilings(dev, reps: int = 10):
     del big
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sinkf = torch.empty((), dtype=torch.int32, device=dev)
-    ts = []
-    for r in range(53):
-        flush.fill_(r & 0xFF)
-        torch.amax(flush.view(torch.int32), dim=0, out=sinkf)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        assert lib.dspark_bench_empty(s) == 0
-        b.record(stream)
-        b.synchronize()
-        if r >= 3:
-            ts.append(a.elapsed_time(b) * 1000.0)
-    out["event_floor_us"] = {"median": statistics.median(ts), "mean": statistics.mean(ts),
-                             "min": min(ts), "max": max(ts)}
+    def floor(launch):
+        ts = []
+        for r in range(53):
+            flush.fill_(r & 0xFF)
+            torch.amax(flush.view(torch.int32), dim=0, out=sinkf)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            assert launch() == 0
+            b.record(stream)
+            b.synchronize()
+            if r >= 3:
+                ts.append(a.elapsed_time(b) * 1000.0)
+        return {"median": statistics.median(ts), "mean": statistics.mean(ts), "min": min(ts), "max": max(ts)}
+
+    out["event_floor_us"] = floor(lambda: lib.dspark_bench_empty(s))
+    # the same with one CTA per SM holding 200 KB of shared memory, like the draft-step kernels
+    out["event_floor_200KB_smem_us"] = floor(lambda: lib.dspark_bench_empty_smem(sms, 200 * 1024, s))
     out["method"] = ("libdspark_bench read kernel (16-byte ld.global.cg, grid = 4 x SMs x 512 "
                      "threads): 64 MiB read 20 times per launch after a warming pass (L2) and "
                      "2 GiB read once (DRAM), best of 10; empty launch between two events "
-                     "after an L2 flush, 50 samples")
+                     "after an L2 flush (1 CTA; and one CTA per SM with 200 KB of shared memory), "
+                     "50 samples")
     return out
 
 
@@ -813,6 +820,48 @@ def markov_roofline(B, mb, t_s, peak, peak_kind, ceil):
     return r
 
 
+def run_one_kernel(name: str) -> int:
+    """Runs one kernel of the workload twice on cuda:0 and exits, for a profiler capture of a
+    single launch (`ncu -k ... -s 1 -c 1`): `ws_4096x4096` (the fp16 weight-stationary matvec,
+    M = 7), `probe_2048` (the batched confidence probe), `q8_lm_head` (the Q8_0 matvec,
+    4096 -> 151936, M = 7).  No timing is taken."""
+    import torch
+
+    from dspark_draft_sampling_gb300 import api
+
+    api.load_library()
+    dev = torch.device("cuda", 0)
+    if name == "ws_4096x4096":
+        w = synth.ws_inputs(7, 4096, 4096, seed=4096 + 4096)
+        W = torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16)
+        X = torch.from_numpy(w["X"].view(np.int16)).to(dev).view(torch.float16)
+        Y = torch.empty((7, 4096), dtype=torch.float16, device=dev)
+        wsp = api.new_ws_workspace(7, 4096, 4096, dev)
+        call = lambda: api.ws_matvec(W, X, out=Y, workspace=wsp)
+    elif name == "probe_2048":
+        pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=0)
+        wq = torch.from_numpy(pr["wq"]).to(dev)
+        hid = torch.from_numpy(pr["hidden"]).to(dev)
+        call = lambda: api.conf_probe(wq, hid, pr["bias"], pr["threshold"])
+    elif name == "q8_lm_head":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        N, K = 151936, 4096
+        q = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
+        d = (torch.rand((N, K // 32), generator=gen, device=dev) * 4e-4).half().view(torch.int16)
+        X = torch.randn((7, K), generator=gen, device=dev).half()
+        Y = torch.empty((7, N), dtype=torch.float16, device=dev)
+        wsq = api.new_ws_q8_workspace(7, N, K, dev)
+        call = lambda: api.ws_matvec_q8(q, d, X, out=Y, workspace=wsq)
+    else:
+        raise SystemExit(f"unknown --kernel {name}")
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    print(f"{name}: ok")
+    return 0
+
+
 # ---------------------------------------------------------------- main -------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -832,7 +881,11 @@ def main():
                     help="skip the separately timed rows beyond the headline step")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration sweep (median/p10/p90, cold and warm L2)")
+    ap.add_argument("--kernel", choices=["ws_4096x4096", "probe_2048", "q8_lm_head"],
+                    help="run only this kernel of the workload twice, untimed (for a profiler)")
     args = ap.parse_args()
+    if args.kernel:
+        return run_one_kernel(args.kernel)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 

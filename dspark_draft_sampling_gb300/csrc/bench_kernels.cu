@@ -42,6 +42,12 @@ __global__ void __launch_bounds__(1024) read_kernel(const uint4 *__restrict__ p,
 
 __global__ void empty_kernel() {}
 
+// what matters is the launch shape (the dynamic shared memory each CTA requests)
+__global__ void empty_smem_kernel() {
+    extern __shared__ unsigned char smem[];
+    smem[threadIdx.x] = static_cast<unsigned char>(threadIdx.x);
+}
+
 }  // namespace
 
 extern "C" int dspark_bench_read(const void *buf, size_t bytes, int passes, unsigned long long *sink, int grid,
@@ -56,5 +62,13 @@ extern "C" int dspark_bench_read(const void *buf, size_t bytes, int passes, unsi
 
 extern "C" int dspark_bench_empty(void *stream) {
     empty_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    return static_cast<int>(cudaGetLastError());
+}
+
+extern "C" int dspark_bench_empty_smem(int ctas, int smem_bytes, void *stream) {
+    if (ctas < 1 || smem_bytes < 16 || smem_bytes > 227 * 1024) return static_cast<int>(cudaErrorInvalidValue);
+    cudaError_t e = cudaFuncSetAttribute(empty_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    empty_smem_kernel<<<ctas, 32, static_cast<size_t>(smem_bytes), static_cast<cudaStream_t>(stream)>>>();
     return static_cast<int>(cudaGetLastError());
 }

@@ -32,6 +32,11 @@ int dspark_bench_read(const void *buf, size_t bytes, int passes, unsigned long l
  * that event timing puts under any single launch. */
 int dspark_bench_empty(void *stream);
 
+/* The same empty kernel on `ctas` CTAs that each request `smem_bytes` of dynamic shared
+ * memory (up to 227 KB): the floor for a launch shaped like the draft-step kernels, which use
+ * 90-220 KB per CTA.  ctas >= 1. */
+int dspark_bench_empty_smem(int ctas, int smem_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -295,7 +295,7 @@ def test_bench_library_exports_its_header():
     hdr = os.path.join(os.path.dirname(HEADER), "dspark_bench.h")
     text = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
     names = sorted(set(re.findall(r"\b(dspark_bench_[a-z0-9_]+)\s*\(", text)))
-    assert names == ["dspark_bench_empty", "dspark_bench_read"]
+    assert names == ["dspark_bench_empty", "dspark_bench_empty_smem", "dspark_bench_read"]
     out = subprocess.run(["nm", "-D", "--defined-only", build.bench_lib_file()], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (dspark_\w+)", out))
