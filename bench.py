@@ -652,7 +652,15 @@ def run_configs(dev, mk27, reps: int = 30):
         plan = api.MarkovPlan(base, w1, w2, d2t, prev)
         out[key] = entry(lambda: plan.launch(stream), markov_bytes(B, k, V, R, d2t is not None))
         out[key]["us_per_position_cold"] = out[key]["us_cold"]["median"] / k
+        out[key]["kernel"] = api.markov_kernel_for(B, k, V, R)
         plan.close()
+        if out[key]["kernel"] == "cluster":
+            # the same lane on the grid kernel, for comparison (direct calls)
+            wsg = api.new_markov_workspace(B, k, V, R, dev)
+            ids = torch.empty((B, k), dtype=torch.int64, device=dev)
+            out[key]["grid_kernel"] = entry(
+                lambda: api.markov_draft(base, w1, w2, d2t, prev, out_ids=ids, workspace=wsg, stream=stream,
+                                         kernel="grid"), markov_bytes(B, k, V, R, d2t is not None))
         del plan, base
     pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=0)
     wq = torch.from_numpy(pr["wq"]).to(dev)
@@ -799,6 +807,11 @@ def markov_roofline(B, mb, t_s, peak, peak_kind, ceil):
                             "used only while the kernel sources hash to the value recorded there"),
          "l2_to_sm_bytes_per_launch": l2b, "l2_to_sm_source": l2_src}
     l2_peak = ceil.get("l2_read_gbs") if ceil else None
+    if r["frac"] > 1.0:
+        r["frac_note"] = ("frac counts markov_w2 once per position (the pages' accounting); after the "
+                          "first position about half of it is served from L2, so frac exceeds 1. "
+                          "frac_dram and frac_l2 divide the kernel's measured DRAM and L2-to-SM bytes by "
+                          "the HBM copy peak and the L2 read bandwidth measured in this run")
     fr = {}
     if traffic:
         fr["dram"] = traffic / t_s / 1e9 / peak

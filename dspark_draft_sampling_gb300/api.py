@@ -26,6 +26,9 @@ SIGNATURES = {
     "dspark_version": (ctypes.c_char_p, []),
     "dspark_markov_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "dspark_markov_draft": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "dspark_markov_draft_kernel": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _I,
+                                        _P]),
+    "dspark_markov_kernel_for": (_I, [_I, _I, _I, _I]),
     "dspark_markov_status": (_I, [_P, _P]),
     "dspark_markov_draft_debug": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _U, _U, _P]),
     "dspark_markov_draft_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -142,11 +145,26 @@ def new_markov_workspace(num_reqs: int, k: int, vocab: int, rank: int, device=No
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def markov_draft(base, w1, w2, d2t, prev, *, out_ids=None, workspace=None, dbg_logits=None,
-                 dbg_bias=None, stream=None):
-    """k-step Markov block draft.  base [B,k,V] fp32, w1/w2 [V,R] bf16, d2t [V] int32 or
-    None, prev [B] int64 (updated in place).  Returns out_ids [B,k] int64 (target ids)."""
+MARKOV_KERNELS = {"auto": 0, "grid": 1, "cluster": 2}
+
+
+def markov_kernel_for(num_reqs, k, vocab, rank) -> str:
+    """Which kernel ``markov_draft(kernel="auto")`` runs for these sizes on the current device
+    (with a 16-byte aligned base): ``"grid"`` or ``"cluster"``."""
     lib = load_library()
+    code = int(lib.dspark_markov_kernel_for(int(num_reqs), int(k), int(vocab), int(rank)))
+    return {v: n for n, v in MARKOV_KERNELS.items()}[code]
+
+
+def markov_draft(base, w1, w2, d2t, prev, *, out_ids=None, workspace=None, dbg_logits=None,
+                 dbg_bias=None, stream=None, kernel="auto"):
+    """k-step Markov block draft.  base [B,k,V] fp32, w1/w2 [V,R] bf16, d2t [V] int32 or
+    None, prev [B] int64 (updated in place).  Returns out_ids [B,k] int64 (target ids).
+    ``kernel``: "auto" (dspark_markov_draft), or "grid" / "cluster" to name the kernel
+    (dspark_markov_draft_kernel)."""
+    lib = load_library()
+    if kernel not in MARKOV_KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(MARKOV_KERNELS)}")
     if base.dim() != 3:
         raise ValueError("base must be [num_reqs, k, vocab]")
     B, k, V = base.shape
@@ -155,7 +173,7 @@ def markov_draft(base, w1, w2, d2t, prev, *, out_ids=None, workspace=None, dbg_l
         out_ids = torch.empty((B, k), dtype=torch.int64, device=base.device)
     if workspace is None:
         workspace = new_markov_workspace(B, k, V, R, base.device)
-    st = lib.dspark_markov_draft(
+    args = [
         _ptr(base, "base", dtypes=(torch.float32,)),
         _ptr(w1, "markov_w1", itemsize=2, dtypes=_BITS16),
         _ptr(w2, "markov_w2", itemsize=2, dtypes=_BITS16),
@@ -165,8 +183,11 @@ def markov_draft(base, w1, w2, d2t, prev, *, out_ids=None, workspace=None, dbg_l
         _ptr(out_ids, "out_ids", dtypes=(torch.int64,)),
         _ptr(dbg_logits, "dbg_logits", dtypes=(torch.float32,), allow_none=True),
         _ptr(dbg_bias, "dbg_bias", dtypes=(torch.float32,), allow_none=True),
-        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _stream(stream))
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()]
+    if kernel == "auto":
+        st = lib.dspark_markov_draft(*args, _stream(stream))
+    else:
+        st = lib.dspark_markov_draft_kernel(*args, MARKOV_KERNELS[kernel], _stream(stream))
     _check(lib, st)
     return out_ids
 

@@ -18,7 +18,7 @@ SRC_DIR = os.path.join(PKG_DIR, "csrc")
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libdspark.so"
-SOURCES = ["common.cu", "markov.cu", "markov_tc.cu", "probe.cu", "ws_matvec.cu", "draft_plan.cu", "gated_plan.cu", "ws_q8.cu", "host_api.cu"]
+SOURCES = ["common.cu", "markov.cu", "markov_tc.cu", "markov_cluster.cu", "probe.cu", "ws_matvec.cu", "draft_plan.cu", "gated_plan.cu", "ws_q8.cu", "host_api.cu"]
 BENCH_LIB_NAME = "libdspark_bench.so"
 BENCH_SOURCES = ["bench_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

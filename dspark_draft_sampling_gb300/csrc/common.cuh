@@ -171,4 +171,13 @@ __device__ __forceinline__ uint32_t argmax_key_index(unsigned long long key) {
     return 0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull);
 }
 
+// Warp-wide max of 64-bit keys with two 32-bit redux.sync reductions: the max high word,
+// then the max low word among the lanes holding it.  All 32 lanes must take part.
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+    const unsigned hi = static_cast<unsigned>(v >> 32);
+    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? static_cast<unsigned>(v) : 0u);
+    return (static_cast<unsigned long long>(mh) << 32) | ml;
+}
+
 }  // namespace dspark

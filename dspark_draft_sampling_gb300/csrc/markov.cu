@@ -23,8 +23,10 @@ size_t workspace_bytes(int k) {
 dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16_t *w2, const int32_t *d2t,
                              int64_t *prev, int B, int k, int V, int R, int64_t *out_ids, float *dbg_logits,
                              float *dbg_bias, void *workspace, size_t ws_bytes, unsigned bar_extra,
-                             unsigned long long timeout_ns, cudaStream_t stream, bool clear_out_ids) {
+                             unsigned long long timeout_ns, cudaStream_t stream, bool clear_out_ids, int kernel) {
     clear_error();
+    if (kernel != kMarkovAuto && kernel != kMarkovGrid && kernel != kMarkovCluster)
+        return fail(DSPARK_ERR_INVALID, "markov: kernel %d", kernel);
     if (B < 0 || k < 0 || V < 1 || R < 1) return fail(DSPARK_ERR_INVALID, "markov: bad sizes B=%d k=%d V=%d R=%d", B, k, V, R);
     if (R != 64 && R != 128 && R != 256)
         return fail(DSPARK_ERR_UNSUPPORTED, "markov: rank %d not in {64, 128, 256}", R);
@@ -44,14 +46,26 @@ dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
 
+    int C = 0;  // cluster size of the single-cluster form, 0 for the grid form
+    if (kernel == kMarkovCluster || (kernel == kMarkovAuto && markov_auto_kernel(base, B, V, R, k) == kMarkovCluster)) {
+        if (aligned(base, 16)) C = markov_cluster_size(B, V, R, k);
+        if (kernel == kMarkovCluster && C == 0)
+            return fail(DSPARK_ERR_UNSUPPORTED,
+                        "markov: the single-cluster kernel does not apply (vocab %d, rank %d, k %d; vocab a "
+                        "multiple of 4, base 16-byte aligned, markov_w1 + markov_w2 in one cluster)",
+                        V, R, k);
+    }
+
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaError_t e;
     if (clear_out_ids) {  // every id -1 until the kernel writes it
         e = cudaMemsetAsync(out_ids, 0xFF, size_t(B) * size_t(k) * sizeof(int64_t), stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(out_ids)");
     }
-    e = cudaMemsetAsync(ws, 0, workspace_bytes(k), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(markov workspace)");
+    if (C == 0) {  // the grid form's barrier counter and keys start from zero
+        e = cudaMemsetAsync(ws, 0, workspace_bytes(k), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(markov workspace)");
+    }
     MarkovArgs args;
     args.base = base;
     args.w1 = w1;
@@ -69,7 +83,17 @@ dspark_status markov_enqueue(const float *base, const uint16_t *w1, const uint16
     args.V = V;
     args.bar_extra = bar_extra;
     args.timeout_ns = timeout_ns;
+    if (C > 0) return launch_markov_cluster(args, R, C, stream);
     return launch_markov_tc(args, R, markov_grid(V, sms), stream);
+}
+
+int markov_auto_kernel(const float *base, int B, int V, int R, int k) {
+    // The single-cluster exchange sends every request's key and candidate row to every CTA
+    // of the cluster; beyond two requests that volume costs more per position than the grid
+    // form's global round trips save (measured on GB300).  Both kernels give the same bits.
+    return (B <= kMarkovClusterAutoMaxReqs && aligned(base, 16) && markov_cluster_size(B, V, R, k) > 0)
+               ? kMarkovCluster
+               : kMarkovGrid;
 }
 
 }  // namespace dspark
@@ -96,6 +120,22 @@ extern "C" dspark_status dspark_markov_draft(const float *base_logits, const uin
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" dspark_status dspark_markov_draft_kernel(const float *base_logits, const uint16_t *markov_w1,
+                                                    const uint16_t *markov_w2, const int32_t *d2t, int64_t *prev,
+                                                    int num_reqs, int k, int vocab, int rank, int64_t *out_ids,
+                                                    float *dbg_logits, float *dbg_bias, void *workspace,
+                                                    size_t workspace_bytes, int kernel, dspark_stream_t stream) {
+    return dspark::markov_enqueue(base_logits, markov_w1, markov_w2, d2t, prev, num_reqs, k, vocab, rank, out_ids,
+                                  dbg_logits, dbg_bias, workspace, workspace_bytes, 0u, dspark::kDefaultTimeoutNs,
+                                  reinterpret_cast<cudaStream_t>(stream), false, kernel);
+}
+
+extern "C" int dspark_markov_kernel_for(int num_reqs, int k, int vocab, int rank) {
+    if (k < 1 || vocab < 1) return dspark::kMarkovGrid;
+    // an aligned stand-in for the base pointer: the choice is made for a 16-byte aligned base
+    return dspark::markov_auto_kernel(reinterpret_cast<const float *>(uintptr_t(256)), num_reqs, vocab, rank, k);
+}
+
 extern "C" dspark_status dspark_markov_draft_debug(const float *base_logits, const uint16_t *markov_w1,
                                                    const uint16_t *markov_w2, const int32_t *d2t, int64_t *prev,
                                                    int num_reqs, int k, int vocab, int rank, int64_t *out_ids,
@@ -107,7 +147,7 @@ extern "C" dspark_status dspark_markov_draft_debug(const float *base_logits, con
     return dspark::markov_enqueue(base_logits, markov_w1, markov_w2, d2t, prev, num_reqs, k, vocab, rank, out_ids,
                                   nullptr, nullptr, workspace, workspace_bytes, missing_arrivals,
                                   static_cast<unsigned long long>(timeout_us) * 1000ull,
-                                  reinterpret_cast<cudaStream_t>(stream));
+                                  reinterpret_cast<cudaStream_t>(stream), false, dspark::kMarkovGrid);
 }
 
 // ---- allocation-free variant ----------------------------------------------------------

@@ -64,15 +64,6 @@ constexpr int base_area_bytes() {
     return (NB * kTileRows * 4 + 1023) / 1024 * 1024;
 }
 
-// Warp-wide max of 64-bit keys with two 32-bit redux.sync reductions: the max high word,
-// then the max low word among the lanes holding it.
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-    const unsigned hi = static_cast<unsigned>(v >> 32);
-    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
-    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? static_cast<unsigned>(v) : 0u);
-    return (static_cast<unsigned long long>(mh) << 32) | ml;
-}
-
 template <int NB, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmBase,

@@ -82,8 +82,17 @@ const char *dspark_version(void);
  *   k >= 0 (k == 0 or num_reqs == 0 enqueues nothing).
  * Device-side errors: a prev entry outside [0, vocab) or a negative d2t entry makes
  *   the affected ids -1 and sets DSPARK_ERR_INDEX in the status word.
- * The k positions run in one cooperative kernel launch (one CTA per SM) preceded by
- *   a memset of the workspace header; both can be captured in a CUDA graph.
+ * Two kernels compute this, with the same tensor-core instructions for every bias value,
+ *   so they give bit-identical logits and ids; the call picks one from the sizes:
+ *   - single-cluster: for num_reqs <= 2 when markov_w1 and markov_w2 (and the exchange
+ *     buffers) fit in the shared memory of one thread-block cluster of up to 16 CTAs (about
+ *     vocab <= 12 K at rank 64, <= 6 K at rank 128, <= 2 K at rank 256), vocab is a multiple
+ *     of 4 and base_logits is 16-byte aligned: one cluster launch that keeps both matrices on
+ *     chip and passes each position's argmax and the winner's markov_w1 row through
+ *     distributed shared memory.  The kernel resets the status word itself.
+ *   - grid: otherwise, one cooperative kernel launch (at most one CTA per SM) preceded by
+ *     a memset of the workspace header.
+ *   Either can be captured in a CUDA graph.
  * ===================================================================================== */
 size_t dspark_markov_workspace_bytes(int num_reqs, int k, int vocab, int rank);
 
@@ -93,13 +102,34 @@ dspark_status dspark_markov_draft(const float *base_logits, const uint16_t *mark
                                   float *dbg_logits, float *dbg_bias, void *workspace,
                                   size_t workspace_bytes, dspark_stream_t stream);
 
+/* The same draft with the kernel named explicitly: DSPARK_MARKOV_KERNEL_AUTO (what
+ * dspark_markov_draft does), DSPARK_MARKOV_KERNEL_GRID or DSPARK_MARKOV_KERNEL_CLUSTER (any
+ * num_reqs, where its shared memory fits).  Asking for the single-cluster kernel where it
+ * does not fit returns DSPARK_ERR_UNSUPPORTED and enqueues nothing; any other value is
+ * DSPARK_ERR_INVALID. */
+#define DSPARK_MARKOV_KERNEL_AUTO 0
+#define DSPARK_MARKOV_KERNEL_GRID 1
+#define DSPARK_MARKOV_KERNEL_CLUSTER 2
+dspark_status dspark_markov_draft_kernel(const float *base_logits, const uint16_t *markov_w1,
+                                         const uint16_t *markov_w2, const int32_t *d2t,
+                                         int64_t *prev, int num_reqs, int k, int vocab, int rank,
+                                         int64_t *out_ids, float *dbg_logits, float *dbg_bias,
+                                         void *workspace, size_t workspace_bytes, int kernel,
+                                         dspark_stream_t stream);
+
+/* The kernel dspark_markov_draft uses on the current device for these sizes and a 16-byte
+ * aligned base_logits: DSPARK_MARKOV_KERNEL_GRID or DSPARK_MARKOV_KERNEL_CLUSTER.  Host
+ * only; may query the device's cluster occupancy once. */
+int dspark_markov_kernel_for(int num_reqs, int k, int vocab, int rank);
+
 /* Synchronizes `stream`, then reads the status word that the last dspark_markov_draft
  * on `workspace` left: DSPARK_OK, DSPARK_ERR_INDEX or DSPARK_ERR_TIMEOUT. */
 dspark_status dspark_markov_status(const void *workspace, dspark_stream_t stream);
 
 /* Fault-injection hook for testing the device-side wait limit: the same launch as
- * dspark_markov_draft, except that the grid-wide step barrier expects
- * `missing_arrivals` more arrivals than there are CTAs (so with missing_arrivals > 0
+ * dspark_markov_draft with the grid kernel (whatever the sizes), except that its grid-wide
+ * step barrier expects `missing_arrivals` more arrivals than there are CTAs (so with
+ * missing_arrivals > 0
  * it can never complete) and every device-side wait gives up after `timeout_us`
  * microseconds.  The kernel then records DSPARK_ERR_TIMEOUT, drains its in-flight
  * copies and returns; nothing hangs.  Not for production use. */

@@ -49,7 +49,7 @@ def markov_to_device(inp, device="cuda"):
     return d
 
 
-def gpu_markov(inp, *, dbg=True, dbg_bias=True, device="cuda"):
+def gpu_markov(inp, *, dbg=True, dbg_bias=True, device="cuda", kernel="auto"):
     t = markov_to_device(inp, device)
     B, k, V = t["base"].shape
     R = t["w2"].shape[1]
@@ -57,7 +57,7 @@ def gpu_markov(inp, *, dbg=True, dbg_bias=True, device="cuda"):
     db = torch.full_like(t["base"], float("nan")) if (dbg and dbg_bias) else None
     ws = api.new_markov_workspace(B, k, V, R, device)
     out = api.markov_draft(t["base"], t["w1"], t["w2"], t["d2t"], t["prev"], dbg_logits=dl,
-                           dbg_bias=db, workspace=ws)
+                           dbg_bias=db, workspace=ws, kernel=kernel)
     status = api.markov_status(ws)
     return dict(out_ids=out.cpu().numpy(), prev=t["prev"].cpu().numpy(),
                 logits=None if dl is None else dl.cpu().numpy(),

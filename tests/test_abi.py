@@ -84,6 +84,29 @@ def test_markov_validation(dspark_lib):
     assert lib.dspark_last_error().decode() == ""
 
 
+def test_markov_kernel_choice(dspark_lib):
+    lib = dspark_lib
+    k_ = lib.dspark_markov_draft_kernel
+    # an unknown kernel is refused before anything else is looked at
+    assert k_(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 64, FAKE, NULL, NULL, FAKE, 1 << 20, 7,
+              NULL) == INVALID
+    assert k_(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 64, FAKE, NULL, NULL, FAKE, 1 << 20, -1,
+              NULL) == INVALID
+    assert k_(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 4096, 100, FAKE, NULL, NULL, FAKE, 1 << 20, 2,
+              NULL) == UNSUPPORTED
+    grid, cluster = 1, 2
+    kf = lib.dspark_markov_kernel_for
+    # small vocabularies with one or two requests go to the single-cluster kernel
+    assert {kf(B, 4, 4096, 64) for B in (1, 2)} == {cluster}
+    assert kf(8, 4, 4096, 64) == grid
+    assert kf(1, 3, 1024, 256) == cluster
+    # the 27B and reduced-vocab lanes, and a vocabulary that is not a multiple of 4, do not
+    assert kf(8, 15, 248320, 256) == grid
+    assert kf(1, 9, 32000, 256) == grid
+    assert kf(1, 4, 4098, 64) == grid
+    assert kf(1, 4, 4096, 100) == grid
+
+
 def test_markov_debug_and_plan_validation(dspark_lib):
     lib = dspark_lib
     assert lib.dspark_markov_draft_debug(FAKE, FAKE, FAKE, NULL, FAKE, 1, 4, 64, 64, FAKE, FAKE,

@@ -76,6 +76,102 @@ def test_ragged_shapes(B, k, V, R, d2t):
     assert rep["n_exempt"] == 0
 
 
+# The single-cluster kernel (vocabularies whose markov_w1 + markov_w2 fit in one cluster's
+# shared memory), named explicitly so that each case runs it whatever the auto choice.
+@pytest.mark.parametrize("B,k,V,R,d2t", [
+    (1, 4, 4096, 64, "identity"),     # the tiny lane's shape
+    (3, 5, 1000, 64, "injective"),    # 8 tiles, the last one ragged
+    (8, 3, 8192, 64, "identity"),     # 64 tiles, 8 requests
+    (2, 6, 2048, 128, "injective"),
+    (2, 2, 2048, 256, "identity"),    # rank 256
+    (2, 1, 100, 256, "identity"),     # a single CTA
+    (7, 9, 508, 64, "identity"),      # 4 tiles, ragged
+    (4, 20, 3000, 64, "injective"),   # more positions than base buffers
+])
+def test_cluster_kernel(B, k, V, R, d2t):
+    inp = synth.markov_inputs(B, k, V, R, base_sd=1.0, w_sd=0.3, d2t=d2t, seed=B * 31 + k)
+    rep = parity.check_markov(inp, parity.gpu_markov(inp, kernel="cluster"))
+    assert rep["n_exempt"] == 0
+
+
+def test_cluster_kernel_production_form_and_ties():
+    """Without debug outputs, with planted exact ties decided by the lowest index."""
+    inp = synth.markov_inputs(3, 8, 6000, 64, base_sd=1.0, w_sd=0.3, tie_frac=0.005,
+                              d2t="injective", seed=41)
+    g = parity.gpu_markov(inp, dbg=False, kernel="cluster")
+    rep = parity.check_markov(inp, g, values=False)
+    assert rep["n_exempt"] == 0
+    gd = parity.draft_from_target(inp, g["out_ids"])
+    for i in inp["spiked_steps"]:
+        v1, _ = inp["ties"][(i // 2) % len(inp["ties"])]
+        assert np.all(gd[:, i] == v1)
+
+
+def test_tiny_lane_on_both_kernels():
+    inp = synth.markov_config("tiny")
+    assert api.markov_kernel_for(1, 4, 4096, 64) == "cluster"
+    for kernel in ("grid", "cluster"):
+        rep = parity.check_markov(inp, parity.gpu_markov(inp, kernel=kernel))
+        assert rep["n_exempt"] == 0
+
+
+@pytest.mark.parametrize("B,k,V,R", [(1, 4, 4096, 64), (6, 5, 3000, 128), (8, 7, 8192, 64),
+                                     (2, 3, 2040, 256)])
+def test_cluster_and_grid_kernels_bit_identical(B, k, V, R):
+    """Both kernels issue the same tensor-core instructions for every bias value, so logits,
+    biases and ids agree bit for bit (the automatic choice, which depends on the shared
+    memory the exchange needs for num_reqs, cannot change a result)."""
+    inp = synth.markov_inputs(B, k, V, R, base_sd=1.0, w_sd=0.3, seed=B + k + R)
+    g = parity.gpu_markov(inp, kernel="grid")
+    c = parity.gpu_markov(inp, kernel="cluster")
+    np.testing.assert_array_equal(g["out_ids"], c["out_ids"])
+    np.testing.assert_array_equal(g["prev"], c["prev"])
+    np.testing.assert_array_equal(g["logits"].view(np.uint32), c["logits"].view(np.uint32))
+    np.testing.assert_array_equal(g["bias"].view(np.uint32), c["bias"].view(np.uint32))
+
+
+def test_cluster_kernel_choice_and_refusal():
+    assert api.markov_kernel_for(1, 9, 32000, 256) == "grid"
+    assert api.markov_kernel_for(8, 15, 248320, 256) == "grid"
+    assert api.markov_kernel_for(1, 4, 4098, 64) == "grid"  # vocab not a multiple of 4
+    inp = synth.markov_inputs(1, 2, 20000, 256, seed=42)
+    t = parity.markov_to_device(inp)
+    with pytest.raises(api.DsparkError) as e:
+        api.markov_draft(t["base"], t["w1"], t["w2"], None, t["prev"], kernel="cluster")
+    assert e.value.status == api.DSPARK_ERR_UNSUPPORTED
+
+
+def test_cluster_kernel_batch_invariance_bitwise():
+    inp = synth.markov_inputs(5, 3, 4000, 128, w_sd=0.3, seed=43)
+    full = parity.gpu_markov(inp, kernel="cluster")
+    for r in range(5):
+        one = dict(inp)
+        one["base"] = inp["base"][r:r + 1]
+        one["prev0"] = inp["prev0"][r:r + 1]
+        g = parity.gpu_markov(one, kernel="cluster")
+        np.testing.assert_array_equal(g["out_ids"][0], full["out_ids"][r])
+        np.testing.assert_array_equal(g["logits"][0].view(np.uint32),
+                                      full["logits"][r].view(np.uint32))
+
+
+def test_cluster_kernel_resets_the_status_word():
+    """A grid-kernel draft that timed out leaves DSPARK_ERR_TIMEOUT in the workspace; the
+    next draft on the same workspace through the cluster kernel reports its own status."""
+    inp = synth.markov_inputs(1, 3, 4096, 64, seed=44)
+    t = parity.markov_to_device(inp)
+    ws = api.new_markov_workspace(1, 3, 4096, 64)
+    out = torch.empty((1, 3), dtype=torch.int64, device="cuda")
+    api.markov_draft_debug(t["base"], t["w1"], t["w2"], None, t["prev"], out, ws,
+                           missing_arrivals=1, timeout_us=20000)
+    assert api.markov_status(ws) == api.DSPARK_ERR_TIMEOUT
+    t["prev"].copy_(torch.from_numpy(inp["prev0"]))
+    g = api.markov_draft(t["base"], t["w1"], t["w2"], None, t["prev"], workspace=ws,
+                         kernel="cluster")
+    assert api.markov_status(ws) == 0
+    o = parity.oracle.markov_draft(inp["base"], inp["w1"], inp["w2"], None, inp["prev0"])
+    np.testing.assert_array_equal(g.cpu().numpy(), o["out_ids"])
+
+
 def test_strong_bias_chain():
     """Large markov weights make the bias dominate the base row, so every position's id
     really depends on the previous one (the chain is exercised, not just argmax(base))."""
