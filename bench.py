@@ -649,18 +649,24 @@ def run_configs(dev, mk27, reps: int = 30):
             prev = torch.from_numpy(mk["prev0"].copy()).to(dev)
             B, k, V, R = mk["num_reqs"], mk["k"], mk["vocab"], mk["rank"]
             key = f"markov_{name}"
-        plan = api.MarkovPlan(base, w1, w2, d2t, prev)
-        out[key] = entry(lambda: plan.launch(stream), markov_bytes(B, k, V, R, d2t is not None))
+        # one dspark_markov_draft call (what a caller of the C ABI pays on the device); the
+        # same call recorded in a CUDA graph (MarkovPlan) is reported beside it
+        nbytes = markov_bytes(B, k, V, R, d2t is not None)
+        wsd = api.new_markov_workspace(B, k, V, R, dev)
+        ids = torch.empty((B, k), dtype=torch.int64, device=dev)
+        out[key] = entry(lambda: api.markov_draft(base, w1, w2, d2t, prev, out_ids=ids, workspace=wsd,
+                                                  stream=stream), nbytes)
         out[key]["us_per_position_cold"] = out[key]["us_cold"]["median"] / k
         out[key]["kernel"] = api.markov_kernel_for(B, k, V, R)
+        plan = api.MarkovPlan(base, w1, w2, d2t, prev)
+        pl = entry(lambda: plan.launch(stream), nbytes)
+        out[key]["graph_plan"] = {"us_cold": pl["us_cold"], "us_warm": pl["us_warm"]}
         plan.close()
         if out[key]["kernel"] == "cluster":
             # the same lane on the grid kernel, for comparison (direct calls)
-            wsg = api.new_markov_workspace(B, k, V, R, dev)
-            ids = torch.empty((B, k), dtype=torch.int64, device=dev)
             out[key]["grid_kernel"] = entry(
-                lambda: api.markov_draft(base, w1, w2, d2t, prev, out_ids=ids, workspace=wsg, stream=stream,
-                                         kernel="grid"), markov_bytes(B, k, V, R, d2t is not None))
+                lambda: api.markov_draft(base, w1, w2, d2t, prev, out_ids=ids, workspace=wsd, stream=stream,
+                                         kernel="grid"), nbytes)
         del plan, base
     pr = synth.probe_inputs(N_PROBES, synth.PROBE_K, seed=0)
     wq = torch.from_numpy(pr["wq"]).to(dev)
