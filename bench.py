@@ -519,7 +519,7 @@ def run_next_rows(dev, reps: int = 20):
     # Q8_0 projections, M = 7: each shape alone, and the four back to back in one timed region
     # (a layer's projections: programmatic dependent launch overlaps each launch's prologue
     # with the previous one's tail)
-    q8_us, q8_bytes, q8_calls = 0.0, 0, []
+    q8_us, q8_bytes, q8_calls, q8_probs = 0.0, 0, [], []
     for (K, N) in synth.WS_SHAPES:
         q, d = q8_weights(N, K)
         X = f16((7, K), 1.0)
@@ -533,12 +533,18 @@ def run_next_rows(dev, reps: int = 20):
         q8_us += us
         q8_bytes += nb
         q8_calls.append(call)
+        q8_probs.append((q, d, X, Y))
     out["ws_q8_qwen3_8b_4_shapes_us"] = q8_us
     out["ws_q8_qwen3_8b_GBps"] = q8_bytes / (q8_us * 1e-6) / 1e9
     seq = timed(lambda: [c() for c in q8_calls])
     out["ws_q8_qwen3_8b_4_shapes_back_to_back_us"] = seq
     out["ws_q8_qwen3_8b_back_to_back_frac_of_hbm"] = q8_bytes / (seq * 1e-6) / 1e9 / peak
-    del q8_calls
+    # the four as one grouped launch (dspark_ws_matvec_q8_grouped)
+    wsg = torch.zeros(256, dtype=torch.uint8, device=dev)
+    grp = timed(lambda: api.ws_matvec_q8_grouped(q8_probs, workspace=wsg, stream=stream))
+    out["ws_q8_qwen3_8b_4_shapes_grouped_us"] = grp
+    out["ws_q8_qwen3_8b_grouped_frac_of_hbm"] = q8_bytes / (grp * 1e-6) / 1e9 / peak
+    del q8_calls, q8_probs
     K, N = 4096, 151936
     q, d = q8_weights(N, K)
     X = f16((7, K), 1.0)

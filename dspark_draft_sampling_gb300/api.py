@@ -65,6 +65,8 @@ SIGNATURES = {
     "dspark_ws_matvec_grouped_host": (_I, [_P, _I, _P, _Z, _P, _P]),
     "dspark_ws_matvec_q8_workspace_bytes": (_Z, [_I, _I, _I]),
     "dspark_ws_matvec_q8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "dspark_ws_matvec_q8_grouped_workspace_bytes": (_Z, [_P, _I]),
+    "dspark_ws_matvec_q8_grouped": (_I, [_P, _I, _P, _Z, _P]),
 }
 
 _lock = threading.Lock()
@@ -492,6 +494,37 @@ def ws_matvec_q8(Wq, Wd, X, *, out=None, out_fp32: bool = False, workspace=None,
                                  _ptr(workspace, "workspace"), workspace.numel(), _stream(stream))
     _check(lib, st)
     return out
+
+
+class WsQ8Problem(ctypes.Structure):
+    """dspark_ws_q8_problem."""
+    _fields_ = [("Wq", ctypes.c_void_p), ("Wd", ctypes.c_void_p), ("X", ctypes.c_void_p),
+                ("Y", ctypes.c_void_p), ("y_is_fp32", ctypes.c_int), ("M", ctypes.c_int),
+                ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
+    """Several independent Y = X dequant(W)^T in one launch.  problems: list of (Wq int8
+    [N,K], Wd fp16 bits [N,K/32], X fp16 [M,K], Y [M,N] fp16 or fp32) device tensors; Y is
+    written in place."""
+    lib = load_library()
+    arr = (WsQ8Problem * len(problems))()
+    for i, (Wq, Wd, X, Y) in enumerate(problems):
+        N, K = Wq.shape
+        M, K2 = X.shape
+        if K != K2 or tuple(Y.shape) != (M, N) or tuple(Wd.shape) != (N, K // 32):
+            raise ValueError(f"problem {i}: Wq [N,K], Wd [N,K/32], X [M,K] and Y [M,N] disagree")
+        arr[i] = WsQ8Problem(_ptr(Wq, "Wq", dtypes=(torch.int8,)), _ptr(Wd, "Wd", itemsize=2, dtypes=_BITS16),
+                             _ptr(X, "X", itemsize=2, dtypes=_BITS16),
+                             _ptr(Y, "Y", dtypes=(torch.float16, torch.float32)),
+                             1 if Y.dtype == torch.float32 else 0, M, N, K)
+    if workspace is None:
+        n = int(lib.dspark_ws_matvec_q8_grouped_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(arr)))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=problems[0][0].device)
+    st = lib.dspark_ws_matvec_q8_grouped(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(workspace, "workspace"),
+                                         workspace.numel(), _stream(stream))
+    _check(lib, st)
+    return [p[3] for p in problems]
 
 
 # ---- host-buffer forms: per-call inputs and outputs in (pinned) host memory ----

@@ -89,35 +89,59 @@ static_assert(kASlots % kMmaIssuers == 0 && kASlots % 2 == 0,
               "the issuer (and the converter group) of stage j must also own stage j - kASlots, "
               "so that its parity waits on the slot's barriers are exact");
 
-struct Q8Args {
+constexpr int kMaxProblems = 8;
+constexpr int kGroupMaxSplit = 2;  // split cap of a grouped launch (a power of two)
+
+struct Q8Problem {
     const uint16_t *d;  // [N, K/32] fp16 scales
     void *Y;
     int y_fp32;
     int M, N, K;
     int nsb;    // 256-k superblocks
     int S;      // units per row block
-    int units;  // row blocks x S; CTA c takes units c, c + gridDim.x, ...
-    int cluster;  // 1: one unit per CTA and the S units of a row block form a cluster
-    int mcols;    // cluster mode: partial columns sent per row (8 or 16)
+    int nrb;    // row blocks (units beyond nrb * S are padding and stream nothing)
+    int unit0;  // first unit of the problem (a multiple of the cluster size)
+    int mcols;  // cluster mode: partial columns sent per row (8 or 16)
+};
+
+// Kernel parameters: up to P problems share one launch.  Units are numbered across the
+// problems, problem p holding units unit0 .. (next problem's unit0) - 1; CTA c takes units c,
+// c + gridDim.x, ...  The tensor maps stay in parameter space (__grid_constant__), where TMA
+// reads them.  A single-problem launch uses P = 1.
+template <int P>
+struct Q8GroupT {
+    int nprob;
+    int units;
+    int cluster;  // 1: one unit per CTA, and the S units of a row block are CTAs of one cluster
+    int csize;    // cluster size (a multiple of every problem's S; 1 without clusters)
     unsigned *status;   // workspace status word: kWsStatusTimeout when a wait gave up
     unsigned long long timeout_ns;
     unsigned long long stall_ns;  // > 0 (fault-injection hook only): the epilogue first waits
                                   // this long on a barrier that nothing signals
+    Q8Problem prob[P];
+    CUtensorMap tmQ[P];
+    CUtensorMap tmX[P];
 };
 
 struct Unit {
-    int rb, sb0, nsup, nst, ks0, n0;
+    int p, rb, sk, sb0, nsup, nst, ks0, n0;
 };
 
-__device__ __forceinline__ Unit unit_geometry(const Q8Args &a, int u) {
+template <int P>
+__device__ __forceinline__ Unit unit_geometry(const Q8GroupT<P> &grp, int u) {
     Unit g;
-    g.rb = u / a.S;
-    const int sk = u % a.S;
+    int p = 0;
+    while (p + 1 < grp.nprob && u >= grp.prob[p + 1].unit0) ++p;
+    const Q8Problem &a = grp.prob[p];
+    const int v = u - a.unit0;
+    g.p = p;
+    g.rb = v / a.S;
+    g.sk = v % a.S;
     // 32-bit: sk <= 8 and nsb < 2^23
-    g.sb0 = static_cast<int>(static_cast<unsigned>(sk) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
+    g.sb0 = static_cast<int>(static_cast<unsigned>(g.sk) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
     const int sb1 =
-        static_cast<int>(static_cast<unsigned>(sk + 1) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
-    g.nsup = sb1 - g.sb0;
+        static_cast<int>(static_cast<unsigned>(g.sk + 1) * static_cast<unsigned>(a.nsb) / static_cast<unsigned>(a.S));
+    g.nsup = g.rb < a.nrb ? sb1 - g.sb0 : 0;  // padding units stream nothing
     g.nst = g.nsup * kSuper;   // 128-k stages
     g.ks0 = g.sb0 * kSuper;    // first 128-k stage index along K
     g.n0 = g.rb * kRows;
@@ -154,7 +178,7 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void store_y(const Q8Args &a, int row, const float (&y)[kNPad]) {
+__device__ __forceinline__ void store_y(const Q8Problem &a, int row, const float (&y)[kNPad]) {
 #pragma unroll
     for (int m = 0; m < kNPad; ++m) {
         if (m < a.M) {
@@ -170,8 +194,8 @@ __device__ __forceinline__ void store_y(const Q8Args &a, int row, const float (&
 // Stage J is the CTA's J-th 128-k stage over all its units, in order.  Ring positions:
 // shared-memory slot J % kStages, TMEM A slot and accumulator group J % kASlots, and the
 // phase of each ring's barrier is (J / ring size) & 1.
-__global__ void __launch_bounds__(kThreads, 1)
-    ws_q8_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, Q8Args a) {
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_constant__ Q8GroupT<P> g) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     unsigned char *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);  // 1024-aligned slots
@@ -192,30 +216,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA producer state (warp kTmaWarp, lane 0): unit u (its geometry computed once), stage j
     // within it, stage J overall
     int pu = blockIdx.x, pj = 0, pJ = 0;
-    Unit pug = unit_geometry(a, pu < a.units ? pu : 0);
+    Unit pug = unit_geometry(g, pu < g.units ? pu : 0);
     bool pstop = false;
     uint64_t pol_q = 0, pol_x = 0;
     // issues the stages up to (not including) stage Jend: int8 tile + two X atoms per stage
     auto produce = [&](int Jend) {
-        while (!pstop && pu < a.units && pJ < Jend) {
+        while (!pstop && pu < g.units && pJ < Jend) {
             if (pj >= pug.nst) {
                 pu += gridDim.x;
                 pj = 0;
-                if (pu < a.units) pug = unit_geometry(a, pu);
+                if (pu < g.units) pug = unit_geometry(g, pu);
                 continue;
             }
             const int st = pJ % kStages;
             // slot st was last used by stage J - kStages
-            if (!mbar_wait(&done[st], static_cast<uint32_t>(((pJ / kStages) & 1) ^ 1), a.timeout_ns)) {
-                atomicOr(a.status, kWsStatusTimeout);
+            if (!mbar_wait(&done[st], static_cast<uint32_t>(((pJ / kStages) & 1) ^ 1), g.timeout_ns)) {
+                atomicOr(g.status, kWsStatusTimeout);
                 pstop = true;
                 break;
             }
             unsigned char *slot = ring + size_t(st) * kSlotBytes;
             const int k0 = (pug.ks0 + pj) * kKS;
             mbar_arrive_expect_tx(&full_r[st], kSlotBytes);
-            tma_load_3d(slot, &tmQ, 0, pug.n0, k0 / 128, &full_r[st], pol_q);
-            tma_load_3d(slot + kQBytes, &tmX, 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
+            tma_load_3d(slot, &g.tmQ[pug.p], 0, pug.n0, k0 / 128, &full_r[st], pol_q);
+            tma_load_3d(slot + kQBytes, &g.tmX[pug.p], 0, 0, k0 / 64, &full_r[st], pol_x);  // both X atoms
             ++pj;
             ++pJ;
         }
@@ -228,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&done[s], 1);
         }
         for (int s = 0; s < kASlots; ++s) mbar_init(&full_a[s], 4);
-        for (int g = 0; g < kTGroups; ++g) mbar_init(&empty_t[g], 4);
+        for (int t = 0; t < kTGroups; ++t) mbar_init(&empty_t[t], 4);
         for (int i = 0; i < kMmaIssuers; ++i) mbar_init(&mma_done[i], 1);
         mbar_init(never, 1);
         fence_mbar_init();
@@ -251,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             produce(0x7fffffff);
             // copies still in flight (possible only after a consumer gave up) land before exit
             for (int i = pJ > kStages ? pJ - kStages : 0; i < pJ; ++i)
-                mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.timeout_ns);
+                mbar_wait(&full_r[i % kStages], static_cast<uint32_t>((i / kStages) & 1), g.timeout_ns);
         }
     } else if (warp >= kMmaWarp) {
         // ---- MMA issuers: warp kMmaWarp + i the stages J = i mod kMmaIssuers ----
@@ -261,23 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dX0 = smem_desc_sw128(smem_addr(ring + kQBytes));
             int J = 0;
             bool stop = false;
-            for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
-                const int nst = unit_geometry(a, u).nst;
+            for (int u = blockIdx.x; u < g.units && !stop; u += gridDim.x) {
+                const int nst = unit_geometry(g, u).nst;
                 for (int j = 0; j < nst; ++j, ++J) {
                     if (J % kMmaIssuers != par) continue;
-                    const int st = J % kStages, g = J % kASlots;
+                    const int st = J % kStages, ag = J % kASlots;
                     const uint32_t ph = static_cast<uint32_t>((J / kASlots) & 1);
                     // the converters arrive on full_a only after the stage's TMA copies (X included)
                     // have landed, so this one wait orders both operands before the MMAs
-                    if (!mbar_wait(&full_a[g], ph, a.timeout_ns) || !mbar_wait(&empty_t[g], ph ^ 1u, a.timeout_ns)) {
-                        atomicOr(a.status, kWsStatusTimeout);
+                    if (!mbar_wait(&full_a[ag], ph, g.timeout_ns) || !mbar_wait(&empty_t[ag], ph ^ 1u, g.timeout_ns)) {
+                        atomicOr(g.status, kWsStatusTimeout);
                         stop = true;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t dB = dX0 + static_cast<uint64_t>(st * (kSlotBytes >> 4));
-                    const uint32_t ta = tmem + kAColBase + static_cast<uint32_t>(g) * kACols;
-                    const uint32_t td = tmem + static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+                    const uint32_t ta = tmem + kAColBase + static_cast<uint32_t>(ag) * kACols;
+                    const uint32_t td = tmem + static_cast<uint32_t>(ag * kBlocksPerStage * kNPad);
 #pragma unroll
                     for (int b = 0; b < kBlocksPerStage; ++b) {
                         // block b = k 32b .. 32b + 31: A columns 16b (+8); X atom b/2, byte offset 64 (b%2) (+32)
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_commit(&mma_done[par]);  // arrives once every MMA this thread issued has completed
-            if (!mbar_wait(&mma_done[par], 0, a.timeout_ns)) atomicOr(a.status, kWsStatusTimeout);
+            if (!mbar_wait(&mma_done[par], 0, g.timeout_ns)) atomicOr(g.status, kWsStatusTimeout);
         }
     } else if (warp >= 4) {
         // ---- converters: one weight row's 128 int8 -> 128 fp16 in TMEM, alternate stages ----
@@ -299,21 +323,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
         bool broken = false;
         int J = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-            const int nst = unit_geometry(a, u).nst;
+        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
+            const int nst = unit_geometry(g, u).nst;
             for (int j = 0; j < nst; ++j, ++J) {
                 if ((J & 1) != par) continue;
                 const int st = J % kStages, as = J % kASlots;
-                if (!broken && !mbar_wait(&full_r[st], static_cast<uint32_t>((J / kStages) & 1), a.timeout_ns))
+                if (!broken && !mbar_wait(&full_r[st], static_cast<uint32_t>((J / kStages) & 1), g.timeout_ns))
                     broken = true;
                 if (J >= kASlots) {  // A slot J % kASlots was last read by stage J - kASlots
                     const int jp = J - kASlots;
                     if (!broken &&
-                        !mbar_wait(&done[jp % kStages], static_cast<uint32_t>((jp / kStages) & 1), a.timeout_ns))
+                        !mbar_wait(&done[jp % kStages], static_cast<uint32_t>((jp / kStages) & 1), g.timeout_ns))
                         broken = true;
                 }
                 broken = __any_sync(0xffffffffu, broken);
-                if (broken && lane == 0) atomicOr(a.status, kWsStatusTimeout);
+                if (broken && lane == 0) atomicOr(g.status, kWsStatusTimeout);
                 if (!broken) {
                     const unsigned char *rowp = ring + size_t(st) * kSlotBytes + r * kKS;
 #pragma unroll
@@ -348,11 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---- epilogue: warp w owns TMEM lanes / weight rows 32w .. 32w+31 of each unit ----
         const int lrow = warp * 32 + lane;
-        if (a.stall_ns && !mbar_wait(never, 0, a.stall_ns) && threadIdx.x == 0) atomicOr(a.status, kWsStatusTimeout);
+        if (g.stall_ns && !mbar_wait(never, 0, g.stall_ns) && threadIdx.x == 0) atomicOr(g.status, kWsStatusTimeout);
         bool ok = true;
         int J = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-            const Unit ug = unit_geometry(a, u);
+        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
+            const Unit ug = unit_geometry(g, u);
+            const Q8Problem &a = g.prob[ug.p];
             const int row = ug.n0 + lrow;
             const bool rowok = row < a.N;
             const uint16_t *drow = a.d + size_t(rowok ? row : 0) * (a.K / 32) + size_t(ug.sb0) * 8;
@@ -374,13 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                    : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int h = 0; h < kSuper; ++h, ++J) {  // one stage = one group of 4 accumulator slots
-                    const int st = J % kStages, g = J % kTGroups;
-                    if (ok) ok = mbar_wait(&done[st], static_cast<uint32_t>((J / kStages) & 1), a.timeout_ns);
+                    const int st = J % kStages, tg = J % kTGroups;
+                    if (ok) ok = mbar_wait(&done[st], static_cast<uint32_t>((J / kStages) & 1), g.timeout_ns);
                     ok = __all_sync(0xffffffffu, ok);
-                    if (!ok && lane == 0) atomicOr(a.status, kWsStatusTimeout);
+                    if (!ok && lane == 0) atomicOr(g.status, kWsStatusTimeout);
                     tc_fence_after();
                     const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
-                                        static_cast<uint32_t>(g * kBlocksPerStage * kNPad);
+                                        static_cast<uint32_t>(tg * kBlocksPerStage * kNPad);
                     // two blocks' sums at a time (fewer live registers); the group is handed back
                     // once all four are read
 #pragma unroll
@@ -397,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hq + 2 == kBlocksPerStage) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0 && ok) mbar_arrive(&empty_t[g]);
+                            if (lane == 0 && ok) mbar_arrive(&empty_t[tg]);
                         }
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
@@ -412,16 +437,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (a.S == 1) {
                 if (ok && rowok) store_y(a, row, acc);
-            } else if (a.cluster) {
+            } else if (g.cluster) {
                 // Every CTA has one unit.  First barrier: every CTA of the cluster has finished
                 // its stream, so the ring of unit 0 is idle; units 1..S-1 then store this row's
                 // partial into it, and after the second barrier unit 0 sums
-                // y = 0 + p_0 + p_1 + ... + p_{S-1}, the order of the workspace path.
-                const int sk = u % a.S;
+                // y = 0 + p_0 + p_1 + ... + p_{S-1}.  Unit 0 of the row block is cluster rank
+                // (c mod cluster size) - sk, the same bits whatever the cluster size.
+                const int sk = ug.sk;
+                const uint32_t rank0 = static_cast<uint32_t>(static_cast<int>(blockIdx.x) % g.csize - sk);
                 cluster_sync_all();
                 float *recv = reinterpret_cast<float *>(ring);
                 if (sk != 0) {
-                    const uint32_t dst = map_to_rank(smem_addr(recv + (size_t(sk - 1) * kRows + lrow) * a.mcols), 0u);
+                    const uint32_t dst = map_to_rank(smem_addr(recv + (size_t(sk - 1) * kRows + lrow) * a.mcols), rank0);
 #pragma unroll
                     for (int q = 0; q < kNPad / 4; ++q)
                         if (4 * q < a.mcols)
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     // cluster mode: the two barriers of the epilogue, for every other thread of the CTA
-    if (a.cluster && a.S > 1 && warp >= 4) {
+    if (g.cluster && warp >= 4 && g.prob[unit_geometry(g, blockIdx.x).p].S > 1) {
         cluster_sync_all();
         cluster_sync_all();
     }
@@ -469,13 +496,17 @@ struct Plan {
 dspark_status configure_kernel(int dev) {
     static int configured_dev = -1;
     if (configured_dev == dev) return DSPARK_OK;
-    cudaError_t e = cudaFuncSetAttribute(ws_q8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec_q8)");
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ws_q8_tc_kernel, kThreads, kSmemBytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec_q8)");
-    if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
+    const void *kerns[2] = {reinterpret_cast<const void *>(ws_q8_tc_kernel<1>),
+                            reinterpret_cast<const void *>(ws_q8_tc_kernel<kMaxProblems>)};
+    for (const void *kern : kerns) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(ws_matvec_q8)");
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ws_matvec_q8)");
+        if (per_sm < 1) return fail(DSPARK_ERR_CUDA, "ws_matvec_q8 kernel cannot be resident on an SM");
+    }
     configured_dev = dev;
     return DSPARK_OK;
 }
@@ -505,7 +536,7 @@ int cluster_capacity(int S) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, ws_q8_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&c, ws_q8_tc_kernel<1>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         c = 0;
     }
@@ -584,59 +615,122 @@ extern "C" size_t dspark_ws_matvec_q8_workspace_bytes(int M, int N, int K) {
 }
 
 namespace {
+using namespace dspark;
 
-dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
-                         int K, void *workspace, size_t workspace_bytes, unsigned long long stall_ns,
-                         dspark_stream_t stream) {
-    using namespace dspark;
+// Validation of one problem; `what` names the entry point in error texts.
+dspark_status check_q8_problem(const dspark_ws_q8_problem &q, const char *what) {
+    if (q.M < 0 || q.N < 0 || q.K < 0) return fail(DSPARK_ERR_INVALID, "%s: negative size", what);
+    if (q.M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "%s: M=%d > 16", what, q.M);
+    if (q.K == 0 || (q.K % 256) != 0)
+        return fail(DSPARK_ERR_UNSUPPORTED, "%s: K=%d is not a multiple of 256", what, q.K);
+    if (q.M == 0 || q.N == 0) return DSPARK_OK;  // nothing to do for this problem
+    if (!q.Wq || !q.Wd || !q.X || !q.Y) return fail(DSPARK_ERR_INVALID, "%s: null pointer argument", what);
+    if (!aligned(q.Wq, 16) || !aligned(q.Wd, 16) || !aligned(q.X, 16))
+        return fail(DSPARK_ERR_INVALID, "%s: Wq, Wd and X must be 16-byte aligned", what);
+    if (!aligned(q.Y, q.y_is_fp32 ? 4 : 2)) return fail(DSPARK_ERR_INVALID, "%s: misaligned Y", what);
+    return DSPARK_OK;
+}
+
+// One launch for n problems.  A single problem keeps its own plan: one unit per CTA in
+// clusters of S when it is split, else persistent CTAs walking the units.  Several problems
+// share one grid of one unit per CTA (as many waves as that takes), each with the split it
+// would get alone capped at kGroupMaxSplit, so that one cluster size (the largest split)
+// serves all of them; problems are padded to whole clusters and taken longest units first.
+// Wider clusters schedule worse in a grid of several waves (a new cluster needs that many free
+// SMs of one GPC at once): on the four Qwen3-8B projections, caps of 8 / 4 / 2 measured 55.3 /
+// 47.3 / 41.1 us, and no split with persistent CTAs 63.5 us.  A problem whose own split is at
+// most the cap gives the same bits alone and in a group.
+dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *workspace, size_t workspace_bytes,
+                               unsigned long long stall_ns, dspark_stream_t stream) {
+    const char *what = n == 1 && probs ? "ws_matvec_q8" : "ws_matvec_q8_grouped";
     clear_error();
-    if (M < 0 || N < 0 || K < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: negative size");
-    if (M > 16) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: M=%d > 16", M);
-    if (K == 0 || (K % 256) != 0) return fail(DSPARK_ERR_UNSUPPORTED, "ws_matvec_q8: K=%d is not a multiple of 256", K);
-    if (M == 0 || N == 0) return DSPARK_OK;  // nothing to enqueue
-    if (!Wq || !Wd || !X || !Y || !workspace) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: null pointer argument");
-    if (!aligned(Wq, 16) || !aligned(Wd, 16) || !aligned(X, 16))
-        return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: Wq, Wd and X must be 16-byte aligned");
-    if (!aligned(Y, y_is_fp32 ? 4 : 2)) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: misaligned Y");
-    if (!aligned(workspace, 256)) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace must be 256-byte aligned");
+    if (n < 0 || n > kMaxProblems) return fail(DSPARK_ERR_UNSUPPORTED, "%s: %d problems (at most %d)", what, n, kMaxProblems);
+    if (n > 0 && !probs) return fail(DSPARK_ERR_INVALID, "%s: null problem array", what);
+    int live = 0;
+    for (int i = 0; i < n; ++i) {
+        dspark_status st = check_q8_problem(probs[i], what);
+        if (st != DSPARK_OK) return st;
+        if (probs[i].M != 0 && probs[i].N != 0) ++live;
+    }
+    if (live == 0) return DSPARK_OK;  // nothing to enqueue
+    if (!workspace) return fail(DSPARK_ERR_INVALID, "%s: null workspace", what);
+    if (!aligned(workspace, 256)) return fail(DSPARK_ERR_INVALID, "%s: workspace must be 256-byte aligned", what);
+    if (workspace_bytes < kWsHeaderBytes)
+        return fail(DSPARK_ERR_INVALID, "%s: workspace of %zu bytes < required %zu", what, workspace_bytes,
+                    kWsHeaderBytes);
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
     int dev = 0;
-    cudaError_t e0 = cudaGetDevice(&dev);
-    if (e0 != cudaSuccess) return cuda_fail(e0, "cudaGetDevice");
-    dspark_status st0 = configure_kernel(dev);
-    if (st0 != DSPARK_OK) return st0;
-    const Plan p = plan_for(N, K, sms);
-    const size_t need = kWsHeaderBytes;
-    if (workspace_bytes < need)
-        return fail(DSPARK_ERR_INVALID, "ws_matvec_q8: workspace of %zu bytes < required %zu", workspace_bytes, need);
-
-    CUtensorMap tmQ, tmX;
-    dspark_status st = make_tmap_kblocks_u8(&tmQ, Wq, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kRows, 1);
-    if (st != DSPARK_OK) return st;
-    st = make_tmap_kblocks(&tmX, X, false, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kNPad, 2);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    dspark_status st = configure_kernel(dev);
     if (st != DSPARK_OK) return st;
 
-    Q8Args args;
-    args.d = Wd;
-    args.Y = Y;
-    args.y_fp32 = y_is_fp32 ? 1 : 0;
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.nsb = p.nsb;
-    args.S = p.S;
-    args.units = p.nrb * p.S;
-    args.timeout_ns = kDefaultTimeoutNs;
-    args.cluster = p.cluster ? 1 : 0;
-    args.mcols = M <= 8 ? 8 : 16;
-    args.status = static_cast<unsigned *>(workspace);
-    args.stall_ns = stall_ns;
+    Q8GroupT<kMaxProblems> g;
+    g.nprob = 0;
+    g.status = static_cast<unsigned *>(workspace);
+    g.timeout_ns = kDefaultTimeoutNs;
+    g.stall_ns = stall_ns;
+    int order[kMaxProblems];
+    Plan plans[kMaxProblems];
+    int norder = 0;
+    for (int i = 0; i < n; ++i)
+        if (probs[i].M != 0 && probs[i].N != 0) {
+            plans[norder] = plan_for(probs[i].N, probs[i].K, sms);
+            if (live > 1) {  // grouped: one unit per CTA, the split capped
+                const int S = plans[norder].S < kGroupMaxSplit ? plans[norder].S : kGroupMaxSplit;
+                plans[norder].S = S;
+                plans[norder].cluster = S > 1;
+            }
+            order[norder++] = i;
+        }
+    auto unit_sup = [&](int j) { return (plans[j].nsb + plans[j].S - 1) / plans[j].S; };
+    int idx[kMaxProblems];
+    for (int j = 0; j < norder; ++j) idx[j] = j;
+    for (int x = 1; x < norder; ++x)  // stable insertion sort, longest units first
+        for (int y = x; y > 0 && unit_sup(idx[y]) > unit_sup(idx[y - 1]); --y) {
+            const int t = idx[y];
+            idx[y] = idx[y - 1];
+            idx[y - 1] = t;
+        }
+    int csize = 1;
+    for (int j = 0; j < norder; ++j) csize = plans[j].S > csize ? plans[j].S : csize;
+    g.csize = csize;
+    g.cluster = csize > 1 ? 1 : 0;
+    unsigned units = 0;
+    for (int oj = 0; oj < norder; ++oj) {
+        const int jj = idx[oj];
+        const dspark_ws_q8_problem &q = probs[order[jj]];
+        const Plan &p = plans[jj];
+        const int j = g.nprob++;
+        st = make_tmap_kblocks_u8(&g.tmQ[j], q.Wq, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K), kRows, 1);
+        if (st != DSPARK_OK) return st;
+        st = make_tmap_kblocks(&g.tmX[j], q.X, false, static_cast<uint64_t>(q.M), static_cast<uint64_t>(q.K), kNPad, 2);
+        if (st != DSPARK_OK) return st;
+        Q8Problem &a = g.prob[j];
+        a.d = q.Wd;
+        a.Y = q.Y;
+        a.y_fp32 = q.y_is_fp32 ? 1 : 0;
+        a.M = q.M;
+        a.N = q.N;
+        a.K = q.K;
+        a.nsb = p.nsb;
+        a.S = p.S;
+        a.nrb = p.nrb;
+        a.unit0 = static_cast<int>(units);
+        a.mcols = q.M <= 8 ? 8 : 16;
+        // whole clusters per problem: the last one may hold padding units
+        const unsigned pu = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
+        units += (pu + static_cast<unsigned>(csize) - 1) / static_cast<unsigned>(csize) * static_cast<unsigned>(csize);
+    }
+    g.units = static_cast<int>(units);
 
-    const int grid = args.units < sms ? args.units : sms;  // persistent: one CTA per SM
+    // one problem unsplit: persistent CTAs (at most one per SM); otherwise one unit per CTA
+    const unsigned grid =
+        (live == 1 && csize == 1) ? (units < static_cast<unsigned>(sms) ? units : static_cast<unsigned>(sms)) : units;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -645,16 +739,38 @@ dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.cluster) {
+    if (csize > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(p.S);
+        attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel, tmQ, tmX, args);
+    if (g.nprob == 1) {  // the small parameter block
+        Q8GroupT<1> g1;
+        g1.nprob = 1;
+        g1.units = g.units;
+        g1.cluster = g.cluster;
+        g1.csize = g.csize;
+        g1.status = g.status;
+        g1.timeout_ns = g.timeout_ns;
+        g1.stall_ns = g.stall_ns;
+        g1.prob[0] = g.prob[0];
+        g1.tmQ[0] = g.tmQ[0];
+        g1.tmX[0] = g.tmX[0];
+        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<1>, g1);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<kMaxProblems>, g);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
+}
+
+dspark_status q8_enqueue(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y, int y_is_fp32, int M, int N,
+                         int K, void *workspace, size_t workspace_bytes, unsigned long long stall_ns,
+                         dspark_stream_t stream) {
+    const dspark_ws_q8_problem q = {Wq, Wd, X, Y, y_is_fp32, M, N, K};
+    return q8_enqueue_group(&q, 1, workspace, workspace_bytes, stall_ns, stream);
 }
 
 }  // namespace
@@ -663,6 +779,17 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
                                              int y_is_fp32, int M, int N, int K, void *workspace,
                                              size_t workspace_bytes, dspark_stream_t stream) {
     return q8_enqueue(Wq, Wd, X, Y, y_is_fp32, M, N, K, workspace, workspace_bytes, 0ull, stream);
+}
+
+extern "C" size_t dspark_ws_matvec_q8_grouped_workspace_bytes(const dspark_ws_q8_problem *problems, int n_problems) {
+    (void)problems;
+    (void)n_problems;
+    return dspark::kWsHeaderBytes;  // the status word
+}
+
+extern "C" dspark_status dspark_ws_matvec_q8_grouped(const dspark_ws_q8_problem *problems, int n_problems,
+                                                     void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
+    return q8_enqueue_group(problems, n_problems, workspace, workspace_bytes, 0ull, stream);
 }
 
 extern "C" dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,

@@ -337,6 +337,30 @@ dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const ui
                                   int y_is_fp32, int M, int N, int K, void *workspace,
                                   size_t workspace_bytes, dspark_stream_t stream);
 
+/* Grouped form: up to 8 independent Q8_0 problems in one launch (e.g. the four projections
+ * of a layer), so the fixed launch and pipeline costs are paid once and the SMs left idle by
+ * one problem take the next one's work.  Each problem has the arguments and limits of
+ * dspark_ws_matvec_q8.  Each problem keeps the K split it gets alone, capped at 2 (so that
+ * clusters of at most 2 CTAs serve them all); a problem whose own split is 1 or 2 gets
+ * results bit-identical to a separate dspark_ws_matvec_q8 call, any other still sums in one
+ * fixed order.  The grid holds one 128-row unit per CTA, in as many waves as that takes.  Problems with M == 0 or N == 0 are
+ * skipped.  The workspace (dspark_ws_matvec_q8_grouped_workspace_bytes, 256, zero-filled
+ * before first use) holds the status word.  More than 8 problems: DSPARK_ERR_UNSUPPORTED. */
+typedef struct dspark_ws_q8_problem {
+    const int8_t *Wq;    /* int8 [N, K] (dspark_q8_0_repack), 16-byte aligned */
+    const uint16_t *Wd;  /* fp16 [N, K/32] scales, 16-byte aligned */
+    const uint16_t *X;   /* fp16 [M, K], 16-byte aligned */
+    void *Y;             /* [M, N], fp32 if y_is_fp32 else fp16 */
+    int y_is_fp32;
+    int M, N, K;
+} dspark_ws_q8_problem;
+
+size_t dspark_ws_matvec_q8_grouped_workspace_bytes(const dspark_ws_q8_problem *problems,
+                                                   int n_problems);
+dspark_status dspark_ws_matvec_q8_grouped(const dspark_ws_q8_problem *problems, int n_problems,
+                                          void *workspace, size_t workspace_bytes,
+                                          dspark_stream_t stream);
+
 /* As dspark_ws_matvec_debug, for the Q8_0 matvec (status read by dspark_ws_matvec_status). */
 dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X,
                                         void *Y, int y_is_fp32, int M, int N, int K,

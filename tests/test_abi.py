@@ -294,6 +294,34 @@ def test_ws_grouped_validation(dspark_lib):
     assert g(p, 1, NULL, 1 << 20, NULL) == INVALID
 
 
+def test_ws_q8_grouped_validation(dspark_lib):
+    lib = dspark_lib
+    P = api.WsQ8Problem
+    arr = (P * 9)()
+    for i in range(9):
+        arr[i] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 256)
+    g = lib.dspark_ws_matvec_q8_grouped
+    p = ctypes.cast(arr, ctypes.c_void_p)
+    assert g(p, 9, FAKE, 1 << 20, NULL) == UNSUPPORTED
+    assert g(NULL, 2, FAKE, 1 << 20, NULL) == INVALID
+    assert g(p, 0, NULL, 0, NULL) == 0
+    arr[1] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 17, 64, 256)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == UNSUPPORTED
+    arr[1] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 288)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == UNSUPPORTED
+    arr[1] = P(FAKE.value, None, FAKE.value, FAKE.value, 0, 7, 64, 256)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == INVALID
+    arr[1] = P(FAKE.value, FAKE_ODD.value, FAKE.value, FAKE.value, 0, 7, 64, 256)
+    assert g(p, 2, FAKE, 1 << 20, NULL) == INVALID
+    arr[0] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 0, 64, 256)
+    arr[1] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 0, 256)
+    assert g(p, 2, NULL, 0, NULL) == 0  # every problem empty: nothing to enqueue
+    arr[0] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 256)
+    assert g(p, 1, NULL, 1 << 20, NULL) == INVALID
+    assert g(p, 1, FAKE, 16, NULL) == INVALID
+    assert lib.dspark_ws_matvec_q8_grouped_workspace_bytes(p, 2) == 256
+
+
 def test_ws_grouped_host_validation(dspark_lib):
     lib = dspark_lib
     arr = (api.WsProblem * 2)()

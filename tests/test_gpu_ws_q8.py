@@ -138,3 +138,57 @@ def test_workspace_status_reports_a_wait_that_gave_up():
     y2 = api.ws_matvec_q8(q, d, X, out_fp32=True, workspace=ws)
     assert api.ws_matvec_status(ws) == 0
     parity.check_ws_q8(inp, y32=y2.cpu().numpy())
+
+
+def _grouped(inps, fp32_flags):
+    devs = [_dev(inp) for inp in inps]
+    outs = [torch.empty((inp["M"], inp["N"]), dtype=torch.float32 if f else torch.float16, device="cuda")
+            for inp, f in zip(inps, fp32_flags)]
+    api.ws_matvec_q8_grouped([(q, d, X, Y) for (q, d, X), Y in zip(devs, outs)])
+    torch.cuda.synchronize()
+    return [Y.cpu().numpy() if Y.dtype == torch.float32 else Y.cpu().view(torch.int16).numpy().view(np.uint16)
+            for Y in outs]
+
+
+def test_grouped_qwen3_8b_shapes():
+    """The four projections in one launch, within tolerance of the oracle; the 4096 -> 12288
+    projection (not split alone) bit-identical to its own call."""
+    inps = [synth.ws_q8_inputs(7, N, K, seed=K + N) for (K, N) in synth.WS_SHAPES]
+    g32 = _grouped(inps, [True] * 4)
+    g16 = _grouped(inps, [False] * 4)
+    for (K, N), inp, a32, a16 in zip(synth.WS_SHAPES, inps, g32, g16):
+        parity.check_ws_q8(inp, y32=a32, y16=a16)
+        if (K, N) == (4096, 12288):
+            y32, y16 = _run(inp)
+            np.testing.assert_array_equal(a32.view(np.uint32), y32.view(np.uint32))
+            np.testing.assert_array_equal(a16, y16)
+
+
+@pytest.mark.parametrize("shapes", [
+    [(1, 40000, 512), (16, 300, 2304), (3, 1, 256)],                  # one problem wider than the SMs
+    [(7, 1000, 4096), (2, 153, 12288), (9, 5000, 256), (4, 64, 1024)],  # splits 1 .. 8 alone, capped at 2
+    [(5, 777, 6400), (8, 128, 768)],                                    # K of 25 and 3 superblocks
+])
+def test_grouped_ragged_mixed(shapes):
+    inps = [synth.ws_q8_inputs(M, N, K, seed=M + N + K) for (M, N, K) in shapes]
+    flags = [i % 2 == 0 for i in range(len(inps))]
+    outs = _grouped(inps, flags)
+    for inp, f, y in zip(inps, flags, outs):
+        if f:
+            parity.check_ws_q8(inp, y32=y)
+        else:
+            parity.check_ws_q8(inp, y16=y)
+
+
+def test_grouped_skips_empty_problems_and_repeats_bitwise():
+    inps = [synth.ws_q8_inputs(3, 500, 1024, seed=5), synth.ws_q8_inputs(6, 2048, 2048, seed=6)]
+    a = _grouped(inps, [True, True])
+    b = _grouped(inps, [True, True])
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x.view(np.uint32), y.view(np.uint32))
+    q, d, X = _dev(inps[0])
+    Y = torch.full((3, 500), 7.0, device="cuda")
+    Ye = torch.full((0, 500), 7.0, device="cuda")
+    api.ws_matvec_q8_grouped([(q, d, X, Y), (q, d, X[:0], Ye)])
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(Y.cpu().numpy().view(np.uint32), a[0].view(np.uint32))
