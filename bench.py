@@ -849,7 +849,8 @@ def run_one_kernel(name: str) -> int:
     """Runs one kernel of the workload twice on cuda:0 and exits, for a profiler capture of a
     single launch (`ncu -k ... -s 1 -c 1`): `ws_4096x4096` (the fp16 weight-stationary matvec,
     M = 7), `probe_2048` (the batched confidence probe), `q8_lm_head` (the Q8_0 matvec,
-    4096 -> 151936, M = 7).  No timing is taken."""
+    4096 -> 151936, M = 7), `q8_grouped_qwen3_8b` (the four Q8_0 projections in one launch),
+    `markov_tiny` (the tiny Markov lane on the single-cluster kernel).  No timing is taken."""
     import torch
 
     from dspark_draft_sampling_gb300 import api
@@ -868,6 +869,25 @@ def run_one_kernel(name: str) -> int:
         wq = torch.from_numpy(pr["wq"]).to(dev)
         hid = torch.from_numpy(pr["hidden"]).to(dev)
         call = lambda: api.conf_probe(wq, hid, pr["bias"], pr["threshold"])
+    elif name == "q8_grouped_qwen3_8b":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        probs = []
+        for (K, N) in synth.WS_SHAPES:
+            q = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
+            d = (torch.rand((N, K // 32), generator=gen, device=dev) * 4e-4).half().view(torch.int16)
+            X = torch.randn((7, K), generator=gen, device=dev).half()
+            probs.append((q, d, X, torch.empty((7, N), dtype=torch.float16, device=dev)))
+        wsg = torch.zeros(256, dtype=torch.uint8, device=dev)
+        call = lambda: api.ws_matvec_q8_grouped(probs, workspace=wsg)
+    elif name == "markov_tiny":
+        mk = synth.markov_config("tiny")
+        base = torch.from_numpy(mk["base"]).to(dev)
+        w1 = torch.from_numpy(mk["w1"].view(np.int16)).to(dev)
+        w2 = torch.from_numpy(mk["w2"].view(np.int16)).to(dev)
+        prev = torch.from_numpy(mk["prev0"].copy()).to(dev)
+        wsm = api.new_markov_workspace(1, 4, 4096, 64, dev)
+        call = lambda: api.markov_draft(base, w1, w2, None, prev, workspace=wsm)
     elif name == "q8_lm_head":
         gen = torch.Generator(device=dev)
         gen.manual_seed(1)
@@ -906,7 +926,8 @@ def main():
                     help="skip the separately timed rows beyond the headline step")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration sweep (median/p10/p90, cold and warm L2)")
-    ap.add_argument("--kernel", choices=["ws_4096x4096", "probe_2048", "q8_lm_head"],
+    ap.add_argument("--kernel", choices=["ws_4096x4096", "probe_2048", "q8_lm_head", "q8_grouped_qwen3_8b",
+                                         "markov_tiny"],
                     help="run only this kernel of the workload twice, untimed (for a profiler)")
     args = ap.parse_args()
     if args.kernel:
