@@ -540,7 +540,7 @@ def run_next_rows(dev, reps: int = 20):
     out["ws_q8_qwen3_8b_4_shapes_back_to_back_us"] = seq
     out["ws_q8_qwen3_8b_back_to_back_frac_of_hbm"] = q8_bytes / (seq * 1e-6) / 1e9 / peak
     # the four as one grouped launch (dspark_ws_matvec_q8_grouped)
-    wsg = torch.zeros(256, dtype=torch.uint8, device=dev)
+    wsg = api.new_ws_q8_grouped_workspace(dev)
     grp = timed(lambda: api.ws_matvec_q8_grouped(q8_probs, workspace=wsg, stream=stream))
     out["ws_q8_qwen3_8b_4_shapes_grouped_us"] = grp
     out["ws_q8_qwen3_8b_grouped_frac_of_hbm"] = q8_bytes / (grp * 1e-6) / 1e9 / peak
@@ -878,7 +878,7 @@ def run_one_kernel(name: str) -> int:
             d = (torch.rand((N, K // 32), generator=gen, device=dev) * 4e-4).half().view(torch.int16)
             X = torch.randn((7, K), generator=gen, device=dev).half()
             probs.append((q, d, X, torch.empty((7, N), dtype=torch.float16, device=dev)))
-        wsg = torch.zeros(256, dtype=torch.uint8, device=dev)
+        wsg = api.new_ws_q8_grouped_workspace(dev)
         call = lambda: api.ws_matvec_q8_grouped(probs, workspace=wsg)
     elif name == "markov_tiny":
         mk = synth.markov_config("tiny")

@@ -503,6 +503,14 @@ class WsQ8Problem(ctypes.Structure):
                 ("N", ctypes.c_int), ("K", ctypes.c_int)]
 
 
+def new_ws_q8_grouped_workspace(device=None):
+    """Zero-filled workspace for ws_matvec_q8_grouped on the current device."""
+    n = int(load_library().dspark_ws_matvec_q8_grouped_workspace_bytes(None, 0))
+    if n == 0:
+        raise DsparkError(DSPARK_ERR_CUDA, "could not size the grouped ws_matvec_q8 workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
 def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
     """Several independent Y = X dequant(W)^T in one launch.  problems: list of (Wq int8
     [N,K], Wd fp16 bits [N,K/32], X fp16 [M,K], Y [M,N] fp16 or fp32) device tensors; Y is
@@ -519,8 +527,7 @@ def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
                              _ptr(Y, "Y", dtypes=(torch.float16, torch.float32)),
                              1 if Y.dtype == torch.float32 else 0, M, N, K)
     if workspace is None:
-        n = int(lib.dspark_ws_matvec_q8_grouped_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(arr)))
-        workspace = torch.zeros(n, dtype=torch.uint8, device=problems[0][0].device)
+        workspace = new_ws_q8_grouped_workspace(problems[0][0].device)
     st = lib.dspark_ws_matvec_q8_grouped(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(workspace, "workspace"),
                                          workspace.numel(), _stream(stream))
     _check(lib, st)

@@ -90,7 +90,6 @@ static_assert(kASlots % kMmaIssuers == 0 && kASlots % 2 == 0,
               "so that its parity waits on the slot's barriers are exact");
 
 constexpr int kMaxProblems = 8;
-constexpr int kGroupMaxSplit = 2;  // split cap of a grouped launch (a power of two)
 
 struct Q8Problem {
     const uint16_t *d;  // [N, K/32] fp16 scales
@@ -102,6 +101,7 @@ struct Q8Problem {
     int nrb;    // row blocks (units beyond nrb * S are padding and stream nothing)
     int unit0;  // first unit of the problem (a multiple of the cluster size)
     int mcols;  // cluster mode: partial columns sent per row (8 or 16)
+    int sb_base;  // stream-K mode: the problem's first superblock in the launch's sequence
 };
 
 // Kernel parameters: up to P problems share one launch.  Units are numbered across the
@@ -121,10 +121,30 @@ struct Q8GroupT {
     Q8Problem prob[P];
     CUtensorMap tmQ[P];
     CUtensorMap tmX[P];
+    // Stream-K mode (grouped launches): the row blocks of all problems, each K-long, form one
+    // sequence of total_sb superblocks; CTA c takes superblocks [c T / G, (c + 1) T / G).  A
+    // row block split between CTAs is finished by the CTA holding its first superblocks, which
+    // adds the later CTAs' partial rows (partials[c], flags[c]) in CTA order.
+    int streamk;
+    int total_sb;
+    float *partials;   // [grid][128][16] fp32
+    unsigned *flags;   // [grid]: 1 while partials[c] holds a row block's later part
 };
 
 struct Unit {
     int p, rb, sk, sb0, nsup, nst, ks0, n0;
+};
+
+// First superblock of CTA c's range in stream-K mode.
+__device__ __forceinline__ int range_begin(int c, int total_sb, int G) {
+    return static_cast<int>(static_cast<long long>(c) * total_sb / G);
+}
+
+// The CTA's work in order: its units c, c + gridDim.x, ..., or in stream-K mode the pieces of
+// row blocks its superblock range covers.
+struct Cursor {
+    int u;         // unit mode: the next unit
+    int gsb, end;  // stream-K mode: the next superblock and the end of the range
 };
 
 template <int P>
@@ -146,6 +166,45 @@ __device__ __forceinline__ Unit unit_geometry(const Q8GroupT<P> &grp, int u) {
     g.ks0 = g.sb0 * kSuper;    // first 128-k stage index along K
     g.n0 = g.rb * kRows;
     return g;
+}
+
+template <bool SK, int P>
+__device__ __forceinline__ Cursor cursor_begin(const Q8GroupT<P> &g) {
+    Cursor c;
+    c.u = blockIdx.x;
+    c.gsb = 0;
+    c.end = 0;
+    if constexpr (SK) {
+        c.gsb = range_begin(blockIdx.x, g.total_sb, gridDim.x);
+        c.end = range_begin(blockIdx.x + 1, g.total_sb, gridDim.x);
+    }
+    return c;
+}
+
+template <bool SK, int P>
+__device__ __forceinline__ bool cursor_next(const Q8GroupT<P> &g, Cursor &c, Unit &out) {
+    if constexpr (!SK) {
+        if (c.u >= g.units) return false;
+        out = unit_geometry(g, c.u);
+        c.u += gridDim.x;
+        return true;
+    }
+    if (c.gsb >= c.end) return false;
+    int p = 0;
+    while (p + 1 < g.nprob && c.gsb >= g.prob[p + 1].sb_base) ++p;
+    const Q8Problem &a = g.prob[p];
+    const int off = c.gsb - a.sb_base;
+    out.p = p;
+    out.rb = off / a.nsb;
+    out.sk = 0;
+    out.sb0 = off - out.rb * a.nsb;
+    const int left = a.nsb - out.sb0;
+    out.nsup = left < c.end - c.gsb ? left : c.end - c.gsb;
+    out.nst = out.nsup * kSuper;
+    out.ks0 = out.sb0 * kSuper;
+    out.n0 = out.rb * kRows;
+    c.gsb += out.nsup;
+    return true;
 }
 
 // Two int8 values (bytes of u selected by `sel`, already biased to q + 128) -> fp16x2 holding
@@ -178,6 +237,21 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (bounded) until *flag is non-zero; false if the limit ran out.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned long long timeout_ns) {
+    if (ld_acquire_u32(flag) != 0u) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (ld_acquire_u32(flag) == 0u) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void store_y(const Q8Problem &a, int row, const float (&y)[kNPad]) {
 #pragma unroll
     for (int m = 0; m < kNPad; ++m) {
@@ -194,7 +268,7 @@ __device__ __forceinline__ void store_y(const Q8Problem &a, int row, const float
 // Stage J is the CTA's J-th 128-k stage over all its units, in order.  Ring positions:
 // shared-memory slot J % kStages, TMEM A slot and accumulator group J % kASlots, and the
 // phase of each ring's barrier is (J / ring size) & 1.
-template <int P>
+template <int P, bool SK>
 __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_constant__ Q8GroupT<P> g) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -213,19 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // TMA producer state (warp kTmaWarp, lane 0): unit u (its geometry computed once), stage j
-    // within it, stage J overall
-    int pu = blockIdx.x, pj = 0, pJ = 0;
-    Unit pug = unit_geometry(g, pu < g.units ? pu : 0);
+    // TMA producer state (warp kTmaWarp, lane 0): the current piece of work (its geometry
+    // computed once), stage j within it, stage J overall
+    Cursor pc = cursor_begin<SK>(g);
+    Unit pug;
+    bool phave = cursor_next<SK>(g, pc, pug);
+    int pj = 0, pJ = 0;
     bool pstop = false;
     uint64_t pol_q = 0, pol_x = 0;
     // issues the stages up to (not including) stage Jend: int8 tile + two X atoms per stage
     auto produce = [&](int Jend) {
-        while (!pstop && pu < g.units && pJ < Jend) {
+        while (!pstop && phave && pJ < Jend) {
             if (pj >= pug.nst) {
-                pu += gridDim.x;
                 pj = 0;
-                if (pu < g.units) pug = unit_geometry(g, pu);
+                phave = cursor_next<SK>(g, pc, pug);
                 continue;
             }
             const int st = pJ % kStages;
@@ -285,8 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
             const uint64_t dX0 = smem_desc_sw128(smem_addr(ring + kQBytes));
             int J = 0;
             bool stop = false;
-            for (int u = blockIdx.x; u < g.units && !stop; u += gridDim.x) {
-                const int nst = unit_geometry(g, u).nst;
+            Cursor cur = cursor_begin<SK>(g);
+            Unit ug;
+            while (!stop && cursor_next<SK>(g, cur, ug)) {
+                const int nst = ug.nst;
                 for (int j = 0; j < nst; ++j, ++J) {
                     if (J % kMmaIssuers != par) continue;
                     const int st = J % kStages, ag = J % kASlots;
@@ -323,8 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
         bool broken = false;
         int J = 0;
-        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
-            const int nst = unit_geometry(g, u).nst;
+        Cursor cur = cursor_begin<SK>(g);
+        Unit ug;
+        while (cursor_next<SK>(g, cur, ug)) {
+            const int nst = ug.nst;
             for (int j = 0; j < nst; ++j, ++J) {
                 if ((J & 1) != par) continue;
                 const int st = J % kStages, as = J % kASlots;
@@ -375,8 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         if (g.stall_ns && !mbar_wait(never, 0, g.stall_ns) && threadIdx.x == 0) atomicOr(g.status, kWsStatusTimeout);
         bool ok = true;
         int J = 0;
-        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
-            const Unit ug = unit_geometry(g, u);
+        Cursor cur = cursor_begin<SK>(g);
+        Unit ug;
+        while (cursor_next<SK>(g, cur, ug)) {
             const Q8Problem &a = g.prob[ug.p];
             const int row = ug.n0 + lrow;
             const bool rowok = row < a.N;
@@ -435,7 +515,54 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
                     }
                 }
             }
-            if (a.S == 1) {
+            if constexpr (SK) {
+                if (ug.sb0 == 0 && ug.nsup == a.nsb) {
+                    if (ok && rowok) store_y(a, row, acc);
+                } else if (ug.sb0 > 0) {
+                    // a later part of a row block (the first piece of this CTA's range): the
+                    // partial rows go to the workspace for the CTA that holds the first part
+                    float4 *pp = reinterpret_cast<float4 *>(g.partials + (size_t(blockIdx.x) * kRows + lrow) * kNPad);
+#pragma unroll
+                    for (int q = 0; q < kNPad / 4; ++q)
+                        pp[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    named_bar_sync(1, 128);  // every row of the partial written
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        st_release_u32(g.flags + blockIdx.x, 1u);
+                    }
+                } else {
+                    // the first part of a row block that later CTAs continue (the last piece of
+                    // this CTA's range): y = p_0 + p_1 + ... in CTA order
+                    const int unit_end = a.sb_base + (ug.rb + 1) * a.nsb;
+                    float y[kNPad];
+#pragma unroll
+                    for (int m = 0; m < kNPad; ++m) y[m] = acc[m];
+                    int jend = blockIdx.x + 1;
+                    for (; jend < static_cast<int>(gridDim.x) && range_begin(jend, g.total_sb, gridDim.x) < unit_end;
+                         ++jend) {
+                        if (ok && !wait_flag(g.flags + jend, g.timeout_ns)) ok = false;
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) {
+                            if (lane == 0) atomicOr(g.status, kWsStatusTimeout);
+                            continue;
+                        }
+                        const float4 *pp =
+                            reinterpret_cast<const float4 *>(g.partials + (size_t(jend) * kRows + lrow) * kNPad);
+#pragma unroll
+                        for (int q = 0; q < kNPad / 4; ++q) {
+                            const float4 t = pp[q];
+                            y[4 * q] += t.x;
+                            y[4 * q + 1] += t.y;
+                            y[4 * q + 2] += t.z;
+                            y[4 * q + 3] += t.w;
+                        }
+                    }
+                    if (ok && rowok) store_y(a, row, y);
+                    named_bar_sync(1, 128);  // every row has read the partials
+                    if (threadIdx.x == 0 && ok)
+                        for (int j = blockIdx.x + 1; j < jend; ++j) g.flags[j] = 0u;  // ready for the next launch
+                }
+            } else if (a.S == 1) {
                 if (ok && rowok) store_y(a, row, acc);
             } else if (g.cluster) {
                 // Every CTA has one unit.  First barrier: every CTA of the cluster has finished
@@ -478,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         }
     }
     // cluster mode: the two barriers of the epilogue, for every other thread of the CTA
-    if (g.cluster && warp >= 4 && g.prob[unit_geometry(g, blockIdx.x).p].S > 1) {
+    if (!SK && g.cluster && warp >= 4 && g.prob[unit_geometry(g, blockIdx.x).p].S > 1) {
         cluster_sync_all();
         cluster_sync_all();
     }
@@ -496,8 +623,8 @@ struct Plan {
 dspark_status configure_kernel(int dev) {
     static int configured_dev = -1;
     if (configured_dev == dev) return DSPARK_OK;
-    const void *kerns[2] = {reinterpret_cast<const void *>(ws_q8_tc_kernel<1>),
-                            reinterpret_cast<const void *>(ws_q8_tc_kernel<kMaxProblems>)};
+    const void *kerns[2] = {reinterpret_cast<const void *>(ws_q8_tc_kernel<1, false>),
+                            reinterpret_cast<const void *>(ws_q8_tc_kernel<kMaxProblems, true>)};
     for (const void *kern : kerns) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kSmemBytes));
@@ -536,7 +663,7 @@ int cluster_capacity(int S) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, ws_q8_tc_kernel<1>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&c, ws_q8_tc_kernel<1, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         c = 0;
     }
@@ -631,15 +758,23 @@ dspark_status check_q8_problem(const dspark_ws_q8_problem &q, const char *what) 
     return DSPARK_OK;
 }
 
+// Workspace of a grouped launch: the status header, one flag per CTA and one partial row
+// block (128 rows x 16 fp32) per CTA, for at most `sms` CTAs.
+size_t flags_bytes(int sms) { return (size_t(sms) * 4 + 255) / 256 * 256; }
+size_t grouped_workspace_bytes(int sms) {
+    return kWsHeaderBytes + flags_bytes(sms) + size_t(sms) * kRows * kNPad * sizeof(float);
+}
+
 // One launch for n problems.  A single problem keeps its own plan: one unit per CTA in
 // clusters of S when it is split, else persistent CTAs walking the units.  Several problems
-// share one grid of one unit per CTA (as many waves as that takes), each with the split it
-// would get alone capped at kGroupMaxSplit, so that one cluster size (the largest split)
-// serves all of them; problems are padded to whole clusters and taken longest units first.
-// Wider clusters schedule worse in a grid of several waves (a new cluster needs that many free
-// SMs of one GPC at once): on the four Qwen3-8B projections, caps of 8 / 4 / 2 measured 55.3 /
-// 47.3 / 41.1 us, and no split with persistent CTAs 63.5 us.  A problem whose own split is at
-// most the cap gives the same bits alone and in a group.
+// run stream-K: their 128-row blocks, each over all of K, form one sequence of superblocks
+// that G = min(SMs, superblocks) co-resident CTAs (a cooperative launch) take in equal
+// contiguous ranges; a row block cut by a range boundary is finished by the CTA holding its
+// first superblocks, which adds the partial rows of the CTAs after it in CTA order.  Every
+// output is summed in one fixed order; a row block that no boundary cuts gives the same bits
+// as the same problem alone without a split.  (A grid of one unit per CTA in clusters of each
+// problem's split measured 41-55 us on the four Qwen3-8B projections, waves of CTAs starting
+// late and tails left alone.)
 dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *workspace, size_t workspace_bytes,
                                unsigned long long stall_ns, dspark_stream_t stream) {
     const char *what = n == 1 && probs ? "ws_matvec_q8" : "ws_matvec_q8_grouped";
@@ -661,6 +796,9 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != DSPARK_OK) return static_cast<dspark_status>(rc);
+    if (live > 1 && workspace_bytes < grouped_workspace_bytes(sms))
+        return fail(DSPARK_ERR_INVALID, "%s: workspace of %zu bytes < required %zu", what, workspace_bytes,
+                    grouped_workspace_bytes(sms));
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -672,37 +810,16 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
     g.status = static_cast<unsigned *>(workspace);
     g.timeout_ns = kDefaultTimeoutNs;
     g.stall_ns = stall_ns;
-    int order[kMaxProblems];
-    Plan plans[kMaxProblems];
-    int norder = 0;
-    for (int i = 0; i < n; ++i)
-        if (probs[i].M != 0 && probs[i].N != 0) {
-            plans[norder] = plan_for(probs[i].N, probs[i].K, sms);
-            if (live > 1) {  // grouped: one unit per CTA, the split capped
-                const int S = plans[norder].S < kGroupMaxSplit ? plans[norder].S : kGroupMaxSplit;
-                plans[norder].S = S;
-                plans[norder].cluster = S > 1;
-            }
-            order[norder++] = i;
-        }
-    auto unit_sup = [&](int j) { return (plans[j].nsb + plans[j].S - 1) / plans[j].S; };
-    int idx[kMaxProblems];
-    for (int j = 0; j < norder; ++j) idx[j] = j;
-    for (int x = 1; x < norder; ++x)  // stable insertion sort, longest units first
-        for (int y = x; y > 0 && unit_sup(idx[y]) > unit_sup(idx[y - 1]); --y) {
-            const int t = idx[y];
-            idx[y] = idx[y - 1];
-            idx[y - 1] = t;
-        }
-    int csize = 1;
-    for (int j = 0; j < norder; ++j) csize = plans[j].S > csize ? plans[j].S : csize;
-    g.csize = csize;
-    g.cluster = csize > 1 ? 1 : 0;
-    unsigned units = 0;
-    for (int oj = 0; oj < norder; ++oj) {
-        const int jj = idx[oj];
-        const dspark_ws_q8_problem &q = probs[order[jj]];
-        const Plan &p = plans[jj];
+    g.streamk = live > 1 ? 1 : 0;
+    g.total_sb = 0;
+    g.partials = nullptr;
+    g.flags = nullptr;
+    g.units = 0;
+    g.csize = 1;
+    g.cluster = 0;
+    for (int i = 0; i < n; ++i) {
+        const dspark_ws_q8_problem &q = probs[i];
+        if (q.M == 0 || q.N == 0) continue;
         const int j = g.nprob++;
         st = make_tmap_kblocks_u8(&g.tmQ[j], q.Wq, static_cast<uint64_t>(q.N), static_cast<uint64_t>(q.K), kRows, 1);
         if (st != DSPARK_OK) return st;
@@ -715,36 +832,58 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
         a.M = q.M;
         a.N = q.N;
         a.K = q.K;
-        a.nsb = p.nsb;
-        a.S = p.S;
-        a.nrb = p.nrb;
-        a.unit0 = static_cast<int>(units);
         a.mcols = q.M <= 8 ? 8 : 16;
-        // whole clusters per problem: the last one may hold padding units
-        const unsigned pu = static_cast<unsigned>(p.nrb) * static_cast<unsigned>(p.S);
-        units += (pu + static_cast<unsigned>(csize) - 1) / static_cast<unsigned>(csize) * static_cast<unsigned>(csize);
+        a.unit0 = 0;
+        a.sb_base = g.total_sb;
+        if (g.streamk) {
+            a.nrb = (q.N + kRows - 1) / kRows;
+            a.nsb = q.K / (kKS * kSuper);
+            a.S = 1;
+            g.total_sb += a.nrb * a.nsb;
+        } else {
+            const Plan p = plan_for(q.N, q.K, sms);
+            a.nrb = p.nrb;
+            a.nsb = p.nsb;
+            a.S = p.S;
+            g.units = p.nrb * p.S;
+            g.csize = p.cluster ? p.S : 1;
+            g.cluster = p.cluster ? 1 : 0;
+        }
     }
-    g.units = static_cast<int>(units);
-
-    // one problem unsplit: persistent CTAs (at most one per SM); otherwise one unit per CTA
-    const unsigned grid =
-        (live == 1 && csize == 1) ? (units < static_cast<unsigned>(sms) ? units : static_cast<unsigned>(sms)) : units;
+    unsigned grid;
+    if (g.streamk) {
+        grid = static_cast<unsigned>(g.total_sb < sms ? g.total_sb : sms);
+        unsigned char *ws = static_cast<unsigned char *>(workspace);
+        g.flags = reinterpret_cast<unsigned *>(ws + kWsHeaderBytes);
+        g.partials = reinterpret_cast<float *>(ws + kWsHeaderBytes + flags_bytes(sms));
+    } else {
+        // split: one unit per CTA in clusters of S; unsplit: persistent CTAs (at most one per SM)
+        grid = g.cluster ? static_cast<unsigned>(g.units)
+                         : static_cast<unsigned>(g.units < sms ? g.units : sms);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (csize > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
+    if (g.streamk) {
+        // a CTA waits for the CTAs after it: all of them must be resident at once
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.numAttrs = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+        if (g.cluster) {
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = static_cast<unsigned>(g.csize);
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        }
     }
     if (g.nprob == 1) {  // the small parameter block
         Q8GroupT<1> g1;
@@ -752,15 +891,19 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
         g1.units = g.units;
         g1.cluster = g.cluster;
         g1.csize = g.csize;
+        g1.streamk = g.streamk;
+        g1.total_sb = g.total_sb;
+        g1.partials = g.partials;
+        g1.flags = g.flags;
         g1.status = g.status;
         g1.timeout_ns = g.timeout_ns;
         g1.stall_ns = g.stall_ns;
         g1.prob[0] = g.prob[0];
         g1.tmQ[0] = g.tmQ[0];
         g1.tmX[0] = g.tmX[0];
-        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<1>, g1);
+        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<1, false>, g1);
     } else {
-        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<kMaxProblems>, g);
+        e = cudaLaunchKernelEx(&cfg, ws_q8_tc_kernel<kMaxProblems, true>, g);
     }
     if (e != cudaSuccess) return cuda_fail(e, "ws_matvec_q8 launch");
     return DSPARK_OK;
@@ -784,7 +927,9 @@ extern "C" dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *W
 extern "C" size_t dspark_ws_matvec_q8_grouped_workspace_bytes(const dspark_ws_q8_problem *problems, int n_problems) {
     (void)problems;
     (void)n_problems;
-    return dspark::kWsHeaderBytes;  // the status word
+    int sms = 0;
+    if (dspark::current_sm_count(&sms) != DSPARK_OK) return 0;
+    return grouped_workspace_bytes(sms);
 }
 
 extern "C" dspark_status dspark_ws_matvec_q8_grouped(const dspark_ws_q8_problem *problems, int n_problems,

@@ -338,14 +338,21 @@ dspark_status dspark_ws_matvec_q8(const int8_t *Wq, const uint16_t *Wd, const ui
                                   size_t workspace_bytes, dspark_stream_t stream);
 
 /* Grouped form: up to 8 independent Q8_0 problems in one launch (e.g. the four projections
- * of a layer), so the fixed launch and pipeline costs are paid once and the SMs left idle by
- * one problem take the next one's work.  Each problem has the arguments and limits of
- * dspark_ws_matvec_q8.  Each problem keeps the K split it gets alone, capped at 2 (so that
- * clusters of at most 2 CTAs serve them all); a problem whose own split is 1 or 2 gets
- * results bit-identical to a separate dspark_ws_matvec_q8 call, any other still sums in one
- * fixed order.  The grid holds one 128-row unit per CTA, in as many waves as that takes.  Problems with M == 0 or N == 0 are
- * skipped.  The workspace (dspark_ws_matvec_q8_grouped_workspace_bytes, 256, zero-filled
- * before first use) holds the status word.  More than 8 problems: DSPARK_ERR_UNSUPPORTED. */
+ * of a layer), so the fixed launch and pipeline costs are paid once and no SM idles while
+ * another finishes a long row block.  Each problem has the arguments and limits of
+ * dspark_ws_matvec_q8.  The 128-row blocks of all problems, each over all of K, form one
+ * sequence of 256-k superblocks that min(SMs, superblocks) co-resident CTAs (a cooperative
+ * launch) take in equal contiguous ranges (stream-K); a row block cut by a range boundary is
+ * finished by the CTA holding its first superblocks, which adds the partial sums of the CTAs
+ * after it in CTA order.  Every output is summed in one fixed order, so results are
+ * deterministic; they can differ in the last bits from a separate dspark_ws_matvec_q8 call,
+ * which splits K differently.  Problems with M == 0 or N == 0 are skipped; with only one
+ * problem left the call is a dspark_ws_matvec_q8 call.  The workspace
+ * (dspark_ws_matvec_q8_grouped_workspace_bytes on the device that runs the call: a status
+ * word, one flag and 8 KB of partial sums per SM) must be zero-filled before its first use;
+ * the kernel leaves the flags zero again, except after a wait that gave up
+ * (DSPARK_ERR_TIMEOUT), after which the workspace must be zero-filled again.  More than 8
+ * problems: DSPARK_ERR_UNSUPPORTED. */
 typedef struct dspark_ws_q8_problem {
     const int8_t *Wq;    /* int8 [N, K] (dspark_q8_0_repack), 16-byte aligned */
     const uint16_t *Wd;  /* fp16 [N, K/32] scales, 16-byte aligned */

@@ -319,7 +319,9 @@ def test_ws_q8_grouped_validation(dspark_lib):
     arr[0] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 256)
     assert g(p, 1, NULL, 1 << 20, NULL) == INVALID
     assert g(p, 1, FAKE, 16, NULL) == INVALID
-    assert lib.dspark_ws_matvec_q8_grouped_workspace_bytes(p, 2) == 256
+    # status word, one flag and one partial row block per SM (0 without a device)
+    n = lib.dspark_ws_matvec_q8_grouped_workspace_bytes(p, 2)
+    assert n == 0 or n >= 256 + 256 + 8192
 
 
 def test_ws_grouped_host_validation(dspark_lib):

@@ -151,23 +151,21 @@ def _grouped(inps, fp32_flags):
 
 
 def test_grouped_qwen3_8b_shapes():
-    """The four projections in one launch, within tolerance of the oracle; the 4096 -> 12288
-    projection (not split alone) bit-identical to its own call."""
+    """The four projections in one launch (stream-K over all their row blocks), within
+    tolerance of the oracle, the fp16 outputs the rounding of the fp32 ones."""
     inps = [synth.ws_q8_inputs(7, N, K, seed=K + N) for (K, N) in synth.WS_SHAPES]
     g32 = _grouped(inps, [True] * 4)
     g16 = _grouped(inps, [False] * 4)
-    for (K, N), inp, a32, a16 in zip(synth.WS_SHAPES, inps, g32, g16):
+    for inp, a32, a16 in zip(inps, g32, g16):
         parity.check_ws_q8(inp, y32=a32, y16=a16)
-        if (K, N) == (4096, 12288):
-            y32, y16 = _run(inp)
-            np.testing.assert_array_equal(a32.view(np.uint32), y32.view(np.uint32))
-            np.testing.assert_array_equal(a16, y16)
 
 
 @pytest.mark.parametrize("shapes", [
     [(1, 40000, 512), (16, 300, 2304), (3, 1, 256)],                  # one problem wider than the SMs
-    [(7, 1000, 4096), (2, 153, 12288), (9, 5000, 256), (4, 64, 1024)],  # splits 1 .. 8 alone, capped at 2
-    [(5, 777, 6400), (8, 128, 768)],                                    # K of 25 and 3 superblocks
+    [(7, 1000, 4096), (2, 153, 12288), (9, 5000, 256), (4, 64, 1024)],  # row blocks of 1 .. 48 superblocks
+    [(5, 777, 6400), (8, 128, 768)],                                    # 178 superblocks
+    [(3, 300, 512), (2, 200, 256)],                                     # 8 superblocks: 8 CTAs
+    [(2, 128, 16384), (1, 128, 256)],                                   # one row block over 64 CTAs
 ])
 def test_grouped_ragged_mixed(shapes):
     inps = [synth.ws_q8_inputs(M, N, K, seed=M + N + K) for (M, N, K) in shapes]
