@@ -154,6 +154,26 @@ def test_cluster_kernel_batch_invariance_bitwise():
                                       full["logits"][r].view(np.uint32))
 
 
+def test_cluster_kernel_in_a_graph_plan():
+    """The single-cluster kernel recorded in a CUDA graph: replays match a direct call and
+    continue the chain from the prev they leave on the device."""
+    inp = synth.markov_config("tiny")
+    assert api.markov_kernel_for(1, 4, 4096, 64) == "cluster"
+    direct = parity.gpu_markov(inp, dbg=False)
+    t = parity.markov_to_device(inp)
+    plan = api.MarkovPlan(t["base"], t["w1"], t["w2"], t["d2t"], t["prev"])
+    for _ in range(3):
+        t["prev"].copy_(torch.from_numpy(inp["prev0"]))
+        out = plan.launch()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy(), direct["out_ids"])
+        assert api.markov_status(plan.workspace) == 0
+    second = plan.launch().cpu().numpy()
+    o = parity.oracle.markov_draft(inp["base"], inp["w1"], inp["w2"], None, direct["prev"])
+    np.testing.assert_array_equal(second, o["out_ids"])
+    plan.close()
+
+
 def test_cluster_kernel_resets_the_status_word():
     """A grid-kernel draft that timed out leaves DSPARK_ERR_TIMEOUT in the workspace; the
     next draft on the same workspace through the cluster kernel reports its own status."""

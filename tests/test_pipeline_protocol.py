@@ -1,4 +1,5 @@
-"""The mbarrier protocol of the Q8_0 weight-stationary kernel, model-checked on the host.
+"""The mbarrier protocols of the Q8_0 weight-stationary kernel, the grid Markov kernel and
+the single-cluster Markov kernel's exchange, model-checked on the host.
 
 The kernel's roles wait on mbarriers by phase parity: a wait for the k-th completion of a
 barrier passes as soon as the number of completed phases c has the other parity than k,
@@ -362,3 +363,111 @@ def test_markov_model_catches_a_slot_freed_by_the_mma_alone():
     rng = random.Random(7)
     assert any(run_markov(3, 4, 6, rng, epilogue_holds_slot=False) for _ in range(300))
     assert min(markov_slots(r, nb) for r in (64, 128, 256) for nb in (1, 2, 4, 8)) >= 3
+
+
+# ---- the single-cluster Markov kernel's exchange (csrc/markov_cluster.cu) ----------------
+# Every CTA sends, per position, its message to every CTA of the cluster (itself included)
+# with stores whose bytes complete on the receiver's inbox barrier for that position's parity;
+# a CTA waits only for its own inbox (parity wait), reads it, re-arms that barrier for the
+# position two ahead (arrive.expect_tx), and only then sends the next position.  The barriers
+# of positions 0 and 1 are armed before any CTA sends.  The model delivers each message at a
+# random later moment and checks that every delivery lands on an armed phase of the right
+# position, that every wait that passes sees exactly its phase, and that a CTA reads its
+# whole inbox of the position it waited for.
+
+class ArmedBarrier:
+    """mbarrier of arrival count 1 with a transaction count."""
+
+    def __init__(self):
+        self.completed = 0  # completed phases
+        self.pending = 1    # arrivals still expected in the current phase
+        self.tx = 0         # transaction bytes still expected (may run ahead of the arm)
+
+    def arrive_expect(self, n):
+        self.pending -= 1
+        self.tx += n
+        self._maybe_complete()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.completed += 1
+            self.pending = 1
+
+
+def run_cluster_exchange(C, k, rng, nbuf=2):
+    bars = [[ArmedBarrier() for _ in range(nbuf)] for _ in range(C)]
+    inbox = [[[None] * C for _ in range(nbuf)] for _ in range(C)]
+    for r in range(C):  # armed before the first cluster barrier
+        for p in range(min(k, nbuf)):
+            bars[r][p % nbuf].arrive_expect(C)
+    pos = [0] * C
+    state = ["send"] * C  # send -> wait -> read -> (next position)
+    in_flight = []        # (sender, receiver, position)
+    error = None
+    while True:
+        actions = [("cta", c) for c in range(C) if pos[c] < k]
+        actions += [("deliver", j) for j in range(len(in_flight))]
+        if not actions:
+            break
+        enabled = []
+        for kind, x in actions:
+            if kind == "deliver":
+                enabled.append((kind, x))
+                continue
+            c = x
+            if state[c] == "wait":
+                i = pos[c]
+                b = bars[c][i % nbuf]
+                if (b.completed & 1) == ((i // nbuf) & 1):
+                    continue  # the parity wait does not pass yet
+            enabled.append((kind, x))
+        if not enabled:
+            return "deadlock"
+        kind, x = rng.choice(enabled)
+        if kind == "deliver":
+            s, r, p = in_flight.pop(x)
+            b = bars[r][p % nbuf]
+            if (b.completed != p // nbuf or b.pending != 0) and error is None:
+                error = f"message of position {p} from CTA {s} landed on phase {b.completed} (armed: {b.pending == 0})"
+            inbox[r][p % nbuf][s] = p
+            b.complete_tx(1)
+            continue
+        c = x
+        i = pos[c]
+        if state[c] == "send":
+            in_flight += [(c, r, i) for r in range(C)]
+            state[c] = "wait"
+        elif state[c] == "wait":
+            b = bars[c][i % nbuf]
+            if b.completed != i // nbuf + 1 and error is None:
+                error = f"CTA {c} passed its wait of position {i} with {b.completed} completed phases"
+            state[c] = "read"
+        else:
+            if any(inbox[c][i % nbuf][s] != i for s in range(C)) and error is None:
+                error = f"CTA {c} read an incomplete inbox at position {i}: {inbox[c][i % nbuf]}"
+            if i + nbuf < k:
+                bars[c][i % nbuf].arrive_expect(C)
+            pos[c] += 1
+            state[c] = "send"
+        if error:
+            return error
+    return error
+
+
+@pytest.mark.parametrize("C,k", [(2, 6), (4, 9), (16, 5)])
+def test_cluster_exchange_protocol_is_exact_under_random_interleavings(C, k):
+    rng = random.Random(C * 100 + k)
+    for _ in range(200):
+        assert run_cluster_exchange(C, k, rng) is None
+
+
+def test_cluster_exchange_model_catches_a_single_inbox():
+    """With one inbox (and one barrier) a fast CTA's next message can land on the phase a slow
+    CTA is still collecting; the model must find such an interleaving."""
+    rng = random.Random(7)
+    found = any(run_cluster_exchange(3, 6, rng, nbuf=1) is not None for _ in range(300))
+    assert found
