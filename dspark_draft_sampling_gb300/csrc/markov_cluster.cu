@@ -269,6 +269,11 @@ __global__ void __launch_bounds__(kThreadsC, 1)
     const int items = a.B * (cpr + 1);          // 16-byte pieces of one message: key + row chunks
     int pg = kThreadsC / items;                 // peer groups: threads that send the same piece
     pg = pg < 1 ? 1 : (pg > C ? C : pg);
+    // this thread's first piece (the same at every position): peer group, request, chunk
+    // (chunk cpr is the key), and the piece's offset within one message
+    const int q0g = tid / items;
+    const int q0r = (tid - q0g * items) / (cpr + 1);
+    const int q0c = tid - q0g * items - q0r * (cpr + 1);
     for (int i = 0; i < a.k; ++i) {
         const int par = i & 1;
         const int b = i % nbuf;
@@ -321,10 +326,13 @@ __global__ void __launch_bounds__(kThreadsC, 1)
         // CTA of the cluster (this one included), straight from registers
         if (!gave_up) {
             for (int q = tid; q < items * pg; q += kThreadsC) {
-                const int g = q / items;
-                const int it = q - g * items;
-                const int r = it / (cpr + 1);
-                const int c = it - r * (cpr + 1);  // cpr: the key
+                int g = q0g, r = q0r, c = q0c;
+                if (q != tid) {  // more pieces than threads: only with many requests and rank 256
+                    g = q / items;
+                    const int it = q - g * items;
+                    r = it / (cpr + 1);
+                    c = it - r * (cpr + 1);
+                }
                 unsigned long long kc = wk[r];
 #pragma unroll
                 for (int w = 1; w < kWarpsC; ++w) {
@@ -355,45 +363,37 @@ __global__ void __launch_bounds__(kThreadsC, 1)
             bool ok = !gave_up;
             if (ok && !mbar_wait(&bar_in[par], static_cast<uint32_t>((i >> 1) & 1), a.timeout_ns)) ok = false;
             ok = __all_sync(0xffffffffu, ok);
-            // Winners: the lanes in groups of 16, one sender per lane and two requests per
-            // pass; lane r < num_reqs ends up with the sender of request r's winner.
-            int src = -1;
-            for (int r0 = 0; r0 < a.B; r0 += 2) {
-                const int r = r0 + (lane >> 4);
-                const int sdr = lane & 15;
-                unsigned long long kv = 0ull;
-                if (ok && r < a.B && sdr < C) {
-                    const uint2 k2 =
-                        *reinterpret_cast<const uint2 *>(inbox + ((size_t(par) * C + sdr) * NB + r) * L.msg);
-                    kv = (static_cast<unsigned long long>(k2.y) << 32) | k2.x;
-                }
-                unsigned long long m = kv;
+            // Winners: per request, lane l < C holds sender l's key; the warp max is the
+            // winner, the lane holding it its sender.
+            int src_of[NB];
 #pragma unroll
-                for (int off = 8; off >= 1; off >>= 1) {
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, off);
-                    m = o > m ? o : m;
+            for (int r = 0; r < NB; ++r) {
+                src_of[r] = -1;
+                if (r < a.B) {
+                    unsigned long long kv = 0ull;
+                    if (ok && lane < C) {
+                        const uint2 k2 =
+                            *reinterpret_cast<const uint2 *>(inbox + ((size_t(par) * C + lane) * NB + r) * L.msg);
+                        kv = (static_cast<unsigned long long>(k2.y) << 32) | k2.x;
+                    }
+                    const unsigned long long best = warp_max_u64(kv);
+                    const unsigned hold = __ballot_sync(0xffffffffu, best != 0ull && kv == best);
+                    const bool has = ok && ((live >> r) & 1u) && best != 0ull;
+                    if (has) src_of[r] = __ffs(hold) - 1;
+                    if (warp == 0 && lane == 0) s_ids[i * kMaxReqs + r] = has ? static_cast<int>(argmax_key_index(best)) : -1;
                 }
-                const unsigned hold = __ballot_sync(0xffffffffu, kv != 0ull && kv == m);
-                int s_here = -1;
-                if (sdr == 0 && r < a.B) {
-                    const bool has = ok && ((live >> r) & 1u) && m != 0ull;
-                    if (has) s_here = __ffs((hold >> (lane & 16)) & 0xffffu) - 1;
-                    if (warp == 0) s_ids[i * kMaxReqs + r] = has ? static_cast<int>(argmax_key_index(m)) : -1;
-                }
-                const int s0 = __shfl_sync(0xffffffffu, s_here, 0);
-                const int s1 = __shfl_sync(0xffffffffu, s_here, 16);
-                if (lane == r0) src = s0;
-                if (lane == r0 + 1) src = s1;
             }
             if (ok) done = i + 1;
             if (ok && i + 1 < a.k) {
                 const int n = a.B * cpr;
-                for (int q0 = 0; q0 < n; q0 += 32) {  // uniform trip count: the shuffle below
-                    const int q = q0 + lane;
-                    const int r = (q < n ? q : n - 1) / cpr;
+                for (int q = lane; q < n; q += 32) {
+                    const int r = q / cpr;
                     const int c = q - r * cpr;
-                    const int sr = __shfl_sync(0xffffffffu, src, r);
-                    if (q < n) {
+                    int sr = -1;
+#pragma unroll
+                    for (int rr = 0; rr < NB; ++rr)
+                        if (rr == r) sr = src_of[rr];
+                    {
                         uint4 v = make_uint4(0u, 0u, 0u, 0u);
                         if (sr >= 0)
                             v = *reinterpret_cast<const uint4 *>(inbox + ((size_t(par) * C + sr) * NB + r) * L.msg +
