@@ -848,7 +848,8 @@ def markov_roofline(B, mb, t_s, peak, peak_kind, ceil):
 def run_one_kernel(name: str) -> int:
     """Runs one kernel of the workload twice on cuda:0 and exits, for a profiler capture of a
     single launch (`ncu -k ... -s 1 -c 1`): `ws_4096x4096` (the fp16 weight-stationary matvec,
-    M = 7), `probe_2048` (the batched confidence probe), `q8_lm_head` (the Q8_0 matvec,
+    M = 7), `ws_grouped_qwen3_8b` (the four fp16 projections in one launch), `probe_2048` (the
+    batched confidence probe), `q8_lm_head` (the Q8_0 matvec,
     4096 -> 151936, M = 7), `q8_grouped_qwen3_8b` (the four Q8_0 projections in one launch),
     `markov_tiny` (the tiny Markov lane on the single-cluster kernel).  No timing is taken."""
     import torch
@@ -880,6 +881,16 @@ def run_one_kernel(name: str) -> int:
             probs.append((q, d, X, torch.empty((7, N), dtype=torch.float16, device=dev)))
         wsg = api.new_ws_q8_grouped_workspace(dev)
         call = lambda: api.ws_matvec_q8_grouped(probs, workspace=wsg)
+    elif name == "ws_grouped_qwen3_8b":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        probs = []
+        for (K, N) in synth.WS_SHAPES:
+            W = (torch.randn((N, K), generator=gen, device=dev) * 0.02).half()
+            X = torch.randn((7, K), generator=gen, device=dev).half()
+            probs.append((W, X, torch.empty((7, N), dtype=torch.float16, device=dev)))
+        wsg = torch.zeros(api.ws_matvec_grouped_workspace_bytes(probs), dtype=torch.uint8, device=dev)
+        call = lambda: api.ws_matvec_grouped(probs, workspace=wsg)
     elif name == "markov_tiny":
         mk = synth.markov_config("tiny")
         base = torch.from_numpy(mk["base"]).to(dev)
@@ -926,8 +937,8 @@ def main():
                     help="skip the separately timed rows beyond the headline step")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration sweep (median/p10/p90, cold and warm L2)")
-    ap.add_argument("--kernel", choices=["ws_4096x4096", "probe_2048", "q8_lm_head", "q8_grouped_qwen3_8b",
-                                         "markov_tiny"],
+    ap.add_argument("--kernel", choices=["ws_4096x4096", "ws_grouped_qwen3_8b", "probe_2048", "q8_lm_head",
+                                         "q8_grouped_qwen3_8b", "markov_tiny"],
                     help="run only this kernel of the workload twice, untimed (for a profiler)")
     args = ap.parse_args()
     if args.kernel:

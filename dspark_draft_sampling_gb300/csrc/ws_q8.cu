@@ -237,21 +237,6 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Waits (bounded) until *flag is non-zero; false if the limit ran out.
-__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned long long timeout_ns) {
-    if (ld_acquire_u32(flag) != 0u) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire_u32(flag) == 0u) {
-        if (global_timer_ns() - t0 > timeout_ns) return false;
-        __nanosleep(64);
-    }
-    return true;
-}
-
 __device__ __forceinline__ void store_y(const Q8Problem &a, int row, const float (&y)[kNPad]) {
 #pragma unroll
     for (int m = 0; m < kNPad; ++m) {
@@ -320,8 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         }
     };
     if (warp == kTmaWarp && lane == 0) {
-        // The producer sets up the barriers and issues the first ring's worth of stages before
-        // the CTA-wide set-up (TMEM allocation, the CTA barrier), so their DRAM latency overlaps it.
+        // The producer sets up the barriers and issues the first stages before the CTA-wide
+        // set-up (TMEM allocation, the CTA barrier), so their DRAM latency overlaps it.  Two
+        // only: each stage takes the producing thread ~0.2 us to issue, and a whole ring issued
+        // here held the converters and MMAs back (single calls 0.6-1.7 us slower).
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_r[s], 1);
             mbar_init(&done[s], 1);
@@ -334,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         pdl_wait();  // no global-memory access before this point
         pol_q = l2_policy_evict_first();
         pol_x = l2_policy_evict_last();
-        produce(kStages);
+        produce(2);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
