@@ -119,8 +119,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // Workspace of the weight-stationary matvecs (fp16 and Q8_0): a status word in a 256-byte
-// header; the grouped Q8_0 launch (stream-K) adds one flag and one partial row block per CTA
-// after it.
+// header (split-K partial sums are reduced in distributed shared memory, not here).
 constexpr size_t kWsHeaderBytes = 256;
 constexpr unsigned kWsStatusTimeout = 1u;
 
@@ -133,21 +132,6 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Waits (bounded) until *flag is non-zero; false if the limit ran out.
-__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned long long timeout_ns) {
-    if (ld_acquire_u32(flag) != 0u) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire_u32(flag) == 0u) {
-        if (global_timer_ns() - t0 > timeout_ns) return false;
-        __nanosleep(64);
-    }
-    return true;
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {

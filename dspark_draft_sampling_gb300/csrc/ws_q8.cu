@@ -237,6 +237,21 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (bounded) until *flag is non-zero; false if the limit ran out.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned long long timeout_ns) {
+    if (ld_acquire_u32(flag) != 0u) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (ld_acquire_u32(flag) == 0u) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void store_y(const Q8Problem &a, int row, const float (&y)[kNPad]) {
 #pragma unroll
     for (int m = 0; m < kNPad; ++m) {
