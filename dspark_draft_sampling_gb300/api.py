@@ -67,6 +67,7 @@ SIGNATURES = {
     "dspark_ws_matvec_q8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "dspark_ws_matvec_q8_grouped_workspace_bytes": (_Z, [_P, _I]),
     "dspark_ws_matvec_q8_grouped": (_I, [_P, _I, _P, _Z, _P]),
+    "dspark_ws_matvec_q8_grouped_debug": (_I, [_P, _I, _P, _Z, _I, _U, _P]),
 }
 
 _lock = threading.Lock()
@@ -511,11 +512,7 @@ def new_ws_q8_grouped_workspace(device=None):
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
-    """Several independent Y = X dequant(W)^T in one launch.  problems: list of (Wq int8
-    [N,K], Wd fp16 bits [N,K/32], X fp16 [M,K], Y [M,N] fp16 or fp32) device tensors; Y is
-    written in place."""
-    lib = load_library()
+def _ws_q8_problems(problems):
     arr = (WsQ8Problem * len(problems))()
     for i, (Wq, Wd, X, Y) in enumerate(problems):
         N, K = Wq.shape
@@ -526,12 +523,31 @@ def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
                              _ptr(X, "X", itemsize=2, dtypes=_BITS16),
                              _ptr(Y, "Y", dtypes=(torch.float16, torch.float32)),
                              1 if Y.dtype == torch.float32 else 0, M, N, K)
+    return arr
+
+
+def ws_matvec_q8_grouped(problems, *, workspace=None, stream=None):
+    """Several independent Y = X dequant(W)^T in one launch.  problems: list of (Wq int8
+    [N,K], Wd fp16 bits [N,K/32], X fp16 [M,K], Y [M,N] fp16 or fp32) device tensors; Y is
+    written in place."""
+    lib = load_library()
+    arr = _ws_q8_problems(problems)
     if workspace is None:
         workspace = new_ws_q8_grouped_workspace(problems[0][0].device)
     st = lib.dspark_ws_matvec_q8_grouped(ctypes.cast(arr, ctypes.c_void_p), len(arr), _ptr(workspace, "workspace"),
                                          workspace.numel(), _stream(stream))
     _check(lib, st)
     return [p[3] for p in problems]
+
+
+def ws_matvec_q8_grouped_debug(problems, workspace, *, withheld_cta: int, timeout_us: int, stream=None):
+    """Fault-injection hook: see dspark_ws_matvec_q8_grouped_debug in dspark.h."""
+    lib = load_library()
+    arr = _ws_q8_problems(problems)
+    st = lib.dspark_ws_matvec_q8_grouped_debug(ctypes.cast(arr, ctypes.c_void_p), len(arr),
+                                               _ptr(workspace, "workspace"), workspace.numel(), int(withheld_cta),
+                                               int(timeout_us), _stream(stream))
+    _check(lib, st)
 
 
 # ---- host-buffer forms: per-call inputs and outputs in (pinned) host memory ----

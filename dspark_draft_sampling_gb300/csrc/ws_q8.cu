@@ -129,6 +129,8 @@ struct Q8GroupT {
     int total_sb;
     float *partials;   // [grid][128][16] fp32
     unsigned *flags;   // [grid]: 1 while partials[c] holds a row block's later part
+    int withheld_flag;  // fault-injection hook only (else -1): this CTA writes its partial but
+                        // never sets its flag, so the CTA finishing that row block gives up
 };
 
 struct Unit {
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
                     for (int q = 0; q < kNPad / 4; ++q)
                         pp[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                     named_bar_sync(1, 128);  // every row of the partial written
-                    if (threadIdx.x == 0) {
+                    if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) != g.withheld_flag) {
                         __threadfence();
                         st_release_u32(g.flags + blockIdx.x, 1u);
                     }
@@ -778,7 +780,8 @@ size_t grouped_workspace_bytes(int sms) {
 // problem's split measured 41-55 us on the four Qwen3-8B projections, waves of CTAs starting
 // late and tails left alone.)
 dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *workspace, size_t workspace_bytes,
-                               unsigned long long stall_ns, dspark_stream_t stream) {
+                               unsigned long long stall_ns, dspark_stream_t stream, int withheld_flag = -1,
+                               unsigned long long timeout_ns = kDefaultTimeoutNs) {
     const char *what = n == 1 && probs ? "ws_matvec_q8" : "ws_matvec_q8_grouped";
     clear_error();
     if (n < 0 || n > kMaxProblems) return fail(DSPARK_ERR_UNSUPPORTED, "%s: %d problems (at most %d)", what, n, kMaxProblems);
@@ -810,12 +813,13 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
     Q8GroupT<kMaxProblems> g;
     g.nprob = 0;
     g.status = static_cast<unsigned *>(workspace);
-    g.timeout_ns = kDefaultTimeoutNs;
+    g.timeout_ns = timeout_ns;
     g.stall_ns = stall_ns;
     g.streamk = live > 1 ? 1 : 0;
     g.total_sb = 0;
     g.partials = nullptr;
     g.flags = nullptr;
+    g.withheld_flag = withheld_flag;
     g.units = 0;
     g.csize = 1;
     g.cluster = 0;
@@ -897,6 +901,7 @@ dspark_status q8_enqueue_group(const dspark_ws_q8_problem *probs, int n, void *w
         g1.total_sb = g.total_sb;
         g1.partials = g.partials;
         g1.flags = g.flags;
+        g1.withheld_flag = -1;
         g1.status = g.status;
         g1.timeout_ns = g.timeout_ns;
         g1.stall_ns = g.stall_ns;
@@ -937,6 +942,20 @@ extern "C" size_t dspark_ws_matvec_q8_grouped_workspace_bytes(const dspark_ws_q8
 extern "C" dspark_status dspark_ws_matvec_q8_grouped(const dspark_ws_q8_problem *problems, int n_problems,
                                                      void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
     return q8_enqueue_group(problems, n_problems, workspace, workspace_bytes, 0ull, stream);
+}
+
+extern "C" dspark_status dspark_ws_matvec_q8_grouped_debug(const dspark_ws_q8_problem *problems, int n_problems,
+                                                           void *workspace, size_t workspace_bytes, int withheld_cta,
+                                                           unsigned timeout_us, dspark_stream_t stream) {
+    using namespace dspark;
+    if (timeout_us == 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8_grouped_debug: timeout_us must be > 0");
+    if (withheld_cta < 0) return fail(DSPARK_ERR_INVALID, "ws_matvec_q8_grouped_debug: withheld_cta must be >= 0");
+    int live = 0;
+    for (int i = 0; problems && i < n_problems; ++i) live += (problems[i].M != 0 && problems[i].N != 0) ? 1 : 0;
+    if (live < 2)
+        return fail(DSPARK_ERR_INVALID, "ws_matvec_q8_grouped_debug: needs at least two non-empty problems");
+    return q8_enqueue_group(problems, n_problems, workspace, workspace_bytes, 0ull, stream, withheld_cta,
+                            1000ull * timeout_us);
 }
 
 extern "C" dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X, void *Y,

@@ -368,6 +368,19 @@ dspark_status dspark_ws_matvec_q8_grouped(const dspark_ws_q8_problem *problems, 
                                           void *workspace, size_t workspace_bytes,
                                           dspark_stream_t stream);
 
+/* Fault-injection hook for testing the grouped launch's wait on another CTA: the same launch
+ * as dspark_ws_matvec_q8_grouped (at least two non-empty problems, else DSPARK_ERR_INVALID),
+ * except that every wait of the kernel gives up after `timeout_us` microseconds instead of
+ * 2 s, and CTA `withheld_cta` writes its partial sums but never sets its flag.  If that
+ * CTA's range starts inside a row block, the CTA finishing the row block waits for the flag,
+ * gives up, skips that row block's outputs and records DSPARK_ERR_TIMEOUT in the workspace
+ * status word (dspark_ws_matvec_status); the workspace must then be zero-filled again.  Any
+ * other CTA number gives the ordinary result.  Not for production use. */
+dspark_status dspark_ws_matvec_q8_grouped_debug(const dspark_ws_q8_problem *problems, int n_problems,
+                                                void *workspace, size_t workspace_bytes,
+                                                int withheld_cta, unsigned timeout_us,
+                                                dspark_stream_t stream);
+
 /* As dspark_ws_matvec_debug, for the Q8_0 matvec (status read by dspark_ws_matvec_status). */
 dspark_status dspark_ws_matvec_q8_debug(const int8_t *Wq, const uint16_t *Wd, const uint16_t *X,
                                         void *Y, int y_is_fp32, int M, int N, int K,

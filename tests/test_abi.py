@@ -322,6 +322,14 @@ def test_ws_q8_grouped_validation(dspark_lib):
     # status word, one flag and one partial row block per SM (0 without a device)
     n = lib.dspark_ws_matvec_q8_grouped_workspace_bytes(p, 2)
     assert n == 0 or n >= 256 + 256 + 8192
+    # the fault-injection hook: a wait limit, a CTA number and two non-empty problems
+    d = lib.dspark_ws_matvec_q8_grouped_debug
+    arr[1] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 7, 64, 256)
+    assert d(p, 2, FAKE, 1 << 20, 1, 0, NULL) == INVALID
+    assert d(p, 2, FAKE, 1 << 20, -1, 100, NULL) == INVALID
+    assert d(p, 1, FAKE, 1 << 20, 1, 100, NULL) == INVALID
+    arr[1] = P(FAKE.value, FAKE.value, FAKE.value, FAKE.value, 0, 0, 64, 256)
+    assert d(p, 2, FAKE, 1 << 20, 1, 100, NULL) == INVALID
 
 
 def test_ws_grouped_host_validation(dspark_lib):

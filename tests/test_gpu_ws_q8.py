@@ -193,3 +193,48 @@ def test_grouped_skips_empty_problems_and_repeats_bitwise():
     y32, _ = _run(inps[0])
     np.testing.assert_array_equal(Y.cpu().numpy().view(np.uint32), y32.view(np.uint32))
     parity.check_ws_q8(inps[0], y32=a[0])
+
+
+def test_grouped_wait_for_a_withheld_partial_gives_up():
+    """Failure detection without a fault: one CTA of the stream-K launch writes its partial
+    sums but never sets its flag; the CTA finishing that row block waits 2 ms, gives up,
+    leaves the row block's outputs alone and records DSPARK_ERR_TIMEOUT.  Every other output
+    is right, and after the workspace is zero-filled again the next launch is whole."""
+    from tests.test_streamk_partition import pieces_of, range_begin, superblock_k
+
+    inps = [synth.ws_q8_inputs(7, N, K, seed=K + N) for (K, N) in synth.WS_SHAPES]
+    sk = superblock_k()
+    problems, total = [], 0
+    for inp in inps:
+        nrb, nsb = -(-inp["N"] // 128), inp["K"] // sk
+        problems.append(dict(nrb=nrb, nsb=nsb, sb_base=total))
+        total += nrb * nsb
+    G = min(torch.cuda.get_device_properties(0).multi_processor_count, total)
+    # a CTA whose range starts inside a row block: its first piece is a later part
+    c = next(c for c in range(1, G) if pieces_of(c, problems, total, G)[0][2] > 0)
+    p, rb = pieces_of(c, problems, total, G)[0][:2]
+    head = max(h for h in range(c) if range_begin(h, total, G) <= problems[p]["sb_base"] + rb * problems[p]["nsb"])
+
+    devs = [_dev(inp) for inp in inps]
+    outs = [torch.full((inp["M"], inp["N"]), 7.0, dtype=torch.float32, device="cuda") for inp in inps]
+    group = [(q, d, X, Y) for (q, d, X), Y in zip(devs, outs)]
+    ws = api.new_ws_q8_grouped_workspace()
+    api.ws_matvec_q8_grouped_debug(group, ws, withheld_cta=c, timeout_us=2000)
+    assert api.ws_matvec_status(ws) == api.DSPARK_ERR_TIMEOUT
+    lo, hi = rb * 128, min((rb + 1) * 128, inps[p]["N"])
+    for i, (inp, Y) in enumerate(zip(inps, outs)):
+        y = Y.cpu().numpy()
+        if i == p:
+            assert np.all(y[:, lo:hi] == 7.0), f"row block {rb} of problem {p} (finished by CTA {head}) was written"
+            ref = parity.oracle.ws_matvec_q8(inp["Wq8"], inp["X"])
+            keep = np.ones(inp["N"], bool)
+            keep[lo:hi] = False
+            ok, err, nbad = parity.within_tol(y[:, keep], ref[:, keep])
+            assert ok, (i, err, nbad)
+        else:
+            parity.check_ws_q8(inp, y32=y)
+    ws.zero_()
+    api.ws_matvec_q8_grouped(group, workspace=ws)
+    assert api.ws_matvec_status(ws) == 0
+    for inp, Y in zip(inps, outs):
+        parity.check_ws_q8(inp, y32=Y.cpu().numpy())
