@@ -9,7 +9,7 @@
 //
 // GB300 design
 //  * Work unit = (128 weight rows, a contiguous range of 64-wide k-blocks).  The split of K
-//    per row block (S units) and the CTAs per SM (1 with a 10-stage ring, 2 with 5 stages)
+//    per row block (S units) and the CTAs per SM (1 with a 10-stage ring, up to 3 with 4 stages)
 //    are chosen per shape so that one wave of CTAs covers every unit with the smallest
 //    largest load on any SM.
 //  * Warp 4 (one thread) streams, per k-block, the W tile [128 rows x 64 k] (16 KB) and
@@ -40,12 +40,13 @@ namespace dspark {
 namespace {
 
 constexpr int kThreads = 192;      // warps 0-3 epilogue, 4 TMA, 5 MMA + TMEM
-// Ring depth per launch: 10 x 18 KB stages with one CTA per SM, 5 stages with two (each SM
-// then overlaps one CTA's fixed costs with the other's stream; measured on the grouped
-// projections 53.0 -> 48.7 us, on a 151936 x 4096 matrix 187 -> 182 us), fewer when a
-// cluster's receive area needs the room.
+// Ring depth per launch: 10 x 18 KB stages with one CTA per SM; launches with more units than
+// SMs take 4 stages in 74 KB, so three CTAs fit on an SM and each SM overlaps one CTA's fixed
+// costs with the others' streams (measured on the grouped projections: one CTA per SM 53.0 us,
+// two with 5 stages 47.1 us, three with 4 stages 43.0 us, the last in one wave; on a
+// 151936 x 4096 matrix 187 / 184 / 180 us); fewer when a cluster's receive area needs the room.
 constexpr int kStagesSolo = 10;
-constexpr int kStagesShared = 5;
+constexpr int kStagesShared = 4;
 // Stages issued before the CTA barrier.  Issuing one stage (two TMA copies) takes the producing
 // thread ~0.2 us, so a whole first ring issued there holds the MMAs back for microseconds;
 // two are enough to cover the set-up (measured: single calls 0.4-0.8 us faster, others equal).
@@ -59,9 +60,13 @@ constexpr int kBBytes = kNPad * kKB * 2;         // 2 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 18 KB (multiple of 1024)
 constexpr uint32_t kTmemCols = 32;
 constexpr size_t kSmemSolo = 227 * 1024;         // per-CTA shared memory with one CTA per SM
-constexpr size_t kSmemShared = 113 * 1024;       // ... with two
+constexpr size_t kSmemShared = 74 * 1024;        // ... with up to three
 // dynamic shared memory: alignment slack, ring, cluster receive area, barriers and flags
 constexpr size_t smem_bytes_for(int nst, size_t recv) { return 1024 + size_t(nst) * kStageBytes + recv + 256; }
+// a grouped launch's unit 0 receives the other units' partial rows in its ring
+static_assert(size_t(kStagesShared) * kStageBytes >= size_t(kMaxSplit - 1) * kRowsPerUnit * kNPad * 4,
+              "the shared ring holds the partials of a split of kMaxSplit");
+static_assert(smem_bytes_for(kStagesShared, 0) <= kSmemShared, "the shared ring fits its budget");
 
 constexpr int kMaxProblems = 8;
 
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_matvec_tc_kernel(const __grid_
 
 struct Plan {
     int nrb, nkb, S;
-    int cps;  // CTAs per SM the split was sized for (1 or 2)
+    int cps;  // 1: split sized for one CTA per SM; 2: the shared ring, several CTAs per SM
 };
 
 // Receive area of a cluster launch: (S - 1) partial tiles of 128 rows x mcols fp32.
@@ -329,8 +334,8 @@ bool clusters_fit(int S, int cps, int M, int units);
 
 // The split of K: for S in {1, 2, 4, 8} units per row block with one CTA per SM, the largest
 // number of k-blocks any SM streams when every unit is resident in one wave; the smallest wins,
-// then the smaller S.  A shape with more row blocks than SMs runs unsplit with two CTAs per SM.
-// (Splits sized for two CTAs per SM were measured about 1 us faster alone on the 12288-row and
+// then the smaller S.  A shape with more row blocks than SMs runs unsplit with the shared ring
+// (up to three CTAs per SM).  (Splits sized for two CTAs per SM were measured about 1 us faster alone on the 12288-row and
 // 12288-wide projections, but their extra short units slowed the grouped launch of the four
 // projections, so they are not used.)  S is a power of two so that one cluster size serves
 // every problem of a grouped launch.  Whether the clusters fit is asked for the largest
@@ -554,8 +559,8 @@ dspark_status ws_enqueue_group(const dspark_ws_problem *probs, int n, void *work
         recv = csize > 1 ? recv_bytes_for(csize, g.prob[0].M) : 0;
         g.nst = stages_for(plans[0].cps, recv);
     } else {
-        // more units than SMs: two CTAs per SM with the shallower ring (unit 0 receives the
-        // partials in its ring, which holds (S - 1) x 128 x 16 fp32 even at S = 8)
+        // more units than SMs: the shallower ring, up to three CTAs per SM (unit 0 receives
+        // the partials in its ring, whose 72 KB hold (S - 1) x 128 x 16 fp32 even at S = 8)
         g.nst = units > static_cast<unsigned>(sms) ? kStagesShared : kStagesSolo;
     }
     if (csize > 1) {
