@@ -335,12 +335,12 @@ bool clusters_fit(int S, int cps, int M, int units);
 // The split of K: for S in {1, 2, 4, 8} units per row block with one CTA per SM, the largest
 // number of k-blocks any SM streams when every unit is resident in one wave; the smallest wins,
 // then the smaller S.  A shape with more row blocks than SMs runs unsplit with the shared ring
-// (up to three CTAs per SM).  (Splits sized for two CTAs per SM were measured about 1 us faster alone on the 12288-row and
-// 12288-wide projections, but their extra short units slowed the grouped launch of the four
-// projections, so they are not used.)  S is a power of two so that one cluster size serves
-// every problem of a grouped launch.  Whether the clusters fit is asked for the largest
-// receive area (M = 16), so the split depends on N and K only and a problem is split the same
-// way in a single and in a grouped launch.
+// (up to three CTAs per SM).  (Splits sized for two CTAs per SM were measured about 1 us faster
+// alone on the 12288-row and 12288-wide projections, but their extra short units slowed the
+// grouped launch of the four projections, so they are not used.)  S is a power of two so that
+// one cluster size serves every problem of a grouped launch.  Whether the clusters fit is
+// asked for the largest receive area (M = 16), so the split depends on N and K only and a
+// problem is split the same way in a single and in a grouped launch.
 Plan plan_for(int N, int K, int sms) {
     Plan p;
     p.nrb = (N + kRowsPerUnit - 1) / kRowsPerUnit;
