@@ -70,6 +70,7 @@ constexpr int kKS = 128;               // k per stage: 128 B of int8 per row (th
 constexpr int kBlocksPerStage = kKS / 32;   // 4 Q8_0 blocks
 constexpr int kSuper = 2;              // stages per 256-k superblock (8 scales of a row)
 constexpr int kStages = 10;            // shared-memory ring (even, so each stage parity keeps its slots)
+constexpr int kPreBarrierStages = 2;   // stages issued before the CTA-wide set-up
 constexpr int kMaxSplit = 8;           // units per row block (the portable cluster size)
 constexpr int kQBytes = kRows * kKS;                // 16 KB int8 tile
 constexpr int kXAtomBytes = kNPad * 64 * 2;         // 2 KB: 16 rows x 64 fp16
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) ws_q8_tc_kernel(const __grid_cons
         pdl_wait();  // no global-memory access before this point
         pol_q = l2_policy_evict_first();
         pol_x = l2_policy_evict_last();
-        produce(2);
+        produce(kPreBarrierStages);
     }
     if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
