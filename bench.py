@@ -745,6 +745,18 @@ def run_configs(dev, mk27, reps: int = 30):
     out["probe_latency_1_mapped_gate_c_abi"] = {"us_host_clock": stats(lat),
                                                 "how": "dspark_conf_probe through ctypes with prepared arguments, "
                                                        "gate stored into pinned host memory, host polls"}
+    # the same through the Python API's prepared call (api.ProbeCall.decide)
+    call = api.ProbeCall(wq, h1, pr["bias"], pr["threshold"], gate_out=g_map, stream=stream)
+    lat = []
+    for r in range(reps + 3):
+        t0 = time.perf_counter()
+        call.decide()
+        if r >= 3:
+            lat.append((time.perf_counter() - t0) * 1e6)
+    stream.synchronize()
+    out["probe_latency_1_probecall"] = {"us_host_clock": stats(lat),
+                                        "how": "api.ProbeCall.decide(): arguments marshalled once, gate stored "
+                                               "into pinned host memory, host polls"}
     for (K, N) in synth.WS_SHAPES:
         w = synth.ws_inputs(7, N, K)
         W = torch.from_numpy(w["W"].view(np.int16)).to(dev).view(torch.float16)

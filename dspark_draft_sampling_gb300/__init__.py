@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     DsparkError,
     GatedDraftPlan,
     MarkovPlan,
+    ProbeCall,
     conf_probe,
     conf_probe_host,
     conf_probe_split,

@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+import time
 
 import torch
 
@@ -376,6 +377,69 @@ def conf_probe(wq, hidden, bias: float, threshold: float, *, logit_out=None, gat
                                _stream(stream))
     _check(lib, st)
     return logit_out, gate_out
+
+
+class ProbeCall:
+    """Confidence probes prepared once for the latency path: the arguments are checked and
+    marshalled at construction, so each ``launch()`` is one C call (dspark_conf_probe).  With
+    ``gate_out`` in pinned host memory the kernel stores each 4-byte decision straight into
+    host memory, and ``decide()`` launches and polls those words: no copy and no stream
+    synchronization on the host path.  The tensors must stay alive and in place."""
+
+    _PENDING = 2  # never a decision: the kernel writes 1, 0, or -1 after a wait that gave up
+
+    def __init__(self, wq, hidden, bias: float, threshold: float, *, gate_out=None, logit_out=None,
+                 stream=None):
+        lib = load_library()
+        if hidden.dim() == 1:
+            hidden = hidden.view(1, -1)
+        n, K = hidden.shape
+        if wq.numel() != (K // 32) * 34:
+            raise ValueError("wq must hold K/32 Q8_0 blocks of 34 bytes")
+        if gate_out is None:
+            gate_out = torch.empty(n, dtype=torch.int32).pin_memory()
+        if gate_out.numel() < n:
+            raise ValueError("gate_out holds fewer than n decisions")
+        self.gate_out, self.logit_out, self.n = gate_out, logit_out, n
+        self._keep = (wq, hidden)
+        self._fn = lib.dspark_conf_probe
+        self._lib = lib
+        self._args = (_ptr(wq, "wq", dtypes=(torch.uint8, torch.int8)),
+                      _ptr(hidden, "hidden", dtypes=(torch.float32,)),
+                      ctypes.c_float(bias), ctypes.c_float(threshold), K, n,
+                      _ptr(logit_out, "logit_out", dtypes=(torch.float32,), allow_none=True),
+                      _ptr(gate_out, "gate_out", dtypes=(torch.int32,), allow_pinned=True),
+                      _stream(stream))
+        self._stream = stream
+        self._gates = None if gate_out.is_cuda else gate_out.numpy()
+
+    def launch(self):
+        st = self._fn(*self._args)
+        if st != DSPARK_OK:
+            _check(self._lib, st)
+
+    def decide(self, timeout_s: float = 1.0):
+        """Launch and wait for the decisions in pinned host memory; returns them as a numpy
+        int32 array (1: keep drafting, 0: stop, -1: the kernel gave up a wait).  After
+        ``timeout_s`` the stream is synchronized and its error, if any, raised."""
+        g = self._gates
+        if g is None:
+            raise ValueError("decide() needs gate_out in pinned host memory")
+        n, pending = self.n, self._PENDING
+        g[:n] = pending
+        self.launch()
+        t0 = time.perf_counter()
+        i = 0  # the probes' stores land in any order; a word stays set once written
+        while i < n:
+            if g[i] != pending:
+                i += 1
+                continue
+            if time.perf_counter() - t0 > timeout_s:
+                (self._stream or torch.cuda.current_stream()).synchronize()
+                if (g[:n] == pending).any():
+                    raise DsparkError(DSPARK_ERR_TIMEOUT, "probe decisions did not arrive")
+                break
+        return g[:n].copy()
 
 
 def conf_probe_split(wq, hidden, state, bias: float, threshold: float, *, logit_out=None,

@@ -148,3 +148,27 @@ def test_large_batch_ring_matches_small_batches_bitwise(split):
         assert torch.equal(z.view(torch.int32), z_big[lo:lo + 64].view(torch.int32)), lo
         assert torch.equal(g, g_big[lo:lo + 64]), lo
     parity.check_probe(inp, z_big.cpu().numpy(), g_big.cpu().numpy())
+
+
+def test_prepared_probe_call_decides_like_the_oracle():
+    """api.ProbeCall: arguments marshalled once; decide() launches and polls the decisions the
+    kernel stores into pinned host memory, call after call, as the oracle decides them."""
+    inp = synth.probe_inputs(5, 7424, seed=12)
+    wq = torch.from_numpy(inp["wq"]).cuda()
+    hid = torch.from_numpy(inp["hidden"]).cuda()
+    _, go = parity.oracle.conf_probe(inp["wq"], inp["hidden"], inp["bias"], 0.5)
+    z = torch.empty(5, dtype=torch.float32, device="cuda")
+    call = api.ProbeCall(wq, hid, inp["bias"], 0.5, logit_out=z)
+    for _ in range(3):
+        np.testing.assert_array_equal(call.decide(), go)
+    torch.cuda.synchronize()
+    parity.check_probe(inp, z.cpu().numpy(), go)
+    one = api.ProbeCall(wq, hid[0], inp["bias"], 0.5)  # a single probe: one 4-byte decision
+    assert one.decide().tolist() == [int(go[0])]
+    dev_gate = torch.empty(5, dtype=torch.int32, device="cuda")
+    on_device = api.ProbeCall(wq, hid, inp["bias"], 0.5, gate_out=dev_gate)
+    on_device.launch()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dev_gate.cpu().numpy(), go)
+    with pytest.raises(ValueError):
+        on_device.decide()
